@@ -1,0 +1,239 @@
+"""ctypes binding of libattn_sink.so.
+
+``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_bwd_workspace_size``,
+``attn_sink_status_string`` and ``attn_sink_device_error`` mirror the C entry
+points of ``include/attn_sink.h`` one to one: they only turn tensors into
+device pointers and return the library's status.  ``forward``, ``backward``
+and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
+the workspace with torch and raise on a non-zero status.  Every step of the
+computation runs in the library's CUDA kernels; there is no other code path,
+and loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+from .build import LIB_PATH, INCLUDE
+
+c_int, c_float, c_void_p, c_size_t = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+ATTN_SINK_OK = 0
+STATUS_NAMES = {0: "ATTN_SINK_OK", 1: "ATTN_SINK_ERR_INVALID_ARG", 2: "ATTN_SINK_ERR_UNSUPPORTED",
+                3: "ATTN_SINK_ERR_WORKSPACE", 4: "ATTN_SINK_ERR_CUDA", 5: "ATTN_SINK_ERR_TIMEOUT"}
+
+
+class AttnSinkParams(ctypes.Structure):
+    """Mirror of ``attn_sink_params`` in include/attn_sink.h (field order matters)."""
+    _fields_ = [
+        ("batch", c_int), ("seqlen_q", c_int), ("seqlen_k", c_int),
+        ("num_seqs", c_int), ("total_q", c_int), ("total_k", c_int),
+        ("max_seqlen_q", c_int), ("max_seqlen_k", c_int),
+        ("heads_q", c_int), ("heads_kv", c_int), ("head_dim", c_int),
+        ("causal", c_int), ("window", c_int), ("softmax_scale", c_float),
+        ("grad_dtype", c_int),
+    ]
+
+
+class AttnSinkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({attn_sink_status_string(status)})")
+
+
+_LIB = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/attn_sink.h declares."""
+    text = open(os.path.join(INCLUDE, "attn_sink.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(attn_sink_\w+)\s*\(", text, flags=re.M)
+
+
+def lib():
+    """Load libattn_sink.so (built in-tree by ``build.build()``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(AttnSinkParams)
+    L.attn_sink_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_void_p]
+    L.attn_sink_fwd.restype = c_int
+    L.attn_sink_bwd_workspace_size.argtypes = [P]
+    L.attn_sink_bwd_workspace_size.restype = c_size_t
+    L.attn_sink_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_void_p, c_void_p, c_size_t, c_void_p]
+    L.attn_sink_bwd.restype = c_int
+    L.attn_sink_status_string.argtypes = [c_int]
+    L.attn_sink_status_string.restype = ctypes.c_char_p
+    L.attn_sink_device_error.argtypes = [c_void_p, ctypes.POINTER(c_int)]
+    L.attn_sink_device_error.restype = c_int
+    _LIB = L
+    return L
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _pref(params):
+    return None if params is None else ctypes.byref(params)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------------------- C entry points
+def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse,
+                  stream=None) -> int:
+    return lib().attn_sink_fwd(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out), _ptr(lse),
+                               _stream(stream))
+
+
+def attn_sink_bwd_workspace_size(params: AttnSinkParams) -> int:
+    return int(lib().attn_sink_bwd_workspace_size(_pref(params)))
+
+
+def attn_sink_bwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse,
+                  dout, dq, dk, dv, dsink, workspace, workspace_bytes: int, stream=None) -> int:
+    return lib().attn_sink_bwd(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out), _ptr(lse),
+                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dsink),
+                               _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_sink_status_string(status: int) -> str:
+    return lib().attn_sink_status_string(int(status)).decode()
+
+
+def attn_sink_device_error(stream=None) -> tuple[int, int]:
+    code = c_int(0)
+    st = lib().attn_sink_device_error(_stream(stream), ctypes.byref(code))
+    return st, code.value
+
+
+# ----------------------------------------------------------------------------- conveniences
+def make_params(q_shape, k_shape, *, causal: bool, window: int, softmax_scale: float | None,
+                num_seqs: int | None = None, max_seqlen_q: int | None = None,
+                max_seqlen_k: int | None = None, grad_dtype: int = 0) -> AttnSinkParams:
+    """Params from tensor shapes: q [B, N, H, d] (dense) or [T, H, d] (packed;
+    then num_seqs and max_seqlen_* are required)."""
+    p = AttnSinkParams()
+    d = int(q_shape[-1])
+    p.head_dim = d
+    p.heads_q = int(q_shape[-2])
+    p.heads_kv = int(k_shape[-2])
+    p.causal = int(bool(causal))
+    p.window = int(window)
+    p.softmax_scale = float(softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(d))
+    p.grad_dtype = int(grad_dtype)
+    if len(q_shape) == 4:
+        p.batch, p.seqlen_q, p.seqlen_k = int(q_shape[0]), int(q_shape[1]), int(k_shape[1])
+    else:
+        if num_seqs is None or max_seqlen_q is None or max_seqlen_k is None:
+            raise ValueError("packed inputs need num_seqs and max_seqlen_q / max_seqlen_k")
+        p.num_seqs = int(num_seqs)
+        p.total_q, p.total_k = int(q_shape[0]), int(k_shape[0])
+        p.max_seqlen_q, p.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
+    return p
+
+
+def _check(status: int, where: str):
+    if status != ATTN_SINK_OK:
+        raise AttnSinkError(status, where)
+
+
+def _lse_len(q) -> int:
+    return q.shape[0] * q.shape[1] if q.dim() == 4 else q.shape[0]
+
+
+def forward(q, k, v, sink, *, causal: bool = True, window: int = 0,
+            softmax_scale: float | None = None, cu_seqlens_q=None, cu_seqlens_k=None,
+            max_seqlen_q: int | None = None, max_seqlen_k: int | None = None, stream=None):
+    """out (like q, bf16) and lse ([H_q, T_q] fp32)."""
+    num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
+                    num_seqs=num_seqs, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[-2], _lse_len(q)), dtype=torch.float32, device=q.device)
+    _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse, stream),
+           "attn_sink_fwd")
+    return out, lse
+
+
+def backward(q, k, v, sink, out, lse, dout, *, causal: bool = True, window: int = 0,
+             softmax_scale: float | None = None, cu_seqlens_q=None, cu_seqlens_k=None,
+             max_seqlen_q: int | None = None, max_seqlen_k: int | None = None,
+             grad_dtype: int = 0, workspace=None, stream=None):
+    """dq, dk, dv (bf16, or fp32 when grad_dtype = 1) and dsink ([H_q] fp32)."""
+    num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
+                    num_seqs=num_seqs, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                    grad_dtype=grad_dtype)
+    gd = torch.float32 if grad_dtype == 1 else torch.bfloat16
+    dq = torch.empty(q.shape, dtype=gd, device=q.device)
+    dk = torch.empty(k.shape, dtype=gd, device=q.device)
+    dv = torch.empty(v.shape, dtype=gd, device=q.device)
+    dsink = torch.empty_like(sink)
+    nbytes = attn_sink_bwd_workspace_size(p)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(attn_sink_bwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse, dout, dq, dk,
+                         dv, dsink, workspace, workspace.numel(), stream), "attn_sink_bwd")
+    return dq, dk, dv, dsink
+
+
+class AttnSinkFunction(torch.autograd.Function):
+    """Autograd wrapper: forward and backward both run in libattn_sink.so."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, sink, causal, window, softmax_scale, cu_seqlens_q, cu_seqlens_k,
+                max_seqlen_q, max_seqlen_k):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        sink32 = sink.detach().float().contiguous()
+        out, lse = forward(q, k, v, sink32, causal=causal, window=window,
+                           softmax_scale=softmax_scale, cu_seqlens_q=cu_seqlens_q,
+                           cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
+                           max_seqlen_k=max_seqlen_k)
+        ctx.save_for_backward(q, k, v, sink32, out, lse, cu_seqlens_q, cu_seqlens_k)
+        ctx.cfg = (causal, window, softmax_scale, max_seqlen_q, max_seqlen_k, sink.dtype)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, sink32, out, lse, cu_q, cu_k = ctx.saved_tensors
+        causal, window, scale, mq, mk, sink_dtype = ctx.cfg
+        dq, dk, dv, dsink = backward(q, k, v, sink32, out, lse, dout.contiguous(), causal=causal,
+                                     window=window, softmax_scale=scale, cu_seqlens_q=cu_q,
+                                     cu_seqlens_k=cu_k, max_seqlen_q=mq, max_seqlen_k=mk)
+        return dq, dk, dv, dsink.to(sink_dtype), None, None, None, None, None, None, None
+
+
+def attn_sink(q, k, v, sink, *, causal: bool = True, window: int = 0,
+              softmax_scale: float | None = None, cu_seqlens_q=None, cu_seqlens_k=None,
+              max_seqlen_q: int | None = None, max_seqlen_k: int | None = None):
+    """Differentiable attention with a learnable per-head sink (bf16 q/k/v)."""
+    return AttnSinkFunction.apply(q, k, v, sink, causal, window, softmax_scale, cu_seqlens_q,
+                                  cu_seqlens_k, max_seqlen_q, max_seqlen_k)

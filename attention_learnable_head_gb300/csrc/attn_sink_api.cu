@@ -1,0 +1,415 @@
+// Host side of libattn_sink.so: argument validation, TMA tensor-map encoding,
+// launch configuration and workspace carving for the C ABI in attn_sink.h.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_sink.h"
+#include "bwd_kernel.cuh"
+#include "fwd_kernel.cuh"
+
+// Device word a kernel sets when it gives up on a bounded wait.
+__device__ int g_attn_sink_device_error = 0;
+
+namespace {
+
+using namespace attn_sink;
+
+constexpr int kMaxDevices = 64;
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+std::mutex g_dev_mutex;
+int g_sm_count[kMaxDevices] = {0};
+int* g_err_ptr[kMaxDevices] = {nullptr};
+bool g_attr_set[kMaxDevices] = {false};
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Per-device state: SM count, address of the error word, kernel attributes.
+int device_state(int* sm_count, int** err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return ATTN_SINK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return ATTN_SINK_ERR_CUDA;
+    void* e = nullptr;
+    if (cudaGetSymbolAddress(&e, g_attn_sink_device_error) != cudaSuccess)
+      return ATTN_SINK_ERR_CUDA;
+    g_sm_count[dev] = n;
+    g_err_ptr[dev] = static_cast<int*>(e);
+  }
+  if (!g_attr_set[dev]) {
+    if (cudaFuncSetAttribute(attn_sink_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kFwdSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_sink_bwd_main_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBwdSmemBytes) != cudaSuccess)
+      return ATTN_SINK_ERR_CUDA;
+    g_attr_set[dev] = true;
+  }
+  *sm_count = g_sm_count[dev];
+  *err = g_err_ptr[dev];
+  return ATTN_SINK_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Problem geometry resolved from the params (dense or packed).
+struct Geometry {
+  bool varlen;
+  int num_seqs;
+  int total_q, total_k;
+  int max_q, max_k;
+  int group;
+};
+
+int validate(const attn_sink_params* p, const int* cu_q, const int* cu_k, Geometry* g) {
+  if (p == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
+  if (p->head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
+  if (p->heads_q <= 0 || p->heads_kv <= 0 || p->heads_q % p->heads_kv != 0)
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return ATTN_SINK_ERR_INVALID_ARG;
+  if (p->window > 0 && !p->causal) return ATTN_SINK_ERR_INVALID_ARG;
+  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale > 0.0f))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (p->grad_dtype != 0 && p->grad_dtype != 1) return ATTN_SINK_ERR_INVALID_ARG;
+  if ((cu_q == nullptr) != (cu_k == nullptr)) return ATTN_SINK_ERR_INVALID_ARG;
+  // One mode at a time: packed (cu_seqlens given, batch = 0) or dense (num_seqs = 0).
+  if (cu_q == nullptr && p->num_seqs > 0) return ATTN_SINK_ERR_INVALID_ARG;
+  if (cu_q != nullptr && p->batch > 0) return ATTN_SINK_ERR_INVALID_ARG;
+  g->varlen = cu_q != nullptr;
+  g->group = p->heads_q / p->heads_kv;
+  if (g->varlen) {
+    if (p->num_seqs < 0 || p->total_q < 0 || p->total_k < 0 || p->max_seqlen_q < 0 ||
+        p->max_seqlen_k < 0)
+      return ATTN_SINK_ERR_INVALID_ARG;
+    if (p->num_seqs > 0 && (p->max_seqlen_q > p->total_q || p->max_seqlen_k > p->total_k))
+      return ATTN_SINK_ERR_INVALID_ARG;
+    g->num_seqs = p->num_seqs;
+    g->total_q = p->total_q;
+    g->total_k = p->total_k;
+    g->max_q = p->max_seqlen_q;
+    g->max_k = p->max_seqlen_k;
+  } else {
+    if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_k < 0) return ATTN_SINK_ERR_INVALID_ARG;
+    const long long tq = (long long)p->batch * p->seqlen_q;
+    const long long tk = (long long)p->batch * p->seqlen_k;
+    if (tq > INT32_MAX || tk > INT32_MAX) return ATTN_SINK_ERR_INVALID_ARG;
+    g->num_seqs = p->batch;
+    g->total_q = (int)tq;
+    g->total_k = (int)tk;
+    g->max_q = p->seqlen_q;
+    g->max_k = p->seqlen_k;
+  }
+  // Launch-grid limits (sequences in grid.y, tiles in grid.z).
+  if (g->num_seqs > 65535) return ATTN_SINK_ERR_UNSUPPORTED;
+  if ((g->max_q + kBlockM - 1) / kBlockM > 65535 || (g->max_k + kBlockN - 1) / kBlockN > 65535)
+    return ATTN_SINK_ERR_UNSUPPORTED;
+  return ATTN_SINK_OK;
+}
+
+int encode_rows(CUtensorMap* m, const void* ptr, int tokens, int heads) {
+  if (!load_encode()) return ATTN_SINK_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kBlockM};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// How many CTAs share one (kv head, key tile) in the backward pass.  Splitting
+// the GQA group shortens the longest CTA when there are too few key tiles to
+// fill the GPU; the split partials are summed in a fixed order afterwards.
+int choose_split(const attn_sink_params* p, const Geometry& g, int sm_count) {
+  const int qt = (g.max_q + kBlockM - 1) / kBlockM;
+  const int kt = (g.max_k + kBlockN - 1) / kBlockN;
+  if (qt == 0 || kt == 0 || g.num_seqs == 0) return 1;
+  double total, longest;           // in units of (query head, query tile, key tile) steps
+  int q_per_key;                   // query tiles a key tile meets at most
+  if (p->causal && p->window > 0) {
+    q_per_key = std::min(qt, (p->window + kBlockM - 1) / kBlockM + 1);
+    total = (double)g.num_seqs * p->heads_q * qt * q_per_key;
+  } else if (p->causal) {
+    q_per_key = qt;
+    total = (double)g.num_seqs * p->heads_q * qt * (kt + 1) * 0.5;
+  } else {
+    q_per_key = qt;
+    total = (double)g.num_seqs * p->heads_q * qt * kt;
+  }
+  int split = 1;
+  while (split < g.group && g.group % (split * 2) == 0) {
+    longest = (double)(g.group / split) * q_per_key;
+    if (longest * sm_count * 2.0 <= total) break;
+    split *= 2;
+  }
+  return split;
+}
+
+struct BwdLayout {
+  size_t off_D, off_part, off_dq, off_dk, off_dv, total;
+  int n_blocks;
+  int split;
+};
+
+BwdLayout bwd_layout(const attn_sink_params* p, const Geometry& g, int sm_count) {
+  BwdLayout L;
+  L.n_blocks = (g.total_q + kPreRows - 1) / kPreRows;
+  L.split = choose_split(p, g, sm_count);
+  size_t off = 0;
+  L.off_D = off;
+  off += align256((size_t)p->heads_q * g.total_q * sizeof(float));
+  L.off_part = off;
+  off += align256((size_t)p->heads_q * std::max(L.n_blocks, 1) * sizeof(float));
+  L.off_dq = off;
+  if (p->grad_dtype == 0) off += align256((size_t)g.total_q * p->heads_q * kHeadDim * sizeof(float));
+  const size_t kv_part = (size_t)L.split * g.total_k * p->heads_kv * kHeadDim * sizeof(float);
+  L.off_dk = off;
+  if (L.split > 1) off += align256(kv_part);
+  L.off_dv = off;
+  if (L.split > 1) off += align256(kv_part);
+  L.total = off;
+  return L;
+}
+
+int sm_count_or_default() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  cudaGetLastError();
+  return 148;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_sink_status_string(int status) {
+  switch (status) {
+    case ATTN_SINK_OK: return "ok";
+    case ATTN_SINK_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_SINK_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_SINK_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_SINK_ERR_CUDA: return "CUDA error";
+    case ATTN_SINK_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
+                  const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  void* out, float* lse, void* stream) {
+  Geometry g;
+  int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
+  if (st != ATTN_SINK_OK) return st;
+  if (g.num_seqs == 0 || g.total_q == 0) return ATTN_SINK_OK;   // nothing to compute
+  if (q == nullptr || sink == nullptr || out == nullptr || lse == nullptr)
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (g.total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_SINK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  int sms = 0;
+  int* err = nullptr;
+  if ((st = device_state(&sms, &err)) != ATTN_SINK_OK) return st;
+
+  FwdParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  // An empty key tensor is never read (every tile has no key); its map only
+  // needs a valid address.
+  const void* kp = g.total_k > 0 ? k : q;
+  const void* vp = g.total_k > 0 ? v : q;
+  const int tk = g.total_k > 0 ? g.total_k : 1;
+  const int hk = g.total_k > 0 ? params->heads_kv : 1;
+  if ((st = encode_rows(&fp.tm_q, q, g.total_q, params->heads_q)) != ATTN_SINK_OK) return st;
+  if ((st = encode_rows(&fp.tm_k, kp, tk, hk)) != ATTN_SINK_OK) return st;
+  if ((st = encode_rows(&fp.tm_v, vp, tk, hk)) != ATTN_SINK_OK) return st;
+  fp.cu_q = cu_seqlens_q;
+  fp.cu_k = cu_seqlens_k;
+  fp.sink = sink;
+  fp.out = static_cast<__nv_bfloat16*>(out);
+  fp.lse = lse;
+  fp.err = err;
+  fp.seqlen_q = g.varlen ? 0 : params->seqlen_q;
+  fp.seqlen_k = g.varlen ? 0 : params->seqlen_k;
+  fp.total_q = g.total_q;
+  fp.heads_q = params->heads_q;
+  fp.group = g.group;
+  fp.causal = params->causal;
+  fp.window = params->window > 0 ? params->window : 0;
+  fp.scale_log2 = params->softmax_scale * kLog2e;
+  fp.n_qtiles = (g.max_q + kBlockM - 1) / kBlockM;
+  if (fp.n_qtiles == 0) return ATTN_SINK_OK;
+  dim3 grid(params->heads_q, g.num_seqs, fp.n_qtiles);
+  attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
+  return cudaGetLastError() == cudaSuccess ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
+size_t attn_sink_bwd_workspace_size(const attn_sink_params* params) {
+  if (params == nullptr) return 0;
+  // Packed fields are used when num_seqs > 0, the dense fields otherwise.
+  static const int kMarker = 0;
+  const bool packed = params->num_seqs > 0;
+  Geometry g;
+  if (validate(params, packed ? &kMarker : nullptr, packed ? &kMarker : nullptr, &g) !=
+      ATTN_SINK_OK)
+    return 0;
+  return bwd_layout(params, g, sm_count_or_default()).total;
+}
+
+int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
+                  const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                  void* dv, float* dsink, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  Geometry g;
+  int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
+  if (st != ATTN_SINK_OK) return st;
+  if (sink == nullptr || dsink == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
+  if (g.total_q > 0 && (q == nullptr || out == nullptr || lse == nullptr || dout == nullptr ||
+                        dq == nullptr))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (g.total_k > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  int sms = 0;
+  int* err = nullptr;
+  if ((st = device_state(&sms, &err)) != ATTN_SINK_OK) return st;
+  const BwdLayout L = bwd_layout(params, g, sms);
+  if (L.total > 0 && (workspace == nullptr || workspace_bytes < L.total ||
+                      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return ATTN_SINK_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* D = reinterpret_cast<float*>(ws + L.off_D);
+  float* partials = reinterpret_cast<float*>(ws + L.off_part);
+  float* dq_acc = params->grad_dtype == 1 ? static_cast<float*>(dq)
+                                          : reinterpret_cast<float*>(ws + L.off_dq);
+  const float scale = params->softmax_scale;
+
+  // 1. D, dsink partials, zero the dq accumulator
+  if (g.total_q > 0) {
+    PreParams pp;
+    pp.out = static_cast<const __nv_bfloat16*>(out);
+    pp.dout = static_cast<const __nv_bfloat16*>(dout);
+    pp.lse = lse;
+    pp.sink = sink;
+    pp.D = D;
+    pp.partials = partials;
+    pp.dq_acc = dq_acc;
+    pp.total_q = g.total_q;
+    pp.heads_q = params->heads_q;
+    pp.n_blocks = L.n_blocks;
+    attn_sink_bwd_pre_kernel<<<dim3(L.n_blocks, params->heads_q), 256, 0, s>>>(pp);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+  }
+  // 2. main loop: dK, dV (and their split partials), dQ accumulation
+  const int n_ktiles = (g.max_k + kBlockN - 1) / kBlockN;
+  if (g.total_k > 0 && g.num_seqs > 0 && n_ktiles > 0) {
+    BwdParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    const void* qp = g.total_q > 0 ? q : k;
+    const void* op = g.total_q > 0 ? dout : k;
+    const int tq = g.total_q > 0 ? g.total_q : 1;
+    const int hq = g.total_q > 0 ? params->heads_q : 1;
+    if ((st = encode_rows(&bp.tm_q, qp, tq, hq)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&bp.tm_do, op, tq, hq)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&bp.tm_k, k, g.total_k, params->heads_kv)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&bp.tm_v, v, g.total_k, params->heads_kv)) != ATTN_SINK_OK) return st;
+    bp.cu_q = cu_seqlens_q;
+    bp.cu_k = cu_seqlens_k;
+    bp.lse = lse;
+    bp.D = D;
+    bp.dq_acc = dq_acc;
+    bp.dk = dk;
+    bp.dv = dv;
+    bp.dk_part = reinterpret_cast<float*>(ws + L.off_dk);
+    bp.dv_part = reinterpret_cast<float*>(ws + L.off_dv);
+    bp.err = err;
+    bp.seqlen_q = g.varlen ? 0 : params->seqlen_q;
+    bp.seqlen_k = g.varlen ? 0 : params->seqlen_k;
+    bp.total_q = g.total_q;
+    bp.total_k = g.total_k;
+    bp.heads_q = params->heads_q;
+    bp.heads_kv = params->heads_kv;
+    bp.group = g.group;
+    bp.split = L.split;
+    bp.causal = params->causal;
+    bp.window = params->window > 0 ? params->window : 0;
+    bp.scale = scale;
+    bp.scale_log2 = scale * kLog2e;
+    bp.n_ktiles = n_ktiles;
+    bp.grad_fp32 = params->grad_dtype;
+    dim3 grid(params->heads_kv * L.split, g.num_seqs, n_ktiles);
+    attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+    if (L.split > 1) {
+      const size_t n4 = (size_t)g.total_k * params->heads_kv * kHeadDim / 4;
+      const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)sms * 8);
+      attn_sink_dkdv_reduce_kernel<<<blocks, 256, 0, s>>>(bp.dk_part, bp.dv_part, L.split, n4,
+                                                          scale, dk, dv, params->grad_dtype);
+      if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+    }
+  }
+  // 3. dq (bf16) from the fp32 accumulator
+  if (g.total_q > 0 && params->grad_dtype == 0) {
+    const size_t n8 = (size_t)g.total_q * params->heads_q * kHeadDim / 8;
+    const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
+    attn_sink_dq_convert_kernel<<<blocks, 256, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
+                                                       n8);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+  }
+  // 4. dsink
+  if (g.total_q > 0) {
+    attn_sink_dsink_reduce_kernel<<<params->heads_q, 256, 0, s>>>(partials, L.n_blocks, dsink);
+  } else {
+    if (cudaMemsetAsync(dsink, 0, sizeof(float) * params->heads_q, s) != cudaSuccess)
+      return ATTN_SINK_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
+int attn_sink_device_error(void* stream, int* code) {
+  if (code == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
+  *code = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_SINK_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_attn_sink_device_error, sizeof(int)) != cudaSuccess)
+    return ATTN_SINK_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_attn_sink_device_error, &zero, sizeof(int)) != cudaSuccess)
+      return ATTN_SINK_ERR_CUDA;
+  }
+  *code = v;
+  return ATTN_SINK_OK;
+}
+
+}  // extern "C"

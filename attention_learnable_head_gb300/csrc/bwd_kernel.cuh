@@ -1,0 +1,524 @@
+// Backward kernels: attention with a per-head sink, sm_103a.
+//
+//   bwd_pre     D_i = sum_d dout_i[d] * out_i[d] (fp32, from the stored bf16 out),
+//               per-block partials of dsink[h] = -sum_i exp(sink[h] - lse_i) * D_i
+//               (the sink gradient of section "反向传播" on the euno.news page:
+//               P_ih = exp(sink[h] - lse_i) because lse includes the sink), and
+//               zeroes the fp32 dq accumulator.
+//   bwd_main    key/value-stationary: one CTA per (kv head, sequence, 128 keys).
+//               Loops over the query heads of the GQA group and the query tiles
+//               that can see these keys; per step five tcgen05 MMAs:
+//                 S^T  = K Q^T        dP^T = V dO^T            (TMEM, fp32)
+//                 P^T  = exp(S^T * scale - lse)  dS^T = P^T o (dP^T - D)
+//                 dV  += P^T dO       (A = P^T from TMEM)
+//                 dK  += dS^T Q       (A = dS^T from SMEM, K-major)
+//                 dQ   = dS K         (A = dS^T from SMEM read MN-major)
+//               dK and dV stay in TMEM for the whole loop; dQ is added into the
+//               fp32 accumulator with vector atomics by a dedicated warpgroup.
+//   dsink_reduce  fixed-order tree over the partials (bitwise reproducible).
+//   dq_convert  fp32 accumulator -> bf16 dq.
+#pragma once
+#include <cuda_bf16.h>
+#include "sm103_ptx.cuh"
+#include "fwd_kernel.cuh"
+
+namespace attn_sink {
+
+constexpr int kBwdStages = 2;
+constexpr int kBwdThreads = 320;   // warps 0-3 compute, 4 TMA, 5 MMA, 6-9 dQ
+constexpr int kPreRows = 128;      // rows per bwd_pre CTA
+constexpr int kBwdSmemBytes =
+    1024 + 2 * (int)kTileBytes + kBwdStages * 2 * (int)kTileBytes + (int)kPTileBytes;
+
+// TMEM columns of bwd_main
+constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
+                   kColPT = 448;
+
+struct BwdParams {
+  CUtensorMap tm_q;    // [T_q][H_q][64]
+  CUtensorMap tm_do;   // [T_q][H_q][64]
+  CUtensorMap tm_k;    // [T_k][H_kv][64]
+  CUtensorMap tm_v;
+  const int* cu_q;
+  const int* cu_k;
+  const float* lse;    // [H_q][T_q]
+  const float* D;      // [H_q][T_q]
+  float* dq_acc;       // [T_q][H_q][64] fp32, pre-zeroed
+  void* dk;            // [T_k][H_kv][64] bf16 or fp32 (split == 1)
+  void* dv;
+  float* dk_part;      // [split][T_k][H_kv][64] fp32 partials (split > 1)
+  float* dv_part;
+  int* err;
+  int seqlen_q, seqlen_k;
+  int total_q, total_k;
+  int heads_q, heads_kv, group;
+  int split;           // CTAs sharing one (kv head, key tile); each takes group/split q heads
+  int causal, window;
+  float scale;         // softmax_scale
+  float scale_log2;    // softmax_scale * log2(e)
+  int n_ktiles;        // key tiles of the longest sequence
+  int grad_fp32;
+};
+
+// ------------------------------------------------------------------ bwd_pre
+struct PreParams {
+  const __nv_bfloat16* out;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  const float* sink;
+  float* D;            // [H_q][T_q]
+  float* partials;     // [H_q][n_blocks]
+  float* dq_acc;       // [T_q][H_q][64]
+  int total_q, heads_q, n_blocks;
+};
+
+__global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams p) {
+  const int h = blockIdx.y;
+  const int blk = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int sub = tid & 7;          // 16-byte slice of the 128-byte row
+  const int rloc = tid >> 3;        // 0..31
+  const float sink_h = p.sink[h];
+  float acc = 0.0f;                 // dsink contribution of this thread's rows
+  #pragma unroll 1
+  for (int pass = 0; pass < kPreRows / 32; ++pass) {
+    const int t = blk * kPreRows + pass * 32 + rloc;
+    float d = 0.0f;
+    if (t < p.total_q) {
+      const size_t base = ((size_t)t * p.heads_q + h) * kHeadDim + sub * 8;
+      const uint4 o = *reinterpret_cast<const uint4*>(p.out + base);
+      const uint4 g = *reinterpret_cast<const uint4*>(p.dout + base);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 a = __bfloat1622float2(o2[u]);
+        const float2 b = __bfloat1622float2(g2[u]);
+        d = fmaf(a.x, b.x, d);
+        d = fmaf(a.y, b.y, d);
+      }
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + base);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 4);
+    if (sub == 0 && t < p.total_q) {
+      p.D[(size_t)h * p.total_q + t] = d;
+      const float lse = p.lse[(size_t)h * p.total_q + t];
+      // P_ih = exp(sink - lse); zero when the sink is -inf.
+      if (sink_h > -INFINITY && lse > -INFINITY)
+        acc -= ex2_approx((sink_h - lse) * kLog2e) * d;
+    }
+  }
+  // fixed-order reduction: lanes (xor tree), then warps in index order
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  __shared__ float wsum[8];
+  if ((tid & 31) == 0) wsum[tid >> 5] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.0f;
+    #pragma unroll
+    for (int w = 0; w < 8; ++w) s += wsum[w];
+    p.partials[(size_t)h * p.n_blocks + blk] = s;
+  }
+}
+
+// ------------------------------------------------------------------ dsink_reduce
+__global__ void __launch_bounds__(256) attn_sink_dsink_reduce_kernel(const float* partials,
+                                                                     int n_blocks,
+                                                                     float* dsink) {
+  const int h = blockIdx.x;
+  const int tid = threadIdx.x;
+  float s = 0.0f;
+  for (int j = tid; j < n_blocks; j += 256) s += partials[(size_t)h * n_blocks + j];
+  #pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  __shared__ float wsum[8];
+  if ((tid & 31) == 0) wsum[tid >> 5] = s;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.0f;
+    #pragma unroll
+    for (int w = 0; w < 8; ++w) t += wsum[w];
+    dsink[h] = t;
+  }
+}
+
+// ------------------------------------------------------------------ dq_convert
+__global__ void __launch_bounds__(256) attn_sink_dq_convert_kernel(const float* acc,
+                                                                   __nv_bfloat16* dq,
+                                                                   size_t n8) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                                 pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
+}
+
+// ------------------------------------------------------------------ dkdv_reduce
+// dK = scale * sum_s dk_part[s], dV = sum_s dv_part[s], in a fixed order
+// (s = 0, 1, ...), so the result is bitwise reproducible.
+__global__ void __launch_bounds__(256) attn_sink_dkdv_reduce_kernel(
+    const float* dk_part, const float* dv_part, int split, size_t n4, float scale, void* dk,
+    void* dv, int grad_fp32) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    #pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const float4* src = reinterpret_cast<const float4*>(which == 0 ? dk_part : dv_part);
+      float4 a = src[i];
+      for (int s = 1; s < split; ++s) {
+        const float4 b = src[(size_t)s * n4 + i];
+        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      }
+      const float mul = which == 0 ? scale : 1.0f;
+      a.x *= mul; a.y *= mul; a.z *= mul; a.w *= mul;
+      void* dst = which == 0 ? dk : dv;
+      if (grad_fp32)
+        reinterpret_cast<float4*>(dst)[i] = a;
+      else
+        reinterpret_cast<uint2*>(dst)[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ bwd_main
+// Store one 64-wide row of dK (which = 0) or dV (which = 1) for key `row`:
+// the final output (times `mul`) when the GQA group is not split, else this
+// CTA's fp32 partial (unscaled; the reduction applies the scale).
+__device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, size_t row,
+                                                  int g, int which, const float* v, float mul) {
+  const size_t base = (row * p.heads_kv + g) * kHeadDim;
+  if (p.split > 1) {
+    float* dst = (which == 0 ? p.dk_part : p.dv_part) +
+                 (size_t)part * p.total_k * p.heads_kv * kHeadDim + base;
+    #pragma unroll
+    for (int u = 0; u < kHeadDim / 4; ++u)
+      reinterpret_cast<float4*>(dst)[u] =
+          make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+  } else if (p.grad_fp32) {
+    float* dst = reinterpret_cast<float*>(which == 0 ? p.dk : p.dv) + base;
+    #pragma unroll
+    for (int u = 0; u < kHeadDim / 4; ++u)
+      reinterpret_cast<float4*>(dst)[u] = make_float4(v[4 * u] * mul, v[4 * u + 1] * mul,
+                                                      v[4 * u + 2] * mul, v[4 * u + 3] * mul);
+  } else {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? p.dk : p.dv) + base;
+    #pragma unroll
+    for (int u = 0; u < kHeadDim / 8; ++u)
+      reinterpret_cast<uint4*>(dst)[u] = make_uint4(
+          pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul), pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
+          pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul), pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
+  }
+}
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t kv_full, s_full, p_full, mma2_done, dq_free, drained;
+  __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
+  __shared__ float s_lse2[kBwdStages][kBlockM];   // lse * log2(e); +inf hides the row
+  __shared__ float s_D[kBwdStages][kBlockM];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int g = blockIdx.x / p.split;      // kv head
+  const int part = blockIdx.x % p.split;   // which slice of the GQA group
+  const int hpc = p.group / p.split;       // query heads handled by this CTA
+  const int h_first = g * p.group + part * hpc;
+  const int seq = blockIdx.y;
+  const int ktile = blockIdx.z;            // low key tiles carry the most work: first
+  const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
+  const int j0 = ktile * kBlockN;
+  if (j0 >= sp.nk) return;                  // uniform per CTA
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int off = sp.nk - sp.nq;
+  const int last_key = min(j0 + kBlockN, sp.nk) - 1;
+
+  // Query rows that can see a key of this tile: i >= j - off, i < j - off + W.
+  int q_lo = 0, q_hi = sp.nq;
+  if (p.causal) {
+    q_lo = max(0, j0 - off);
+    if (p.window > 0) q_hi = min(sp.nq, last_key - off + p.window);
+  }
+  const int qt_first = q_lo / kBlockM;
+  const int nqt = (q_hi > q_lo) ? ((q_hi + kBlockM - 1) / kBlockM - qt_first) : 0;
+  const int num = nqt * hpc;                // steps: (query head) x (query tile)
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + kTileBytes;
+  uint8_t* sQ = sV + kTileBytes;                      // kBwdStages tiles
+  uint8_t* sdO = sQ + kBwdStages * kTileBytes;        // kBwdStages tiles
+  uint8_t* sdS = sdO + kBwdStages * kTileBytes;       // [128 keys][128 queries] bf16
+
+  if (num == 0) {
+    // No query sees these keys: dK = dV = 0.
+    if (tid < kBlockN && j0 + tid < sp.nk) {
+      const size_t row = (size_t)(sp.k0 + j0 + tid);
+      float zero[kHeadDim];
+      #pragma unroll
+      for (int c = 0; c < kHeadDim; ++c) zero[c] = 0.0f;
+      store_kv_grad_row(p, part, row, g, 0, zero, 1.0f);
+      store_kv_grad_row(p, part, row, g, 1, zero, 1.0f);
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&kv_full, 1);
+    mbar_init(&s_full, 1);
+    mbar_init(&p_full, kBlockN);
+    mbar_init(&mma2_done, 1);
+    mbar_init(&dq_free, kBlockM);
+    mbar_init(&drained, 1);
+    for (int s = 0; s < kBwdStages; ++s) {
+      mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 producer lanes (lse / D)
+      mbar_init(&q_empty[s], 1);
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(&kv_full, 2 * kTileBytes);
+      tma_load_3d(&p.tm_k, &kv_full, sK, 0, g, sp.k0 + j0);
+      tma_load_3d(&p.tm_v, &kv_full, sV, 0, g, sp.k0 + j0);
+    }
+    int issued = 0;
+    for (int m = 0; m < num; ++m) {
+      const int st = m % kBwdStages;
+      if (m >= kBwdStages &&
+          !mbar_wait_warp(&q_empty[st], ((m / kBwdStages) & 1) ^ 1, &abort_flag)) {
+        if (lane == 0) {
+          abort_flag = 1;
+          atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 1);
+        }
+        break;
+      }
+      const int h = h_first + m / nqt;
+      const int i0 = (qt_first + m % nqt) * kBlockM;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&q_full[st], 2 * kTileBytes);
+        tma_load_3d(&p.tm_q, &q_full[st], sQ + st * kTileBytes, 0, h, sp.q0 + i0);
+        tma_load_3d(&p.tm_do, &q_full[st], sdO + st * kTileBytes, 0, h, sp.q0 + i0);
+      }
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = lane + 32 * u;
+        const int i = i0 + t;
+        float l2 = INFINITY, dd = 0.0f;
+        if (i < sp.nq) {
+          const size_t idx = (size_t)h * p.total_q + sp.q0 + i;
+          const float lse = p.lse[idx];
+          l2 = (lse > -INFINITY) ? lse * kLog2e : INFINITY;
+          dd = p.D[idx];
+        }
+        s_lse2[st][t] = l2;
+        s_D[st][t] = dd;
+      }
+      mbar_arrive(&q_full[st]);
+      issued = m + 1;
+    }
+    if (abort_flag && lane == 0) {
+      mbar_wait(&kv_full, 0, nullptr);
+      for (int m = max(0, issued - kBwdStages); m < issued; ++m)
+        mbar_wait(&q_full[m % kBwdStages], (m / kBwdStages) & 1, nullptr);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = make_idesc_bf16(kBlockN, kBlockM, false, false);   // S^T, dP^T
+      const uint32_t id_dvdk = make_idesc_bf16(kBlockN, kHeadDim, false, true);
+      const uint32_t id_dq = make_idesc_bf16(kBlockM, kHeadDim, true, true);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aS = smem_u32(sdS);
+      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+      for (int m = 0; ok && m < num; ++m) {
+        const int st = m % kBwdStages;
+        if (!mbar_wait(&q_full[st], (m / kBwdStages) & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ + st * kTileBytes);
+        const uint32_t aO = smem_u32(sdO + st * kTileBytes);
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_bf16_ss(tmem + kColST, make_sdesc_sw128(aK + 32 * k, 16, 1024),
+                      make_sdesc_sw128(aQ + 32 * k, 16, 1024), id_s, k > 0);
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_bf16_ss(tmem + kColDPT, make_sdesc_sw128(aV + 32 * k, 16, 1024),
+                      make_sdesc_sw128(aO + 32 * k, 16, 1024), id_s, k > 0);
+        mma_commit(&s_full);
+        if (!mbar_wait(&p_full, m & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // dV += P^T dO  (A: P^T in TMEM, K = query index; B: dO tile read MN-major)
+        #pragma unroll
+        for (int k = 0; k < kBlockM / 16; ++k)
+          mma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * k,
+                      make_sdesc_sw128(aO + k * 2048, 16384, 1024), id_dvdk, (m > 0 || k > 0));
+        // dK += dS^T Q  (A: dS^T in SMEM, K-major over queries; B: Q read MN-major)
+        #pragma unroll
+        for (int k = 0; k < kBlockM / 16; ++k)
+          mma_bf16_ss(tmem + kColDK,
+                      make_sdesc_sw128(aS + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
+                      make_sdesc_sw128(aQ + k * 2048, 16384, 1024), id_dvdk, (m > 0 || k > 0));
+        if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // dQ = dS K  (A: dS^T SMEM read MN-major, M = queries; B: K read MN-major)
+        #pragma unroll
+        for (int k = 0; k < kBlockN / 16; ++k)
+          mma_bf16_ss(tmem + kColDQ, make_sdesc_sw128(aS + k * 2048, 16384, 1024),
+                      make_sdesc_sw128(aK + k * 2048, 16384, 1024), id_dq, k > 0);
+        mma_commit(&mma2_done);
+        mma_commit(&q_empty[st]);
+      }
+      if (!ok) {
+        abort_flag = 1;
+        atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 2);
+      }
+      mma_commit(&drained);
+      mbar_wait(&drained, 0, nullptr);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- compute warps
+    const int r = tid;                               // key row in tile = TMEM lane
+    const int j = j0 + r;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const uint32_t sbase = smem_u32(sdS);
+    bool ok = true;
+    for (int m = 0; m < num; ++m) {
+      const int st = m % kBwdStages;
+      const int i0 = (qt_first + m % nqt) * kBlockM;
+      // q_full: the producer's lse / D rows of this step are in SMEM.
+      if (!mbar_wait_warp(&q_full[st], (m / kBwdStages) & 1, &abort_flag) ||
+          !mbar_wait_warp(&s_full, m & 1, &abort_flag)) { ok = false; break; }
+      // The previous step's dV/dK/dQ MMAs have read P^T and dS^T.
+      if (m > 0 && !mbar_wait_warp(&mma2_done, (m - 1) & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const bool need_mask = (j0 + kBlockN > sp.nk) || (i0 + kBlockM > sp.nq) ||
+                             (p.causal && (j0 + kBlockN - 1 > i0 + off ||
+                                           (p.window > 0 && j0 <= i0 + kBlockM - 1 + off - p.window)));
+      // query rows this key is visible to: [imin, imax]
+      const int imin = p.causal ? j - off : 0;
+      const int imax = (p.causal && p.window > 0) ? j - off + p.window - 1 : sp.nq - 1;
+      const bool key_ok = j < sp.nk;
+      #pragma unroll 1
+      for (int c = 0; c < kBlockM; c += 32) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_x32(tmem + lane_base + kColST + c, sr);
+        tmem_ld_x32(tmem + lane_base + kColDPT + c, dr);
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+        #pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int ci = c + e + u;
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -s_lse2[st][ci]));
+            if (need_mask) {
+              const int i = i0 + ci;
+              if (!key_ok || i < imin || i > imax || i >= sp.nq) pe = 0.0f;
+            }
+            pv[u] = pe;
+            dv[u] = pe * (__uint_as_float(dr[e + u]) - s_D[st][ci]);
+          }
+          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+          dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_st_x16(tmem + lane_base + kColPT + (c >> 1), pk);
+        // dS^T row r, queries c..c+31: 4 chunks of 16 bytes in sub-tile c/64
+        const uint32_t tb = sbase + (c >> 6) * kTileBytes;
+        #pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(tb + sw128_offset(r, ((c & 63) >> 3) + u), dk[4 * u], dk[4 * u + 1],
+                       dk[4 * u + 2], dk[4 * u + 3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    if (ok && !mbar_wait_warp(&mma2_done, (num - 1) & 1, &abort_flag)) ok = false;
+    if (!ok) {
+      abort_flag = 1;
+      atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 3);
+    } else {
+      tc_fence_after();
+      // Epilogue: dK (times the softmax scale) and dV for this key row.
+      const bool valid = j < sp.nk;
+      const size_t row = (size_t)(sp.k0 + j);
+      #pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float v[kHeadDim];
+        const uint32_t col = which == 0 ? kColDK : kColDV;
+        tmem_ld_x32(tmem + lane_base + col, reinterpret_cast<uint32_t*>(v));
+        tmem_ld_x32(tmem + lane_base + col + 32, reinterpret_cast<uint32_t*>(v + 32));
+        tmem_ld_wait();
+        if (valid) store_kv_grad_row(p, part, row, g, which, v, which == 0 ? p.scale : 1.0f);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ warps (6-9)
+    const int r = 32 * (warp & 3) + lane;            // query row in tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    bool ok = true;
+    for (int m = 0; m < num; ++m) {
+      const int h = h_first + m / nqt;
+      const int i0 = (qt_first + m % nqt) * kBlockM;
+      if (!mbar_wait_warp(&mma2_done, m & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld_x32(tmem + lane_base + kColDQ, v);
+      tmem_ld_x32(tmem + lane_base + kColDQ + 32, v + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&dq_free);
+      const int i = i0 + r;
+      if (i < sp.nq) {
+        float4* dst = reinterpret_cast<float4*>(
+            p.dq_acc + ((size_t)(sp.q0 + i) * p.heads_q + h) * kHeadDim);
+        #pragma unroll
+        for (int u = 0; u < 16; ++u)
+          atomicAdd(dst + u, make_float4(__uint_as_float(v[4 * u]) * p.scale,
+                                         __uint_as_float(v[4 * u + 1]) * p.scale,
+                                         __uint_as_float(v[4 * u + 2]) * p.scale,
+                                         __uint_as_float(v[4 * u + 3]) * p.scale));
+      }
+    }
+    if (!ok) {
+      abort_flag = 1;
+      if (lane == 0) atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 4);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn_sink

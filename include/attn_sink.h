@@ -1,0 +1,151 @@
+/*
+ * attn_sink.h -- C ABI of libattn_sink.so: fused scaled-dot-product attention
+ * with one learnable scalar sink logit per query head, forward and backward,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  For query row i of head h (key/value head g = h / (H_q/H_kv)):
+ *   S_ij = softmax_scale * <q_i, k_j>            over the keys j visible to i
+ *   P_ij = exp(S_ij) / (sum_j' exp(S_ij') + exp(sink[h]))
+ *   P_ih = exp(sink[h]) / (same denominator)
+ *   out_i = sum_j P_ij v_j                          (the sink multiplies no value row)
+ *   lse_i = log(sum_j exp(S_ij) + exp(sink[h]))      (natural log, sink included)
+ * This is the concat-sink softmax of the listing "带汇聚的注意力（GPT-OSS）" and the
+ * P_ij / P_ih equations (section "数学公式") on the page "解锁 GPT-OSS 的 Agentic RL
+ * 训练：实用回顾" (euno.news); the same listing is on the page "Treinamento de RL
+ * Agêntico para modelos GPT-OSS" (section "Desafio 3: Attention Sinks no
+ * FlashAttention").  The sink is not multiplied by softmax_scale.
+ *
+ * Backward (section "反向传播" of the euno.news page for the sink; the ordinary
+ * softmax-attention backward for the rest), with D_i = sum_d dout_i[d] * out_i[d]:
+ *   dS_ij    = P_ij (<dout_i, v_j> - D_i)
+ *   dq_i     = softmax_scale * sum_j dS_ij k_j
+ *   dk_j     = softmax_scale * sum_{h in group, i} dS_ij q_i
+ *   dv_j     = sum_{h in group, i} P_ij dout_i
+ *   dsink[h] = - sum_i P_ih * D_i            (summed over every sequence)
+ *
+ * Masks.  causal: bottom-right aligned, query row i (0-based within its sequence)
+ * sees key j iff j <= i + (N_k - N_q).  window W > 0 (requires causal): also
+ * j > i + (N_k - N_q) - W, i.e. the W most recent keys including the diagonal.
+ * A row that sees no key gets out = 0 and lse = sink[h].
+ *
+ * Layouts (all contiguous, head_dim innermost, token-major):
+ *   q, out, dout, dq : [T_q, H_q, head_dim]     bf16 (dq: bf16 or fp32, see grad_dtype)
+ *   k, v, dk, dv     : [T_k, H_kv, head_dim]    bf16 (dk, dv: bf16 or fp32)
+ *   sink, dsink      : [H_q]                    fp32
+ *   lse              : [H_q, T_q]               fp32
+ *   cu_seqlens_q/k   : [num_seqs + 1]           int32, device memory, cu[0] = 0
+ * Dense batches (cu_seqlens == NULL) use T_q = batch * seqlen_q, T_k = batch * seqlen_k,
+ * sequence b occupying tokens [b*seqlen, (b+1)*seqlen).
+ *
+ * Ownership and threading.  Every pointer argument is DEVICE memory owned by the
+ * caller (params is a host pointer read during the call only).  The library
+ * allocates nothing.  Calls are asynchronous on `stream` (a cudaStream_t;
+ * NULL = legacy default stream) and never synchronise the host.  All calls are
+ * thread-safe; the only global state is the cached driver entry point for
+ * tensor-map encoding, initialised once.  Outputs are overwritten, never
+ * accumulated into.  Device pointers of q, k, v, out, dout, dq, dk, dv must be
+ * 16-byte aligned; the workspace must be 256-byte aligned.
+ *
+ * Errors.  Arguments are validated on the host before any launch; a bad
+ * argument returns ATTN_SINK_ERR_INVALID_ARG / _UNSUPPORTED / _WORKSPACE and
+ * launches nothing.  A failed launch returns ATTN_SINK_ERR_CUDA.  Every wait
+ * inside the kernels is bounded: a wait that does not complete records an
+ * error code in a device word (read it with attn_sink_device_error) and the
+ * kernel returns instead of hanging.  The host never reads cu_seqlens.
+ */
+#ifndef ATTN_SINK_H
+#define ATTN_SINK_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_SINK_OK = 0,
+  ATTN_SINK_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, misaligned pointer */
+  ATTN_SINK_ERR_UNSUPPORTED = 2,  /* head_dim != 64, or a combination not built */
+  ATTN_SINK_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  ATTN_SINK_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed */
+  ATTN_SINK_ERR_TIMEOUT = 5       /* a kernel gave up on a bounded wait */
+} attn_sink_status;
+
+/* Set the fields of one mode and leave the other mode's at 0: dense (batch,
+ * seqlen_q, seqlen_k; cu_seqlens NULL) or packed (num_seqs, total_q, total_k,
+ * max_seqlen_q, max_seqlen_k; cu_seqlens given).  Mixing them is an error. */
+typedef struct attn_sink_params {
+  /* dense batch (used when cu_seqlens_q == NULL) */
+  int batch;
+  int seqlen_q;
+  int seqlen_k;
+  /* packed variable-length sequences (used when cu_seqlens_q != NULL) */
+  int num_seqs;
+  int total_q;        /* T_q: tokens in q (= cu_seqlens_q[num_seqs]) */
+  int total_k;        /* T_k */
+  int max_seqlen_q;   /* upper bound on every query length; sizes the launch grid */
+  int max_seqlen_k;   /* upper bound on every key length */
+  /* heads */
+  int heads_q;        /* H_q, a multiple of heads_kv */
+  int heads_kv;       /* H_kv */
+  int head_dim;       /* must be 64 */
+  /* masking */
+  int causal;         /* 0 or 1 */
+  int window;         /* <= 0: no window; W > 0 needs causal = 1 */
+  float softmax_scale;/* multiplies q.k only; finite and > 0 */
+  /* backward outputs: 0 = bf16 dq/dk/dv, 1 = fp32 dq/dk/dv */
+  int grad_dtype;
+} attn_sink_params;
+
+/*
+ * Forward.  Writes out [T_q, H_q, 64] bf16 and lse [H_q, T_q] fp32.
+ * cu_seqlens_q and cu_seqlens_k are both NULL (dense) or both non-NULL (packed).
+ * Passage: listing "带汇聚的注意力（GPT-OSS）" and section "数学公式" of the
+ * euno.news page.  Returns an attn_sink_status.
+ */
+int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k,
+                  const void* v, const float* sink, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, void* out, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace attn_sink_bwd needs for these params (0 if the
+ * params are invalid).  The packed fields are used when num_seqs > 0, the
+ * dense ones otherwise.  The workspace holds the row terms D [H_q, T_q], the
+ * per-block dsink partials, the fp32 dq accumulator [T_q, H_q, 64] (bf16 dq
+ * only) and, when the backward splits a GQA group over several CTAs (decided
+ * from the shapes and the current device's SM count), fp32 dK/dV partials.
+ * Query it on the device the backward will run on.
+ */
+size_t attn_sink_bwd_workspace_size(const attn_sink_params* params);
+
+/*
+ * Backward.  Reads q, k, v, sink, out and lse from the forward and dout; writes
+ * dq, dk, dv (bf16 or fp32 per grad_dtype) and dsink [H_q] fp32.  dk and dv sum
+ * over the query heads of each group.  dq, dk, dv and dsink are overwritten.
+ * dsink is reduced in a fixed order (bitwise reproducible); dk and dv are too;
+ * dq is accumulated with fp32 atomics and may differ in the last bits between
+ * runs.  Passage: section "反向传播" of the euno.news page for dsink.
+ * Returns an attn_sink_status.
+ */
+int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k,
+                  const void* v, const float* sink, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, const void* out, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* dsink,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_sink_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that a
+ * kernel sets when it gives up on a bounded wait.  *code receives 0 when no
+ * kernel timed out.  Returns ATTN_SINK_OK, or ATTN_SINK_ERR_CUDA when the
+ * synchronisation itself failed.
+ */
+int attn_sink_device_error(void* stream, int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SINK_H */

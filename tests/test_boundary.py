@@ -1,0 +1,151 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host (no launch, no device
+call) with the documented status codes."""
+import ctypes
+import math
+
+import pytest
+
+from attention_learnable_head_gb300 import binding
+from attention_learnable_head_gb300.build import build
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    return binding.lib()
+
+
+def test_exports_every_declared_symbol():
+    names = binding.header_functions()
+    assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
+                          "attn_sink_status_string", "attn_sink_device_error"}
+    lib = binding.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_params_struct_layout():
+    # 14 ints + 1 float, no padding: must match attn_sink_params in the header.
+    assert ctypes.sizeof(binding.AttnSinkParams) == 60
+
+
+def test_status_strings():
+    for code in range(6):
+        s = binding.attn_sink_status_string(code)
+        assert isinstance(s, str) and s
+    assert binding.attn_sink_status_string(99) == "unknown status"
+
+
+def _dense(**kw):
+    p = binding.AttnSinkParams()
+    p.batch, p.seqlen_q, p.seqlen_k = 1, 256, 256
+    p.heads_q, p.heads_kv, p.head_dim = 8, 2, 64
+    p.causal, p.window, p.softmax_scale, p.grad_dtype = 1, 0, 0.125, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+FAKE = 0x7F0000000000       # never dereferenced: validation fails first
+FAKE_ODD = FAKE + 8
+
+
+def _fwd(p, q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, lse=FAKE):
+    return binding.attn_sink_fwd(p, q, k, v, sink, cu_q, cu_k, out, lse, stream=0)
+
+
+def _bwd(p, ws=FAKE, ws_bytes=1 << 40, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, lse=FAKE,
+                dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, dsink=FAKE)
+    args.update(kw)
+    return binding.attn_sink_bwd(p, args["q"], args["k"], args["v"], args["sink"], args["cu_q"],
+                                 args["cu_k"], args["out"], args["lse"], args["dout"], args["dq"],
+                                 args["dk"], args["dv"], args["dsink"], ws, ws_bytes, stream=0)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 128, UNSUPPORTED),
+    ("head_dim", 32, UNSUPPORTED),
+    ("heads_q", 7, INVALID),            # not a multiple of heads_kv
+    ("heads_kv", 0, INVALID),
+    ("causal", 2, INVALID),
+    ("window", 16, None),               # window needs causal: tested with causal = 0 below
+    ("softmax_scale", 0.0, INVALID),
+    ("softmax_scale", -1.0, INVALID),
+    ("softmax_scale", float("nan"), INVALID),
+    ("softmax_scale", float("inf"), INVALID),
+    ("grad_dtype", 2, INVALID),
+    ("batch", -1, INVALID),
+    ("num_seqs", 3, INVALID),           # packed field set without cu_seqlens
+])
+def test_invalid_params_rejected_on_host(field, value, status):
+    p = _dense(**{field: value})
+    if status is None:
+        p.causal = 0
+        status = INVALID
+    assert _fwd(p) == status
+    assert _bwd(p) == status
+    if field not in ("num_seqs",):
+        assert binding.attn_sink_bwd_workspace_size(p) == 0
+
+
+def test_null_and_misaligned_pointers():
+    p = _dense()
+    assert binding.attn_sink_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 0) == INVALID
+    assert _fwd(p, q=None) == INVALID
+    assert _fwd(p, sink=None) == INVALID
+    assert _fwd(p, out=None) == INVALID
+    assert _fwd(p, lse=None) == INVALID
+    assert _fwd(p, q=FAKE_ODD) == INVALID
+    assert _fwd(p, v=FAKE + 4) == INVALID
+    assert _bwd(p, dsink=None) == INVALID
+    assert _bwd(p, dq=None) == INVALID
+    assert _bwd(p, dk=FAKE_ODD) == INVALID
+    # one cu_seqlens without the other
+    assert _fwd(p, cu_q=FAKE) == INVALID
+
+
+def test_packed_mode_checks():
+    p = _dense(batch=0, seqlen_q=0, seqlen_k=0, num_seqs=2, total_q=100, total_k=100,
+               max_seqlen_q=60, max_seqlen_k=60)
+    # dense batch field set together with cu_seqlens
+    p2 = _dense(num_seqs=2, total_q=100, total_k=100, max_seqlen_q=60, max_seqlen_k=60)
+    assert _fwd(p2, cu_q=FAKE, cu_k=FAKE) == INVALID
+    # a max length above the total is inconsistent
+    p3 = _dense(batch=0, num_seqs=2, total_q=100, total_k=100, max_seqlen_q=160,
+                max_seqlen_k=60)
+    assert _fwd(p3, cu_q=FAKE, cu_k=FAKE) == INVALID
+    # too many sequences for the launch grid
+    p4 = _dense(batch=0, num_seqs=70000, total_q=70000, total_k=70000, max_seqlen_q=1,
+                max_seqlen_k=1)
+    assert _fwd(p4, cu_q=FAKE, cu_k=FAKE) == UNSUPPORTED
+    assert binding.attn_sink_bwd_workspace_size(p) > 0
+
+
+def test_empty_problem_is_a_no_op():
+    # Nothing to compute: returns OK without touching the device.
+    assert _fwd(_dense(batch=0)) == OK
+    assert _fwd(_dense(seqlen_q=0)) == OK
+
+
+def test_workspace_size():
+    p = _dense(batch=2, seqlen_q=1000, seqlen_k=1000, heads_q=64, heads_kv=8)
+    n_bf16 = binding.attn_sink_bwd_workspace_size(p)
+    t, h = 2000, 64
+    assert n_bf16 % 256 == 0
+    # at least D, the partials and the fp32 dq accumulator
+    assert n_bf16 >= t * h * 4 + t * h * 64 * 4
+    p.grad_dtype = 1
+    n_fp32 = binding.attn_sink_bwd_workspace_size(p)
+    assert n_fp32 < n_bf16       # fp32 dq is accumulated in place
+    assert binding.attn_sink_bwd_workspace_size(None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()

@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded bf16 inputs, element by element.  Sizes span several 128-row
+tiles and ragged tails; edge cases cover GQA groups, windows around the tile
+size, rows that see no key, empty sequences and extreme sinks."""
+import math
+
+import pytest
+import torch
+
+from attention_learnable_head_gb300.inputs import WORKLOADS, make_case, small_workload, with_
+from oracle import oracle_bwd
+from parity import check_against, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _ref(case, cu_q=None, cu_k=None, **kw):
+    w = case.workload
+    cq = case.cu_seqlens if cu_q is None else cu_q
+    ck = case.cu_seqlens if cu_k is None else cu_k
+    return oracle_bwd(case.q, case.k, case.v, case.sink, case.dout, scale=w.scale,
+                      causal=w.causal, window=w.window, cu_seqlens_q=cq, cu_seqlens_k=ck, **kw)
+
+
+def test_tiny_config():
+    """B=1, H_q=H_kv=2, N=128, causal, sink ~ N(0,1): fwd + bwd."""
+    c = make_case(WORKLOADS["tiny"])
+    check_against(run_gpu(c), _ref(c))
+    check_against(run_gpu(c, dense=True), _ref(c))
+
+
+SMALL = [
+    # name, heads_q, heads_kv, lengths, causal, window
+    ("ragged_g8", 8, 1, [1, 5, 127, 128, 129, 300], True, 0),
+    ("g2_window127", 4, 2, [200, 77, 256], True, 127),
+    ("g1_window1", 2, 2, [300, 3], True, 1),
+    ("g2_window128", 4, 2, [385], True, 128),
+    ("g2_window129", 4, 2, [385, 130], True, 129),
+    ("noncausal", 2, 2, [129, 64, 1], False, 0),
+    ("g8_long", 16, 2, [700], True, 0),
+]
+
+
+@pytest.mark.parametrize("name,hq,hkv,lengths,causal,window", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("grad_dtype", [0, 1])
+def test_small_cases(name, hq, hkv, lengths, causal, window, grad_dtype):
+    w = small_workload(name, 300 + len(name), hq, hkv, lengths, causal=causal, window=window)
+    c = make_case(w)
+    check_against(run_gpu(c, grad_dtype=grad_dtype), _ref(c))
+
+
+def test_dense_batch_layout():
+    w = small_workload("dense", 411, 8, 2, [200, 200, 200], causal=True)
+    c = make_case(w)
+    check_against(run_gpu(c, dense=True), _ref(c))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_different_query_and_key_lengths(causal):
+    """N_q != N_k per sequence (bottom-right causal), including a sequence whose
+    first query rows see no key (N_q > N_k) and an empty query sequence."""
+    lq, lk = [100, 64, 0, 130], [150, 10, 40, 130]
+    cq, ck = [0], [0]
+    for a, b in zip(lq, lk):
+        cq.append(cq[-1] + a)
+        ck.append(ck[-1] + b)
+    w = small_workload("qk", 421 + causal, 4, 2, [sum(lq)], causal=causal)
+    c = make_case(w)
+    g = torch.Generator().manual_seed(4242)
+    k = torch.randn((sum(lk), 2, 64), generator=g).to(torch.bfloat16)
+    v = torch.randn((sum(lk), 2, 64), generator=g).to(torch.bfloat16)
+    c.k, c.v = k, v
+    res = run_gpu(c, cu_q=cq, cu_k=ck)
+    check_against(res, _ref(c, cu_q=cq, cu_k=ck))
+
+
+@pytest.mark.parametrize("sink_kind,const", [("neginf", 0.0), ("const", 8.0), ("const", -30.0),
+                                             ("choice", 0.0)])
+def test_extreme_sinks(sink_kind, const):
+    """sink = -inf (standard attention), saturating +8 and vanishing -30."""
+    w = small_workload("sinks", 431, 8, 2, [257, 31], sink_kind=sink_kind, sink_const=const)
+    c = make_case(w)
+    res = run_gpu(c)
+    ref = _ref(c)
+    if sink_kind == "neginf":
+        assert torch.equal(res["dsink"], torch.zeros_like(res["dsink"]))
+        ref.pop("dsink")
+    check_against(res, ref)
+
+
+def test_peaked_scores_fp32_grads():
+    """q scaled by 3 (peaked softmax) as in the long-batch workload."""
+    w = small_workload("peaked", 441, 8, 1, [512, 200], q_mult=3.0, sink_sigma=2.0)
+    c = make_case(w)
+    check_against(run_gpu(c, grad_dtype=1), _ref(c))
+
+
+def test_rows_without_keys_in_tiles():
+    """N_q > N_k: whole query tiles with no visible key get out = 0, lse = sink."""
+    cq, ck = [0, 300], [0, 20]
+    w = small_workload("nokeys", 451, 2, 1, [300])
+    c = make_case(w)
+    g = torch.Generator().manual_seed(4511)
+    c.k = torch.randn((20, 1, 64), generator=g).to(torch.bfloat16)
+    c.v = torch.randn((20, 1, 64), generator=g).to(torch.bfloat16)
+    res = run_gpu(c, cu_q=cq, cu_k=ck)
+    ref = _ref(c, cu_q=cq, cu_k=ck)
+    check_against(res, ref)
+    assert torch.equal(res["out"][:200].float(), torch.zeros(200, 2, 64))
+    assert torch.allclose(res["lse"][:, :200], c.sink.unsqueeze(1).expand(2, 200))
+
+
+def test_backward_determinism():
+    """dk, dv and dsink are bitwise reproducible; dq agrees within tolerance."""
+    w = small_workload("det", 461, 16, 2, [640, 129])
+    c = make_case(w)
+    a = run_gpu(c)
+    b = run_gpu(c)
+    for name in ("dk", "dv", "dsink", "out", "lse"):
+        assert torch.equal(a[name], b[name]), name
+    assert (a["dq"].float() - b["dq"].float()).abs().max() <= 1e-2
+
+
+def test_autograd_function():
+    from attention_learnable_head_gb300.binding import attn_sink
+    w = small_workload("ag", 471, 4, 2, [96])
+    c = make_case(w)
+    dev = torch.device("cuda:0")
+    q = c.q.view(1, 96, 4, 64).to(dev).requires_grad_()
+    k = c.k.view(1, 96, 2, 64).to(dev).requires_grad_()
+    v = c.v.view(1, 96, 2, 64).to(dev).requires_grad_()
+    sink = c.sink.to(dev).requires_grad_()
+    out = attn_sink(q, k, v, sink, causal=True, softmax_scale=w.scale)
+    out.backward(c.dout.view(1, 96, 4, 64).to(dev))
+    ref = _ref(c)
+    check_against(dict(out=out.detach().view(96, 4, 64).cpu(), dq=q.grad.view(96, 4, 64).cpu(),
+                       dk=k.grad.view(96, 2, 64).cpu(), dv=v.grad.view(96, 2, 64).cpu(),
+                       dsink=sink.grad.cpu()), ref)
