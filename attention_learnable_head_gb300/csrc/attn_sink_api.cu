@@ -262,9 +262,9 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   fp.causal = params->causal;
   fp.window = params->window > 0 ? params->window : 0;
   fp.scale_log2 = params->softmax_scale * kLog2e;
-  fp.n_qtiles = (g.max_q + kBlockM - 1) / kBlockM;
-  if (fp.n_qtiles == 0) return ATTN_SINK_OK;
-  dim3 grid(params->heads_q, g.num_seqs, fp.n_qtiles);
+  fp.n_qblocks = (g.max_q + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
+  if (fp.n_qblocks == 0) return ATTN_SINK_OK;
+  dim3 grid(params->heads_q, g.num_seqs, fp.n_qblocks);
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
   return cudaGetLastError() == cudaSuccess ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
 }

@@ -1,19 +1,29 @@
 // Forward kernel: attention with a per-head sink, sm_103a (tcgen05 + TMA).
 //
-// Computes, for one (query head h, sequence, 128-row query tile) per CTA,
-//   S = Q K^T (tcgen05, fp32 in TMEM), an online softmax whose running max and
-//   sum start from the sink logit (m0 = sink[h], l0 = 1 in the exp2 domain), and
-//   O += P V (tcgen05), then out = O / l and lse = ln(l) + m (sink included).
-// The sink enters the softmax denominator only: it is the extra column of the
+// One CTA per (query head h, sequence, 256-row query block).  The block is two
+// 128-row tiles, A and B, that share every K/V tile and run in ping-pong: while
+// one softmax warpgroup turns its S tile into P, the tensor cores run the other
+// tile's MMAs.  Per tile and key tile:
+//   S = Q K^T (tcgen05, fp32 accumulators in TMEM),
+//   online softmax whose running max and sum start from the sink logit
+//   (m0 = sink[h] * log2 e, l0 = 1 in the exp2 domain),
+//   P (bf16) written to TMEM and consumed there by O += P V (tcgen05, A from TMEM),
+// then out = O / l and lse = ln 2 * (m + log2 l), which includes the sink.
+// The sink joins the softmax denominator only: it is the extra column of the
 // concat listing "带汇聚的注意力（GPT-OSS）" on the euno.news page, and the
 // P_ij / P_ih equations of its section "数学公式".
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t); rescales O in
-//              TMEM, writes P (bf16) to a swizzled SMEM tile, runs the epilogue.
-//   warp 4     TMA producer: Q once, then K/V tiles through an NSTAGE ring.
-//   warp 5     MMA issuer (one lane) and TMEM owner.
-// TMEM columns: S double buffer at 0 and 128 (128 fp32 columns each), O at 256.
+// Rescaling of O is lazy: the running max used for the exponentials only moves
+// when a row's max grows by more than kRescaleThreshold (log2 units); P stays
+// below 2^threshold, and out/lse are exact because l and O use the same max.
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax + epilogue of tile A (thread t owns row t = TMEM lane t)
+//   warps 4-7  softmax + epilogue of tile B
+//   warp 8     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
+//   warp 9     MMA issuer (one lane) and TMEM owner
+// TMEM columns: S_A 0, S_B 128 (128 fp32 each), O_A 256, O_B 320 (64 each),
+//               P_A 384, P_B 448 (128 bf16 packed in 64 columns each).
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -23,14 +33,16 @@ namespace attn_sink {
 constexpr int kBlockM = 128;   // query rows per tile
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kHeadDim = 64;
-constexpr int kFwdStages = 3;
-constexpr int kFwdThreads = 192;
+constexpr int kFwdTiles = 2;   // query tiles per CTA
+constexpr int kFwdStages = 4;
+constexpr int kFwdThreads = 320;
+constexpr int kFwdRowsPerCta = kFwdTiles * kBlockM;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
-constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 P tile
-constexpr int kFwdSmemBytes =
-    1024 + (int)kTileBytes * (1 + 2 * kFwdStages) + 2 * (int)kPTileBytes;
+constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
+constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (kFwdTiles + 2 * kFwdStages);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
 
 struct FwdParams {
   CUtensorMap tm_q;   // [T_q][H_q][64] bf16, box 64 x 1 x 128, 128B swizzle
@@ -47,7 +59,7 @@ struct FwdParams {
   int heads_q, group;
   int causal, window;
   float scale_log2;   // softmax_scale * log2(e)
-  int n_qtiles;       // number of query tiles of the longest sequence
+  int n_qblocks;      // 256-row query blocks of the longest sequence
 };
 
 struct SeqSpan {
@@ -71,73 +83,100 @@ __device__ __forceinline__ SeqSpan seq_span(const int* cu_q, const int* cu_k, in
   return s;
 }
 
+// Key tiles [lo, lo + num) that query rows [r0, r1] (inclusive) can see.
+struct KeyRange {
+  int lo, num;
+};
+
+__device__ __forceinline__ KeyRange key_tiles(int r0, int r1, const SeqSpan& sp, int causal,
+                                              int window) {
+  KeyRange kr{0, 0};
+  if (r1 < r0) return kr;
+  const int off = sp.nk - sp.nq;
+  int kv_lo = 0, kv_hi = sp.nk;
+  if (causal) {
+    kv_hi = min(sp.nk, r1 + off + 1);
+    if (window > 0) kv_lo = max(0, r0 + off - window + 1);
+  }
+  if (kv_hi <= kv_lo) return kr;
+  kr.lo = kv_lo / kBlockN;
+  kr.num = (kv_hi + kBlockN - 1) / kBlockN - kr.lo;
+  return kr;
+}
+
 __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, pv_done, mma_drained;
+  __shared__ __align__(8) uint64_t q_full, mma_drained;
   __shared__ __align__(8) uint64_t k_full[kFwdStages], v_full[kFwdStages], kv_empty[kFwdStages];
-  __shared__ __align__(8) uint64_t s_full[2], p_full[2];
+  __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
-  const int qtile = p.n_qtiles - 1 - (int)blockIdx.z;   // longest work first
+  const int qblock = p.n_qblocks - 1 - (int)blockIdx.z;   // longest work first
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
-  const int i0 = qtile * kBlockM;
-  if (i0 >= sp.nq) return;                              // uniform per CTA
+  const int i0 = qblock * (kFwdTiles * kBlockM);
+  if (i0 >= sp.nq) return;                                // uniform per CTA
   const int g = h / p.group;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int off = sp.nk - sp.nq;                         // bottom-right causal offset
-  const int last_row = min(i0 + kBlockM, sp.nq) - 1;
-
-  // Key range [kv_lo, kv_hi) any row of this tile can see.
-  int kv_lo = 0, kv_hi = sp.nk;
-  if (p.causal) {
-    kv_hi = min(sp.nk, last_row + off + 1);
-    if (p.window > 0) kv_lo = max(0, i0 + off - p.window + 1);
+  const bool has_b = i0 + kBlockM < sp.nq;
+  const KeyRange kr_a = key_tiles(i0, min(i0 + kBlockM, sp.nq) - 1, sp, p.causal, p.window);
+  const KeyRange kr_b = has_b ? key_tiles(i0 + kBlockM, min(i0 + 2 * kBlockM, sp.nq) - 1, sp,
+                                          p.causal, p.window)
+                              : KeyRange{0, 0};
+  // union of the two tiles' key ranges
+  int lo, hi;
+  if (kr_a.num > 0 && kr_b.num > 0) {
+    lo = min(kr_a.lo, kr_b.lo);
+    hi = max(kr_a.lo + kr_a.num, kr_b.lo + kr_b.num);
+  } else if (kr_a.num > 0) {
+    lo = kr_a.lo; hi = kr_a.lo + kr_a.num;
+  } else {
+    lo = kr_b.lo; hi = kr_b.lo + kr_b.num;
   }
-  const int n_first = kv_lo / kBlockN;
-  const int num = (kv_hi > kv_lo) ? ((kv_hi + kBlockN - 1) / kBlockN - n_first) : 0;
+  const int num = (kr_a.num > 0 || kr_b.num > 0) ? hi - lo : 0;
   const float sink_h = __ldg(p.sink + h);
 
   if (num == 0) {
-    // No row of this tile sees a key: out = 0, lse = sink (the sink alone).
-    if (tid < kBlockM && i0 + tid < sp.nq) {
-      const size_t row = (size_t)(sp.q0 + i0 + tid);
-      uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.heads_q + h) * kHeadDim);
-      #pragma unroll
-      for (int c = 0; c < 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
-      p.lse[(size_t)h * p.total_q + row] = sink_h;
+    // No row of this block sees a key: out = 0, lse = sink (the sink alone).
+    for (int t = tid; t < kFwdTiles * kBlockM; t += kFwdThreads) {
+      if (i0 + t < sp.nq) {
+        const size_t row = (size_t)(sp.q0 + i0 + t);
+        uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.heads_q + h) * kHeadDim);
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+        p.lse[(size_t)h * p.total_q + row] = sink_h;
+      }
     }
     return;
   }
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + kTileBytes;
+  uint8_t* sQ = smem;                                   // kFwdTiles tiles
+  uint8_t* sK = sQ + kFwdTiles * kTileBytes;
   uint8_t* sV = sK + kFwdStages * kTileBytes;
-  uint8_t* sP = sV + kFwdStages * kTileBytes;
 
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&q_full, 1);
-    mbar_init(&pv_done, 1);
     mbar_init(&mma_drained, 1);
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], kBlockM);
+    for (int x = 0; x < kFwdTiles; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], kBlockM);
+      mbar_init(&pv_done[x], 1);
     }
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
@@ -145,17 +184,17 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tm_o = tmem + 256;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       const uint64_t keep = l2_policy_evict_last();
-      mbar_arrive_expect_tx(&q_full, kTileBytes);
+      mbar_arrive_expect_tx(&q_full, (has_b ? 2 : 1) * kTileBytes);
       tma_load_3d(&p.tm_q, &q_full, sQ, 0, h, sp.q0 + i0);
+      if (has_b) tma_load_3d(&p.tm_q, &q_full, sQ + kTileBytes, 0, h, sp.q0 + i0 + kBlockM);
       int issued = 0;
       for (int it = 0; it < num; ++it) {
         const int st = it % kFwdStages;
@@ -165,7 +204,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 1);
           break;
         }
-        const int row = sp.k0 + (n_first + it) * kBlockN;
+        const int row = sp.k0 + (lo + it) * kBlockN;
         mbar_arrive_expect_tx(&k_full[st], kTileBytes);
         tma_load_3d_hint(&p.tm_k, &k_full[st], sK + st * kTileBytes, 0, g, row, keep);
         mbar_arrive_expect_tx(&v_full[st], kTileBytes);
@@ -182,54 +221,56 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
       const uint32_t idesc_o = make_idesc_bf16(kBlockM, kHeadDim, false, true);
-      const uint32_t aQ = smem_u32(sQ);
-      bool ok = mbar_wait(&q_full, 0, &abort_flag) && mbar_wait(&k_full[0], 0, &abort_flag);
-      if (ok) {
+      const KeyRange kr[kFwdTiles] = {kr_a, kr_b};
+      bool ok = mbar_wait(&q_full, 0, &abort_flag);
+      // S_x(n) = Q_x K_n^T into S_x; n is a union index.
+      auto issue_s = [&](int x, int n) -> bool {
+        const int st = n % kFwdStages;
+        if (!mbar_wait(&k_full[st], (n / kFwdStages) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t aK = smem_u32(sK);
+        const uint32_t aQ = smem_u32(sQ + x * kTileBytes);
+        const uint32_t aK = smem_u32(sK + st * kTileBytes);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_bf16_ss(tmem, make_sdesc_sw128(aQ + 32 * k, 16, 1024),
+          mma_bf16_ss(tmem + x * 128, make_sdesc_sw128(aQ + 32 * k, 16, 1024),
                       make_sdesc_sw128(aK + 32 * k, 16, 1024), idesc_s, k > 0);
-        mma_commit(&s_full[0]);
-      }
-      for (int it = 0; ok && it < num; ++it) {
-        if (it + 1 < num) {
-          const int st1 = (it + 1) % kFwdStages;
-          if (!mbar_wait(&k_full[st1], ((it + 1) / kFwdStages) & 1, &abort_flag)) {
+        mma_commit(&s_full[x]);
+        return true;
+      };
+      auto in_range = [&](int x, int n) {
+        const int a = lo + n;
+        return kr[x].num > 0 && a >= kr[x].lo && a < kr[x].lo + kr[x].num;
+      };
+      for (int x = 0; ok && x < kFwdTiles; ++x)
+        if (kr[x].num > 0) ok = issue_s(x, kr[x].lo - lo);
+      for (int n = 0; ok && n < num; ++n) {
+        const int st = n % kFwdStages;
+        #pragma unroll
+        for (int x = 0; x < kFwdTiles; ++x) {
+          if (!ok || !in_range(x, n)) continue;
+          const int local = lo + n - kr[x].lo;
+          if (!mbar_wait(&p_full[x], local & 1, &abort_flag) ||
+              !mbar_wait(&v_full[st], (n / kFwdStages) & 1, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t aK = smem_u32(sK + st1 * kTileBytes);
-          const uint32_t dS = tmem + ((it + 1) & 1) * 128;
+          const uint32_t aV = smem_u32(sV + st * kTileBytes);
+          const uint32_t tP = tmem + 384 + x * 64;
+          const uint32_t tO = tmem + 256 + x * 64;
           #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k)
-            mma_bf16_ss(dS, make_sdesc_sw128(aQ + 32 * k, 16, 1024),
-                        make_sdesc_sw128(aK + 32 * k, 16, 1024), idesc_s, k > 0);
-          mma_commit(&s_full[(it + 1) & 1]);
+          for (int k = 0; k < kBlockN / 16; ++k)
+            mma_bf16_ts(tO, tP + 8 * k, make_sdesc_sw128(aV + k * 2048, 16384, 1024), idesc_o,
+                        (local > 0 || k > 0));
+          mma_commit(&pv_done[x]);
+          if (in_range(x, n + 1)) ok = issue_s(x, n + 1);
         }
-        const int b = it & 1;
-        const int st = it % kFwdStages;
-        if (!mbar_wait(&p_full[b], (it >> 1) & 1, &abort_flag) ||
-            !mbar_wait(&v_full[st], (it / kFwdStages) & 1, &abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t aP = smem_u32(sP + b * kPTileBytes);
-        const uint32_t aV = smem_u32(sV + st * kTileBytes);
-        #pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k)
-          mma_bf16_ss(tm_o, make_sdesc_sw128(aP + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                      make_sdesc_sw128(aV + k * 2048, 16384, 1024), idesc_o, (it > 0 || k > 0));
-        mma_commit(&kv_empty[st]);
-        mma_commit(&pv_done);
+        if (ok) mma_commit(&kv_empty[st]);
       }
       if (!ok) {
         abort_flag = 1;
@@ -241,83 +282,104 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else {
     // ---------------------------------------------------------------- softmax warps
-    const int r = tid;                       // query row within the tile, TMEM lane
-    const int i = i0 + r;                    // row within the sequence
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int x = warp >> 2;                 // tile 0 (A) or 1 (B)
+    const int r = tid & 127;                 // row within the tile = TMEM lane
+    const int i = i0 + x * kBlockM + r;      // row within the sequence
+    const KeyRange kx = x == 0 ? kr_a : kr_b;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_base;
+    const uint32_t tO = tmem + 256 + x * 64 + lane_base;
+    const uint32_t tP = tmem + 384 + x * 64 + lane_base;
+    const int off = sp.nk - sp.nq;
+    const int tile_r0 = i0 + x * kBlockM;
+    const int tile_r1 = min(tile_r0 + kBlockM, sp.nq) - 1;
     const bool sink_finite = sink_h > -INFINITY;
     float m = sink_finite ? sink_h * kLog2e : -INFINITY;   // running max, log2 domain
     float l = sink_finite ? 1.0f : 0.0f;                    // running sum, sink term = 1
     const float sl2 = p.scale_log2;
+    const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
+    const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
     bool ok = true;
-    for (int it = 0; it < num; ++it) {
-      const int b = it & 1;
-      if (!mbar_wait_warp(&s_full[b], (it >> 1) & 1, &abort_flag)) { ok = false; break; }
+    for (int it = 0; it < kx.num; ++it) {
+      if (!mbar_wait_warp(&s_full[x], it & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      float s[kBlockN];
-      #pragma unroll
-      for (int c = 0; c < kBlockN; c += 32)
-        tmem_ld_x32(tmem + lane_base + b * 128 + c, reinterpret_cast<uint32_t*>(s + c));
-      tmem_ld_wait();
-
-      const int j0 = (n_first + it) * kBlockN;
+      const int j0 = (kx.lo + it) * kBlockN;
       const bool need_mask = (j0 + kBlockN > sp.nk) ||
-                             (p.causal && (j0 + kBlockN - 1 > i0 + off ||
-                                           (p.window > 0 && j0 <= last_row + off - p.window)));
-      if (need_mask) {
-        const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
-        const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
-        #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) {
-          const int j = j0 + c;
-          if (j > jmax || j < jmin) s[c] = -INFINITY;
-        }
-      }
+                             (p.causal && (j0 + kBlockN - 1 > tile_r0 + off ||
+                                           (p.window > 0 && j0 <= tile_r1 + off - p.window)));
+      // pass 1: row max (S read from TMEM 64 columns at a time)
       float mx = -INFINITY;
       #pragma unroll
-      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * sl2);
-      const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-
+      for (int c = 0; c < kBlockN; c += 64) {
+        uint32_t a[64];
+        tmem_ld_x32(tS + c, a);
+        tmem_ld_x32(tS + c + 32, a + 32);
+        tmem_ld_wait();
+        if (need_mask) {
+          #pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int j = j0 + c + e;
+            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+          }
+        }
+        #pragma unroll
+        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
+      }
+      mx *= sl2;
+      // Lazy rescale: move the max only when it grows by more than the threshold.
+      float alpha = 1.0f;
+      if (mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY)) {
+        alpha = ex2_approx(m - mx);
+        m = mx;
+      }
+      // PV of the previous key tile has finished: O may be rescaled, P_x reused.
       if (it > 0) {
-        // P(it-1)V finished: O may be rescaled and the P buffer of it-2 is free.
-        if (!mbar_wait_warp(&pv_done, (it - 1) & 1, &abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&pv_done[x], (it - 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
           #pragma unroll
           for (int c = 0; c < kHeadDim; c += 32) {
             uint32_t o[32];
-            tmem_ld_x32(tm_o + lane_base + c, o);
+            tmem_ld_x32(tO + c, o);
             tmem_ld_wait();
             #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_x32(tm_o + lane_base + c, o);
+            tmem_st_x32(tO + c, o);
           }
-          tmem_st_wait();
         }
       }
-      m = m_new;
-
+      // pass 2: P = exp2(S * scale * log2 e - m), bf16, into TMEM P_x
+      const float m_use = (m == -INFINITY) ? 0.0f : m;
       float rowsum = 0.0f;
-      const uint32_t pbase = smem_u32(sP + b * kPTileBytes);
       #pragma unroll
-      for (int c = 0; c < kBlockN; c += 8) {
-        float e[8];
-        #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          e[u] = ex2_approx(fmaf(s[c + u], sl2, -m_use));
-          rowsum += e[u];
+      for (int c = 0; c < kBlockN; c += 32) {
+        uint32_t a[32];
+        tmem_ld_x32(tS + c, a);
+        tmem_ld_wait();
+        if (need_mask) {
+          #pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = j0 + c + e;
+            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+          }
         }
-        const uint32_t addr = pbase + (c >> 6) * kTileBytes + sw128_offset(r, (c & 63) >> 3);
-        st_shared_v4(addr, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                     pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+        uint32_t pk[16];
+        #pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float e0 = ex2_approx(fmaf(__uint_as_float(a[e]), sl2, -m_use));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(a[e + 1]), sl2, -m_use));
+          rowsum += e0 + e1;
+          pk[e >> 1] = pack_bf16x2(e0, e1);
+        }
+        tmem_st_x16(tP + (c >> 1), pk);
       }
       l = l * alpha + rowsum;
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[x]);
     }
-    if (ok && !mbar_wait_warp(&pv_done, (num - 1) & 1, &abort_flag)) ok = false;
+    if (ok && kx.num > 0 && !mbar_wait_warp(&pv_done[x], (kx.num - 1) & 1, &abort_flag))
+      ok = false;
     if (!ok) {
       abort_flag = 1;
       atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 3);
@@ -329,8 +391,13 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       #pragma unroll
       for (int c = 0; c < kHeadDim; c += 32) {
         uint32_t o[32];
-        tmem_ld_x32(tm_o + lane_base + c, o);
-        tmem_ld_wait();
+        if (kx.num > 0) {
+          tmem_ld_x32(tO + c, o);
+          tmem_ld_wait();
+        } else {
+          #pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + (row * p.heads_q + h) * kHeadDim + c);
           #pragma unroll
@@ -350,7 +417,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

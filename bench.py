@@ -1,0 +1,395 @@
+"""Throughput of attention with a learnable per-head sink, forward + backward.
+
+One step = attn_sink_fwd + attn_sink_bwd (through the C ABI) over one batch of
+the workload (default: the GPT-OSS-20B-shaped full-attention layer, B=1,
+H_q=64, H_kv=8, d=64, N=4096, causal).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU float64 oracle, on host cores
+
+Timing: CUDA events on the launching stream around the fwd and bwd calls of
+each step; a 256 MiB buffer is written between steps (outside the events) so
+every step starts with a cold L2.  Under torchrun every rank runs its own
+replica (no collective in the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from attention_learnable_head_gb300.inputs import WORKLOADS, make_case  # noqa: E402
+
+METRIC = "attention-with-sinks fwd and bwd TFLOP/s on 1 GB300; % of dense-bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- counting
+def visible_pairs(lengths, causal: bool, window: int) -> int:
+    """Visible (query, key) pairs per query head, summed over the sequences."""
+    total = 0
+    for n in lengths:
+        if not causal:
+            total += n * n
+        elif window <= 0:
+            total += n * (n + 1) // 2
+        else:
+            w = min(window, n)
+            total += w * (w + 1) // 2 + (n - w) * w
+    return total
+
+
+def algorithmic(w, lengths):
+    """Algorithmic flops (fwd 4 d, bwd 10 d per pair and head) and minimum bytes."""
+    pairs = visible_pairs(lengths, w.causal, w.window)
+    d, hq, hkv = w.head_dim, w.heads_q, w.heads_kv
+    t = sum(lengths)
+    fwd_flops = 4.0 * d * hq * pairs
+    bwd_flops = 10.0 * d * hq * pairs
+    q_bytes, kv_bytes, lse_bytes = t * hq * d * 2, t * hkv * d * 2, t * hq * 4
+    fwd_bytes = q_bytes + 2 * kv_bytes + q_bytes + lse_bytes
+    bwd_bytes = (q_bytes + 2 * kv_bytes + q_bytes + q_bytes + lse_bytes      # q k v out dout lse
+                 + q_bytes + 2 * kv_bytes + hq * 4)                          # dq dk dv dsink
+    return dict(pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, fwd_bytes=fwd_bytes,
+                 bwd_bytes=bwd_bytes)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.4)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_rate(w, case, budget_s: float):
+    """Time the CPU float64 oracle (fwd + bwd) on whole query heads of the
+    workload until ``budget_s`` is spent (at least one GQA group)."""
+    from oracle import oracle_bwd  # test infrastructure: only this leg runs it
+    torch.set_num_threads(os.cpu_count() or 1)
+    group = w.heads_q // w.heads_kv
+    cu = case.cu_seqlens
+    pairs = visible_pairs(case.lengths, w.causal, w.window)
+    done_heads, t0 = 0, time.perf_counter()
+    while done_heads < w.heads_q:
+        heads = list(range(done_heads, done_heads + group))
+        oracle_bwd(case.q, case.k, case.v, case.sink, case.dout, scale=w.scale, causal=w.causal,
+                   window=w.window, cu_seqlens_q=cu, cu_seqlens_k=cu, heads=heads)
+        done_heads += group
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 14.0 * w.head_dim * pairs * done_heads
+    return dict(value=flops / dt / 1e12, unit="TFLOP/s", cores=torch.get_num_threads(),
+                kind="oracle", seconds=dt,
+                sample=f"{w.name}: query heads 0..{done_heads - 1} of {w.heads_q}, all rows, "
+                       f"fwd+bwd in float64")
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def count_launches(fn) -> int | None:
+    """Kernels of libattn_sink launched by one call of fn (CUDA activity trace)."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+        return sum(1 for n in names if "attn_sink" in n)
+    except Exception:
+        return None
+
+
+def run_reference(args, w, case):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    steps = []
+    rates = []
+    res = None
+    for i in range(args.warmup + args.steps):
+        res = cpu_oracle_rate(w, case, budget_s=args.ref_budget)
+        if i >= args.warmup:
+            steps.append(res["seconds"])
+            rates.append(res["value"])
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "lengths": case.lengths, "heads_q": w.heads_q,
+                   "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal,
+                   "window": w.window},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"],
+                         "kind": "oracle", "sample": res["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gptoss_full", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of CPU oracle work for the cpu_baseline leg")
+    ap.add_argument("--ref-budget", type=float, default=6.0,
+                    help="seconds of CPU oracle work per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    w = WORKLOADS[args.workload]
+    case = make_case(w)
+    if args.impl == "reference":
+        run_reference(args, w, case)
+        return
+
+    from attention_learnable_head_gb300 import binding
+    from attention_learnable_head_gb300.build import build
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0 or ws == 1:
+        build()
+    if ws > 1:
+        dist.barrier()
+    binding.lib()
+
+    lengths = case.lengths
+    cu = torch.tensor(case.cu_seqlens, dtype=torch.int32, device=dev)
+    q, k, v, dout = (t.to(dev) for t in (case.q, case.k, case.v, case.dout))
+    sink = case.sink.to(dev)
+    packed = w.is_varlen
+    kw = dict(causal=w.causal, window=w.window, softmax_scale=w.scale)
+    if packed:
+        kw.update(cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=max(lengths),
+                  max_seqlen_k=max(lengths))
+    else:
+        b, n = len(lengths), lengths[0]
+        q, dout = q.view(b, n, *q.shape[1:]), dout.view(b, n, *dout.shape[1:])
+        k, v = k.view(b, n, *k.shape[1:]), v.view(b, n, *v.shape[1:])
+    p = binding.make_params(q.shape, k.shape, num_seqs=len(lengths) if packed else None,
+                            max_seqlen_q=max(lengths), max_seqlen_k=max(lengths), **kw)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.heads_q, sum(lengths)), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsink = torch.empty_like(sink)
+    nws = binding.attn_sink_bwd_workspace_size(p)
+    workspace = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+    cu_arg = cu if packed else None
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        st = binding.attn_sink_fwd(p, q, k, v, sink, cu_arg, cu_arg, out, lse)
+        if st:
+            raise binding.AttnSinkError(st, "attn_sink_fwd")
+
+    def bwd():
+        st = binding.attn_sink_bwd(p, q, k, v, sink, cu_arg, cu_arg, out, lse, dout, dq, dk, dv,
+                                   dsink, workspace, workspace.numel())
+        if st:
+            raise binding.AttnSinkError(st, "attn_sink_bwd")
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    launches_per_step = count_launches(lambda: (fwd(), bwd()))
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        fwd()
+        ev[i][1].record()
+        bwd()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    fwd_t, bwd_t = sum(fwd_ms) / n, sum(bwd_ms) / n
+    step_ms = fwd_t + bwd_t
+    if ws > 1:
+        tt = torch.tensor([step_ms, fwd_t, bwd_t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms, fwd_t, bwd_t = (float(x) for x in tt.tolist())
+
+    # end to end through the C ABI with pinned host buffers, copies inside
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dout))
+    hs = sink.cpu().pin_memory()
+    ho, hl, hdq, hdk, hdv, hds = (torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                                  for t in (out, lse, dq, dk, dv, dsink))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hs))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv, hds))
+    e2e_steps = max(3, min(n, 20))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        dout.copy_(hdo, non_blocking=True)
+        sink.copy_(hs, non_blocking=True)
+        fwd()
+        bwd()
+        for h, d_ in ((ho, out), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv), (hds, dsink)):
+            h.copy_(d_, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    st, code = binding.attn_sink_device_error()
+    if st != 0 or code != 0:
+        raise RuntimeError(f"device error word {code:#x}")
+
+    alg = algorithmic(w, lengths)
+    flops = alg["fwd_flops"] + alg["bwd_flops"]
+    value = ws * flops / (step_ms * 1e-3) / 1e12
+    fwd_tf = alg["fwd_flops"] / (fwd_t * 1e-3) / 1e12
+    bwd_tf = alg["bwd_flops"] / (bwd_t * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    dominant = "bwd" if bwd_t >= fwd_t else "fwd"
+    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": n, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": len(lengths) if not packed else None,
+                   "lengths": lengths if packed else None,
+                   "seq_len": None if packed else lengths[0], "heads_q": w.heads_q,
+                   "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal,
+                   "window": w.window, "parallelism": f"replicas x{ws}",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+        "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_ms": fwd_t, "bwd_ms": bwd_t,
+        "frac_of_peak": value / peak, "fwd_frac_of_peak": fwd_tf / peak,
+        "bwd_frac_of_peak": bwd_tf / peak, "peak_source": src,
+        "roofline": {"kernel": "attn_sink_bwd (bwd_pre + bwd_main + reductions)"
+                     if dominant == "bwd" else "attn_sink_fwd_kernel",
+                     "bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": dom_tf / peak, "traffic": None,
+                     "peak_note": f"{src} dense bf16 burst"},
+        "roofline_fwd": {"kernel": "attn_sink_fwd_kernel", "bound": "tensor",
+                         "achieved": fwd_tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": fwd_tf / peak,
+                         "hbm_gbs": alg["fwd_bytes"] / (fwd_t * 1e-3) / 1e9},
+        "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": None if launches_per_step is None else launches_per_step * n,
+        "gpu_launches_per_step": launches_per_step,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_rate(w, case, budget_s=args.cpu_budget)
+        line["cpu_baseline"].pop("seconds", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -3,6 +3,8 @@ and compare with the float64 oracle element by element.
 
 Tolerances (bf16 inputs, fp32 accumulation):
   out, dq, dk, dv : max |err| <= 2e-2 and ||err||_F / ||ref||_F <= 5e-3
+                    (for bf16-stored results the max-abs bar is taken beyond
+                    the half-ulp rounding of the bf16 store itself)
   dsink           : ||err||_2 / ||ref||_2 <= 1e-2 over the heads checked
   lse             : max |err| <= 1e-3 (natural log)
 """
@@ -30,9 +32,29 @@ def err_stats(got: torch.Tensor, ref: torch.Tensor):
     return max_abs, rel
 
 
+def bf16_half_ulp(ref: torch.Tensor) -> torch.Tensor:
+    """Half a bf16 ulp at |ref|: the rounding any bf16-stored result carries."""
+    a = ref.abs().clamp_min(2.0 ** -126)
+    return torch.exp2(torch.floor(torch.log2(a)) - 8)
+
+
 def assert_close(name, got, ref, max_abs=TOL_MAX_ABS, rel_fro=TOL_REL_FRO):
+    """max |got - ref| <= max_abs and relative Frobenius error <= rel_fro.
+
+    For a bf16-stored result the max-abs bar is taken on top of the storage
+    rounding (half a bf16 ulp of the reference value); fp32-stored results
+    meet the bar as it stands."""
     a, r = err_stats(got, ref)
-    assert a <= max_abs and r <= rel_fro, f"{name}: max abs {a:.3e} (<= {max_abs}), rel fro {r:.3e} (<= {rel_fro})"
+    if got.dtype == torch.bfloat16:
+        g, rr = got.double().cpu(), ref.double().cpu()
+        m = ~torch.isnan(rr)
+        excess = ((g - rr).abs() - bf16_half_ulp(rr))[m]
+        a_eff = max(0.0, excess.max().item()) if excess.numel() else 0.0
+    else:
+        a_eff = a
+    assert a_eff <= max_abs and r <= rel_fro, (
+        f"{name}: max abs {a:.3e} (beyond storage rounding {a_eff:.3e}, <= {max_abs}), "
+        f"rel fro {r:.3e} (<= {rel_fro})")
     return a, r
 
 
