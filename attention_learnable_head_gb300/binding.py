@@ -68,13 +68,13 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER(AttnSinkParams)
     L.attn_sink_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                c_void_p, c_void_p, c_void_p]
+                                c_void_p, c_void_p, c_void_p, c_void_p]
     L.attn_sink_fwd.restype = c_int
     L.attn_sink_bwd_workspace_size.argtypes = [P]
     L.attn_sink_bwd_workspace_size.restype = c_size_t
     L.attn_sink_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                c_void_p, c_void_p, c_size_t, c_void_p]
+                                c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     L.attn_sink_bwd.restype = c_int
     L.attn_sink_status_string.argtypes = [c_int]
     L.attn_sink_status_string.restype = ctypes.c_char_p
@@ -105,23 +105,25 @@ def _stream(stream) -> int | None:
 
 
 # ----------------------------------------------------------------------------- C entry points
-def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse,
-                  stream=None) -> int:
+def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out,
+                  out_residual, lse, stream=None) -> int:
     return lib().attn_sink_fwd(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
-                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out), _ptr(lse),
-                               _stream(stream))
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                               _ptr(out_residual), _ptr(lse), _stream(stream))
 
 
 def attn_sink_bwd_workspace_size(params: AttnSinkParams) -> int:
     return int(lib().attn_sink_bwd_workspace_size(_pref(params)))
 
 
-def attn_sink_bwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse,
-                  dout, dq, dk, dv, dsink, workspace, workspace_bytes: int, stream=None) -> int:
+def attn_sink_bwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out,
+                  out_residual, lse, dout, dq, dk, dv, dsink, workspace, workspace_bytes: int,
+                  stream=None) -> int:
     return lib().attn_sink_bwd(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
-                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out), _ptr(lse),
-                               _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dsink),
-                               _ptr(workspace), int(workspace_bytes), _stream(stream))
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                               _ptr(out_residual), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(dsink), _ptr(workspace), int(workspace_bytes),
+                               _stream(stream))
 
 
 def attn_sink_status_string(status: int) -> str:
@@ -171,22 +173,26 @@ def _lse_len(q) -> int:
 
 def forward(q, k, v, sink, *, causal: bool = True, window: int = 0,
             softmax_scale: float | None = None, cu_seqlens_q=None, cu_seqlens_k=None,
-            max_seqlen_q: int | None = None, max_seqlen_k: int | None = None, stream=None):
-    """out (like q, bf16) and lse ([H_q, T_q] fp32)."""
+            max_seqlen_q: int | None = None, max_seqlen_k: int | None = None,
+            residual: bool = True, stream=None):
+    """(out, lse, out_residual): out like q (bf16), lse [H_q, T_q] fp32, and the
+    bf16 rounding residual of out (None when residual=False)."""
     num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
                     num_seqs=num_seqs, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
     out = torch.empty_like(q)
+    res = torch.empty_like(q) if residual else None
     lse = torch.empty((q.shape[-2], _lse_len(q)), dtype=torch.float32, device=q.device)
-    _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse, stream),
+    _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, res, lse, stream),
            "attn_sink_fwd")
-    return out, lse
+    return out, lse, res
 
 
-def backward(q, k, v, sink, out, lse, dout, *, causal: bool = True, window: int = 0,
-             softmax_scale: float | None = None, cu_seqlens_q=None, cu_seqlens_k=None,
-             max_seqlen_q: int | None = None, max_seqlen_k: int | None = None,
-             grad_dtype: int = 0, workspace=None, stream=None):
+def backward(q, k, v, sink, out, lse, dout, *, out_residual=None, causal: bool = True,
+             window: int = 0, softmax_scale: float | None = None, cu_seqlens_q=None,
+             cu_seqlens_k=None, max_seqlen_q: int | None = None,
+             max_seqlen_k: int | None = None, grad_dtype: int = 0, workspace=None,
+             stream=None):
     """dq, dk, dv (bf16, or fp32 when grad_dtype = 1) and dsink ([H_q] fp32)."""
     num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
@@ -200,8 +206,9 @@ def backward(q, k, v, sink, out, lse, dout, *, causal: bool = True, window: int 
     nbytes = attn_sink_bwd_workspace_size(p)
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
-    _check(attn_sink_bwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, lse, dout, dq, dk,
-                         dv, dsink, workspace, workspace.numel(), stream), "attn_sink_bwd")
+    _check(attn_sink_bwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                         dout, dq, dk, dv, dsink, workspace, workspace.numel(), stream),
+           "attn_sink_bwd")
     return dq, dk, dv, dsink
 
 
@@ -213,19 +220,20 @@ class AttnSinkFunction(torch.autograd.Function):
                 max_seqlen_q, max_seqlen_k):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         sink32 = sink.detach().float().contiguous()
-        out, lse = forward(q, k, v, sink32, causal=causal, window=window,
-                           softmax_scale=softmax_scale, cu_seqlens_q=cu_seqlens_q,
-                           cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
-                           max_seqlen_k=max_seqlen_k)
-        ctx.save_for_backward(q, k, v, sink32, out, lse, cu_seqlens_q, cu_seqlens_k)
+        out, lse, res = forward(q, k, v, sink32, causal=causal, window=window,
+                                softmax_scale=softmax_scale, cu_seqlens_q=cu_seqlens_q,
+                                cu_seqlens_k=cu_seqlens_k, max_seqlen_q=max_seqlen_q,
+                                max_seqlen_k=max_seqlen_k)
+        ctx.save_for_backward(q, k, v, sink32, out, res, lse, cu_seqlens_q, cu_seqlens_k)
         ctx.cfg = (causal, window, softmax_scale, max_seqlen_q, max_seqlen_k, sink.dtype)
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        q, k, v, sink32, out, lse, cu_q, cu_k = ctx.saved_tensors
+        q, k, v, sink32, out, res, lse, cu_q, cu_k = ctx.saved_tensors
         causal, window, scale, mq, mk, sink_dtype = ctx.cfg
-        dq, dk, dv, dsink = backward(q, k, v, sink32, out, lse, dout.contiguous(), causal=causal,
+        dq, dk, dv, dsink = backward(q, k, v, sink32, out, lse, dout.contiguous(),
+                                     out_residual=res, causal=causal,
                                      window=window, softmax_scale=scale, cu_seqlens_q=cu_q,
                                      cu_seqlens_k=cu_k, max_seqlen_q=mq, max_seqlen_k=mk)
         return dq, dk, dv, dsink.to(sink_dtype), None, None, None, None, None, None, None

@@ -127,13 +127,14 @@ int validate(const attn_sink_params* p, const int* cu_q, const int* cu_k, Geomet
   return ATTN_SINK_OK;
 }
 
-int encode_rows(CUtensorMap* m, const void* ptr, int tokens, int heads) {
+int encode_rows(CUtensorMap* m, const void* ptr, int tokens, int heads,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   if (!load_encode()) return ATTN_SINK_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
   cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kBlockM};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+  CUresult r = g_encode(m, dtype, 3, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -171,7 +172,7 @@ int choose_split(const attn_sink_params* p, const Geometry& g, int sm_count) {
 }
 
 struct BwdLayout {
-  size_t off_D, off_part, off_dq, off_dk, off_dv, total;
+  size_t off_D, off_part, off_dq, off_dk, off_dv, off_q16, off_do16, off_k16, off_v16, total;
   int n_blocks;
   int split;
 };
@@ -192,6 +193,16 @@ BwdLayout bwd_layout(const attn_sink_params* p, const Geometry& g, int sm_count)
   if (L.split > 1) off += align256(kv_part);
   L.off_dv = off;
   if (L.split > 1) off += align256(kv_part);
+  const size_t q16 = (size_t)g.total_q * p->heads_q * kHeadDim * 2;
+  const size_t k16 = (size_t)g.total_k * p->heads_kv * kHeadDim * 2;
+  L.off_q16 = off;
+  off += align256(q16);
+  L.off_do16 = off;
+  off += align256(q16);
+  L.off_k16 = off;
+  off += align256(k16);
+  L.off_v16 = off;
+  off += align256(k16);
   L.total = off;
   return L;
 }
@@ -223,7 +234,7 @@ const char* attn_sink_status_string(int status) {
 
 int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
                   const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                  void* out, float* lse, void* stream) {
+                  void* out, void* out_residual, float* lse, void* stream) {
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -231,7 +242,8 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   if (q == nullptr || sink == nullptr || out == nullptr || lse == nullptr)
     return ATTN_SINK_ERR_INVALID_ARG;
   if (g.total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_SINK_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(out_residual))
     return ATTN_SINK_ERR_INVALID_ARG;
   int sms = 0;
   int* err = nullptr;
@@ -252,6 +264,7 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   fp.cu_k = cu_seqlens_k;
   fp.sink = sink;
   fp.out = static_cast<__nv_bfloat16*>(out);
+  fp.out_lo = static_cast<__nv_bfloat16*>(out_residual);
   fp.lse = lse;
   fp.err = err;
   fp.seqlen_q = g.varlen ? 0 : params->seqlen_q;
@@ -283,9 +296,9 @@ size_t attn_sink_bwd_workspace_size(const attn_sink_params* params) {
 
 int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
                   const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                  const void* out, const float* lse, const void* dout, void* dq, void* dk,
-                  void* dv, float* dsink, void* workspace, size_t workspace_bytes,
-                  void* stream) {
+                  const void* out, const void* out_residual, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* dsink,
+                  void* workspace, size_t workspace_bytes, void* stream) {
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -296,7 +309,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
   if (g.total_k > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr))
     return ATTN_SINK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(out_residual))
     return ATTN_SINK_ERR_INVALID_ARG;
   int sms = 0;
   int* err = nullptr;
@@ -312,10 +325,19 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
   float* dq_acc = params->grad_dtype == 1 ? static_cast<float*>(dq)
                                           : reinterpret_cast<float*>(ws + L.off_dq);
   const float scale = params->softmax_scale;
+  uint16_t* q16 = reinterpret_cast<uint16_t*>(ws + L.off_q16);
+  uint16_t* do16 = reinterpret_cast<uint16_t*>(ws + L.off_do16);
+  uint16_t* k16 = reinterpret_cast<uint16_t*>(ws + L.off_k16);
+  uint16_t* v16 = reinterpret_cast<uint16_t*>(ws + L.off_v16);
 
-  // 1. D, dsink partials, zero the dq accumulator
+  // 1. D, dsink partials, fp16 operand copies, zero the dq accumulator
   if (g.total_q > 0) {
     PreParams pp;
+    pp.q = static_cast<const __nv_bfloat16*>(q);
+    pp.out_lo = static_cast<const __nv_bfloat16*>(out_residual);
+    pp.q16 = q16;
+    pp.do16 = do16;
+    pp.err = err;
     pp.out = static_cast<const __nv_bfloat16*>(out);
     pp.dout = static_cast<const __nv_bfloat16*>(dout);
     pp.lse = lse;
@@ -329,19 +351,32 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     attn_sink_bwd_pre_kernel<<<dim3(L.n_blocks, params->heads_q), 256, 0, s>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
   }
+  if (g.total_k > 0) {
+    const size_t n8 = (size_t)g.total_k * params->heads_kv * kHeadDim / 8;
+    const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
+    attn_sink_kv_convert_kernel<<<blocks, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), k16, v16, n8,
+        err);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+  }
   // 2. main loop: dK, dV (and their split partials), dQ accumulation
   const int n_ktiles = (g.max_k + kBlockN - 1) / kBlockN;
   if (g.total_k > 0 && g.num_seqs > 0 && n_ktiles > 0) {
     BwdParams bp;
     std::memset(&bp, 0, sizeof(bp));
-    const void* qp = g.total_q > 0 ? q : k;
-    const void* op = g.total_q > 0 ? dout : k;
+    // An empty query tensor is never read (no key tile has a query); its maps
+    // only need a valid address.
+    const void* qp = g.total_q > 0 ? (const void*)q16 : (const void*)k16;
+    const void* op = g.total_q > 0 ? (const void*)do16 : (const void*)k16;
     const int tq = g.total_q > 0 ? g.total_q : 1;
     const int hq = g.total_q > 0 ? params->heads_q : 1;
-    if ((st = encode_rows(&bp.tm_q, qp, tq, hq)) != ATTN_SINK_OK) return st;
-    if ((st = encode_rows(&bp.tm_do, op, tq, hq)) != ATTN_SINK_OK) return st;
-    if ((st = encode_rows(&bp.tm_k, k, g.total_k, params->heads_kv)) != ATTN_SINK_OK) return st;
-    if ((st = encode_rows(&bp.tm_v, v, g.total_k, params->heads_kv)) != ATTN_SINK_OK) return st;
+    const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((st = encode_rows(&bp.tm_q, qp, tq, hq, f16)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&bp.tm_do, op, tq, hq, f16)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&bp.tm_k, k16, g.total_k, params->heads_kv, f16)) != ATTN_SINK_OK)
+      return st;
+    if ((st = encode_rows(&bp.tm_v, v16, g.total_k, params->heads_kv, f16)) != ATTN_SINK_OK)
+      return st;
     bp.cu_q = cu_seqlens_q;
     bp.cu_k = cu_seqlens_k;
     bp.lse = lse;

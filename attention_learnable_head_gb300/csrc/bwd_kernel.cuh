@@ -1,13 +1,17 @@
 // Backward kernels: attention with a per-head sink, sm_103a.
 //
-//   bwd_pre     D_i = sum_d dout_i[d] * out_i[d] (fp32, from the stored bf16 out),
-//               per-block partials of dsink[h] = -sum_i exp(sink[h] - lse_i) * D_i
-//               (the sink gradient of section "反向传播" on the euno.news page:
-//               P_ih = exp(sink[h] - lse_i) because lse includes the sink), and
-//               zeroes the fp32 dq accumulator.
+//   bwd_pre     D_i = sum_d dout_i[d] * out_i[d] (fp32; out = the stored bf16 out
+//               plus, when given, its bf16 residual), per-block partials of
+//               dsink[h] = -sum_i exp(sink[h] - lse_i) * D_i (the sink gradient of
+//               section "反向传播" on the euno.news page: P_ih = exp(sink[h] - lse_i)
+//               because lse includes the sink), fp16 copies of q and dout for the
+//               tensor cores, and zeroes the fp32 dq accumulator.
+//   kv_convert  fp16 copies of k and v.
 //   bwd_main    key/value-stationary: one CTA per (kv head, sequence, 128 keys).
 //               Loops over the query heads of the GQA group and the query tiles
-//               that can see these keys; per step five tcgen05 MMAs:
+//               that can see these keys; per step five tcgen05 MMAs, all on
+//               fp16 operands (the inputs convert exactly; P and dS keep 11
+//               significand bits instead of bf16's 8):
 //                 S^T  = K Q^T        dP^T = V dO^T            (TMEM, fp32)
 //                 P^T  = exp(S^T * scale - lse)  dS^T = P^T o (dP^T - D)
 //                 dV  += P^T dO       (A = P^T from TMEM)
@@ -35,10 +39,10 @@ constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ
                    kColPT = 448;
 
 struct BwdParams {
-  CUtensorMap tm_q;    // [T_q][H_q][64]
-  CUtensorMap tm_do;   // [T_q][H_q][64]
-  CUtensorMap tm_k;    // [T_k][H_kv][64]
-  CUtensorMap tm_v;
+  CUtensorMap tm_q;    // [T_q][H_q][64] fp16 copy of q
+  CUtensorMap tm_do;   // [T_q][H_q][64] fp16 copy of dout
+  CUtensorMap tm_k;    // [T_k][H_kv][64] fp16 copy of k
+  CUtensorMap tm_v;    // fp16 copy of v
   const int* cu_q;
   const int* cu_k;
   const float* lse;    // [H_q][T_q]
@@ -62,13 +66,18 @@ struct BwdParams {
 
 // ------------------------------------------------------------------ bwd_pre
 struct PreParams {
+  const __nv_bfloat16* q;
   const __nv_bfloat16* out;
+  const __nv_bfloat16* out_lo;   // residual of out, or null
   const __nv_bfloat16* dout;
   const float* lse;
   const float* sink;
   float* D;            // [H_q][T_q]
   float* partials;     // [H_q][n_blocks]
   float* dq_acc;       // [T_q][H_q][64]
+  uint16_t* q16;       // [T_q][H_q][64] fp16 copy of q
+  uint16_t* do16;      // [T_q][H_q][64] fp16 copy of dout
+  int* err;
   int total_q, heads_q, n_blocks;
 };
 
@@ -80,6 +89,7 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
   const int rloc = tid >> 3;        // 0..31
   const float sink_h = p.sink[h];
   float acc = 0.0f;                 // dsink contribution of this thread's rows
+  bool overflow = false;
   #pragma unroll 1
   for (int pass = 0; pass < kPreRows / 32; ++pass) {
     const int t = blk * kPreRows + pass * 32 + rloc;
@@ -88,15 +98,22 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
       const size_t base = ((size_t)t * p.heads_q + h) * kHeadDim + sub * 8;
       const uint4 o = *reinterpret_cast<const uint4*>(p.out + base);
       const uint4 g = *reinterpret_cast<const uint4*>(p.dout + base);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+      const uint4 qq = *reinterpret_cast<const uint4*>(p.q + base);
+      uint4 ol = make_uint4(0, 0, 0, 0);
+      if (p.out_lo) ol = *reinterpret_cast<const uint4*>(p.out_lo + base);
+      const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+      const uint32_t lw[4] = {ol.x, ol.y, ol.z, ol.w};
       #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float2 a = __bfloat1622float2(o2[u]);
-        const float2 b = __bfloat1622float2(g2[u]);
-        d = fmaf(a.x, b.x, d);
-        d = fmaf(a.y, b.y, d);
+        d = fmaf(bf16_lo(ow[u]) + bf16_lo(lw[u]), bf16_lo(gw[u]), d);
+        d = fmaf(bf16_hi(ow[u]) + bf16_hi(lw[u]), bf16_hi(gw[u]), d);
       }
+      *reinterpret_cast<uint4*>(p.q16 + base) =
+          make_uint4(bf16x2_to_f16x2(qq.x, &overflow), bf16x2_to_f16x2(qq.y, &overflow),
+                     bf16x2_to_f16x2(qq.z, &overflow), bf16x2_to_f16x2(qq.w, &overflow));
+      *reinterpret_cast<uint4*>(p.do16 + base) =
+          make_uint4(bf16x2_to_f16x2(g.x, &overflow), bf16x2_to_f16x2(g.y, &overflow),
+                     bf16x2_to_f16x2(g.z, &overflow), bf16x2_to_f16x2(g.w, &overflow));
       float4* z = reinterpret_cast<float4*>(p.dq_acc + base);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -112,6 +129,7 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
         acc -= ex2_approx((sink_h - lse) * kLog2e) * d;
     }
   }
+  if (overflow) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
   // fixed-order reduction: lanes (xor tree), then warps in index order
   #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -124,6 +142,26 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
     for (int w = 0; w < 8; ++w) s += wsum[w];
     p.partials[(size_t)h * p.n_blocks + blk] = s;
   }
+}
+
+// ------------------------------------------------------------------ kv_convert
+// fp16 copies of k and v (n8 = elements / 8 of each).
+__global__ void __launch_bounds__(256) attn_sink_kv_convert_kernel(
+    const __nv_bfloat16* k, const __nv_bfloat16* v, uint16_t* k16, uint16_t* v16, size_t n8,
+    int* err) {
+  bool overflow = false;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 a = reinterpret_cast<const uint4*>(k)[i];
+    const uint4 b = reinterpret_cast<const uint4*>(v)[i];
+    reinterpret_cast<uint4*>(k16)[i] =
+        make_uint4(bf16x2_to_f16x2(a.x, &overflow), bf16x2_to_f16x2(a.y, &overflow),
+                   bf16x2_to_f16x2(a.z, &overflow), bf16x2_to_f16x2(a.w, &overflow));
+    reinterpret_cast<uint4*>(v16)[i] =
+        make_uint4(bf16x2_to_f16x2(b.x, &overflow), bf16x2_to_f16x2(b.y, &overflow),
+                   bf16x2_to_f16x2(b.z, &overflow), bf16x2_to_f16x2(b.w, &overflow));
+  }
+  if (overflow) atomicCAS(err, 0, DEVERR_FP16_RANGE);
 }
 
 // ------------------------------------------------------------------ dsink_reduce
@@ -257,7 +295,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint8_t* sV = sK + kTileBytes;
   uint8_t* sQ = sV + kTileBytes;                      // kBwdStages tiles
   uint8_t* sdO = sQ + kBwdStages * kTileBytes;        // kBwdStages tiles
-  uint8_t* sdS = sdO + kBwdStages * kTileBytes;       // [128 keys][128 queries] bf16
+  uint8_t* sdS = sdO + kBwdStages * kTileBytes;       // [128 keys][128 queries] fp16
 
   if (num == 0) {
     // No query sees these keys: dK = dV = 0.
@@ -349,9 +387,9 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = make_idesc_bf16(kBlockN, kBlockM, false, false);   // S^T, dP^T
-      const uint32_t id_dvdk = make_idesc_bf16(kBlockN, kHeadDim, false, true);
-      const uint32_t id_dq = make_idesc_bf16(kBlockM, kHeadDim, true, true);
+      const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM, false, false);  // S^T, dP^T
+      const uint32_t id_dvdk = make_idesc(kFmtF16, kBlockN, kHeadDim, false, true);
+      const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aS = smem_u32(sdS);
       bool ok = mbar_wait(&kv_full, 0, &abort_flag);
       for (int m = 0; ok && m < num; ++m) {
@@ -362,11 +400,11 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         const uint32_t aO = smem_u32(sdO + st * kTileBytes);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_bf16_ss(tmem + kColST, make_sdesc_sw128(aK + 32 * k, 16, 1024),
+          mma_ss(tmem + kColST, make_sdesc_sw128(aK + 32 * k, 16, 1024),
                       make_sdesc_sw128(aQ + 32 * k, 16, 1024), id_s, k > 0);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_bf16_ss(tmem + kColDPT, make_sdesc_sw128(aV + 32 * k, 16, 1024),
+          mma_ss(tmem + kColDPT, make_sdesc_sw128(aV + 32 * k, 16, 1024),
                       make_sdesc_sw128(aO + 32 * k, 16, 1024), id_s, k > 0);
         mma_commit(&s_full);
         if (!mbar_wait(&p_full, m & 1, &abort_flag)) { ok = false; break; }
@@ -374,12 +412,12 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         // dV += P^T dO  (A: P^T in TMEM, K = query index; B: dO tile read MN-major)
         #pragma unroll
         for (int k = 0; k < kBlockM / 16; ++k)
-          mma_bf16_ts(tmem + kColDV, tmem + kColPT + 8 * k,
+          mma_ts(tmem + kColDV, tmem + kColPT + 8 * k,
                       make_sdesc_sw128(aO + k * 2048, 16384, 1024), id_dvdk, (m > 0 || k > 0));
         // dK += dS^T Q  (A: dS^T in SMEM, K-major over queries; B: Q read MN-major)
         #pragma unroll
         for (int k = 0; k < kBlockM / 16; ++k)
-          mma_bf16_ss(tmem + kColDK,
+          mma_ss(tmem + kColDK,
                       make_sdesc_sw128(aS + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
                       make_sdesc_sw128(aQ + k * 2048, 16384, 1024), id_dvdk, (m > 0 || k > 0));
         if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
@@ -387,7 +425,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         // dQ = dS K  (A: dS^T SMEM read MN-major, M = queries; B: K read MN-major)
         #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k)
-          mma_bf16_ss(tmem + kColDQ, make_sdesc_sw128(aS + k * 2048, 16384, 1024),
+          mma_ss(tmem + kColDQ, make_sdesc_sw128(aS + k * 2048, 16384, 1024),
                       make_sdesc_sw128(aK + k * 2048, 16384, 1024), id_dq, k > 0);
         mma_commit(&mma2_done);
         mma_commit(&q_empty[st]);
@@ -444,8 +482,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
             pv[u] = pe;
             dv[u] = pe * (__uint_as_float(dr[e + u]) - s_D[st][ci]);
           }
-          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+          pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
+          dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
         }
         tmem_st_x16(tmem + lane_base + kColPT + (c >> 1), pk);
         // dS^T row r, queries c..c+31: 4 chunks of 16 bytes in sub-tile c/64

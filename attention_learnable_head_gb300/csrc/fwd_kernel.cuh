@@ -7,8 +7,13 @@
 //   S = Q K^T (tcgen05, fp32 accumulators in TMEM),
 //   online softmax whose running max and sum start from the sink logit
 //   (m0 = sink[h] * log2 e, l0 = 1 in the exp2 domain),
-//   P (bf16) written to TMEM and consumed there by O += P V (tcgen05, A from TMEM),
-// then out = O / l and lse = ln 2 * (m + log2 l), which includes the sink.
+//   P (fp16) written to TMEM and consumed there by O += P V (tcgen05, A from
+//   TMEM, V converted to fp16 in SMEM by a converter warp),
+// then out = O / l (bf16, plus optionally the bf16 residual O/l - out) and
+// lse = ln 2 * (m + log2 l), which includes the sink.  S = Q K^T multiplies the
+// bf16 inputs exactly; P and V go to the tensor cores as fp16 (11-bit
+// significand) so that O, and the backward's D = rowsum(dO o O), keep ~3 more
+// bits than a bf16 P would give.
 // The sink joins the softmax denominator only: it is the extra column of the
 // concat listing "带汇聚的注意力（GPT-OSS）" on the euno.news page, and the
 // P_ij / P_ih equations of its section "数学公式".
@@ -17,13 +22,14 @@
 // when a row's max grows by more than kRescaleThreshold (log2 units); P stays
 // below 2^threshold, and out/lse are exact because l and O use the same max.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  softmax + epilogue of tile A (thread t owns row t = TMEM lane t)
 //   warps 4-7  softmax + epilogue of tile B
 //   warp 8     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
 //   warp 9     MMA issuer (one lane) and TMEM owner
+//   warp 10    converts each landed V tile from bf16 to fp16 in place
 // TMEM columns: S_A 0, S_B 128 (128 fp32 each), O_A 256, O_B 320 (64 each),
-//               P_A 384, P_B 448 (128 bf16 packed in 64 columns each).
+//               P_A 384, P_B 448 (128 fp16 packed in 64 columns each).
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -35,7 +41,7 @@ constexpr int kBlockN = 128;   // keys per tile
 constexpr int kHeadDim = 64;
 constexpr int kFwdTiles = 2;   // query tiles per CTA
 constexpr int kFwdStages = 4;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;
 constexpr int kFwdRowsPerCta = kFwdTiles * kBlockM;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
 constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
@@ -52,6 +58,7 @@ struct FwdParams {
   const int* cu_k;
   const float* sink;  // [H_q]
   __nv_bfloat16* out; // [T_q][H_q][64]
+  __nv_bfloat16* out_lo; // [T_q][H_q][64] residual O/l - out, or null
   float* lse;         // [H_q][T_q]
   int* err;           // device error word
   int seqlen_q, seqlen_k;
@@ -109,6 +116,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, mma_drained;
   __shared__ __align__(8) uint64_t k_full[kFwdStages], v_full[kFwdStages], kv_empty[kFwdStages];
+  __shared__ __align__(8) uint64_t v_conv[kFwdStages];
   __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -148,6 +156,11 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.heads_q + h) * kHeadDim);
         #pragma unroll
         for (int c = 0; c < 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+        if (p.out_lo) {
+          uint4* ol = reinterpret_cast<uint4*>(p.out_lo + (row * p.heads_q + h) * kHeadDim);
+          #pragma unroll
+          for (int c = 0; c < 8; ++c) ol[c] = make_uint4(0, 0, 0, 0);
+        }
         p.lse[(size_t)h * p.total_q + row] = sink_h;
       }
     }
@@ -168,6 +181,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_conv[s], 32);
     }
     for (int x = 0; x < kFwdTiles; ++x) {
       mbar_init(&s_full[x], 1);
@@ -225,7 +239,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
-      const uint32_t idesc_o = make_idesc_bf16(kBlockM, kHeadDim, false, true);
+      const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
       const KeyRange kr[kFwdTiles] = {kr_a, kr_b};
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
       // S_x(n) = Q_x K_n^T into S_x; n is a union index.
@@ -237,7 +251,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         const uint32_t aK = smem_u32(sK + st * kTileBytes);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_bf16_ss(tmem + x * 128, make_sdesc_sw128(aQ + 32 * k, 16, 1024),
+          mma_ss(tmem + x * 128, make_sdesc_sw128(aQ + 32 * k, 16, 1024),
                       make_sdesc_sw128(aK + 32 * k, 16, 1024), idesc_s, k > 0);
         mma_commit(&s_full[x]);
         return true;
@@ -255,7 +269,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           if (!ok || !in_range(x, n)) continue;
           const int local = lo + n - kr[x].lo;
           if (!mbar_wait(&p_full[x], local & 1, &abort_flag) ||
-              !mbar_wait(&v_full[st], (n / kFwdStages) & 1, &abort_flag)) {
+              !mbar_wait(&v_conv[st], (n / kFwdStages) & 1, &abort_flag)) {
             ok = false;
             break;
           }
@@ -265,7 +279,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           const uint32_t tO = tmem + 256 + x * 64;
           #pragma unroll
           for (int k = 0; k < kBlockN / 16; ++k)
-            mma_bf16_ts(tO, tP + 8 * k, make_sdesc_sw128(aV + k * 2048, 16384, 1024), idesc_o,
+            mma_ts(tO, tP + 8 * k, make_sdesc_sw128(aV + k * 2048, 16384, 1024), idesc_o,
                         (local > 0 || k > 0));
           mma_commit(&pv_done[x]);
           if (in_range(x, n + 1)) ok = issue_s(x, n + 1);
@@ -280,6 +294,32 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       mma_commit(&mma_drained);
       mbar_wait(&mma_drained, 0, nullptr);
     }
+  } else if (warp == 10) {
+    // ---------------------------------------------------------------- V converter
+    bool overflow = false;
+    for (int it = 0; it < num; ++it) {
+      const int st = it % kFwdStages;
+      if (!mbar_wait_warp(&v_full[st], (it / kFwdStages) & 1, &abort_flag)) {
+        if (lane == 0) {
+          abort_flag = 1;
+          atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 4);
+        }
+        break;
+      }
+      uint4* tile = reinterpret_cast<uint4*>(sV + st * kTileBytes);
+      #pragma unroll 4
+      for (int c = lane; c < (int)(kTileBytes / 16); c += 32) {
+        uint4 w = tile[c];
+        w.x = bf16x2_to_f16x2(w.x, &overflow);
+        w.y = bf16x2_to_f16x2(w.y, &overflow);
+        w.z = bf16x2_to_f16x2(w.z, &overflow);
+        w.w = bf16x2_to_f16x2(w.w, &overflow);
+        tile[c] = w;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&v_conv[st]);
+    }
+    if (overflow) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
   } else {
     // ---------------------------------------------------------------- softmax warps
     const int x = warp >> 2;                 // tile 0 (A) or 1 (B)
@@ -369,7 +409,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           const float e0 = ex2_approx(fmaf(__uint_as_float(a[e]), sl2, -m_use));
           const float e1 = ex2_approx(fmaf(__uint_as_float(a[e + 1]), sl2, -m_use));
           rowsum += e0 + e1;
-          pk[e >> 1] = pack_bf16x2(e0, e1);
+          pk[e >> 1] = pack_f16x2(e0, e1);
         }
         tmem_st_x16(tP + (c >> 1), pk);
       }
@@ -399,14 +439,22 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (row * p.heads_q + h) * kHeadDim + c);
+          const size_t base = (row * p.heads_q + h) * kHeadDim + c;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + base);
+          uint4* dlo = p.out_lo ? reinterpret_cast<uint4*>(p.out_lo + base) : nullptr;
           #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float* f = reinterpret_cast<const float*>(o + 8 * u);
-            dst[u] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
-                                pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
-                                pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
-                                pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+            float f[8];
+            uint32_t hi[4], lo[4];
+            #pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * u + e]) * inv_l;
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+              lo[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
+            }
+            dst[u] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            if (dlo) dlo[u] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
       }

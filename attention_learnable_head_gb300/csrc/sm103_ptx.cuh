@@ -27,6 +27,7 @@ enum : int {
   DEVERR_NONE = 0,
   DEVERR_TIMEOUT_FWD = 0x100,
   DEVERR_TIMEOUT_BWD = 0x200,
+  DEVERR_FP16_RANGE = 0x400,   // an input lies outside the fp16 range of the MMA operands
 };
 
 // Give up on an mbarrier after this many nanoseconds.  Every legitimate wait
@@ -184,14 +185,22 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
 // ----------------------------------------------------------------------------
 // tcgen05: MMA
 // ----------------------------------------------------------------------------
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   15 A major (1 = MN-major), 16 B major, 17-22 N>>3, 24-28 M>>4.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major,
-                                                       bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+// Instruction descriptor for kind::f16 with fp32 accumulation.
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always share one type here), 15 A major (1 = MN-major),
+//   16 B major, 17-22 N>>3, 24-28 M>>4.
+enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1 };
+
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, int M, int N, bool a_mn_major,
+                                                  bool b_mn_major) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool a_mn_major,
+                                                       bool b_mn_major) {
+  return make_idesc(kFmtBF16, M, N, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -209,8 +218,9 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
   return d;
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T-as-described.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem] (kind::f16: A and B both f16 or both bf16,
+// as the instruction descriptor says).
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -220,8 +230,9 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: A is M lanes x K bf16, two per 32-bit column.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// D[tmem] (+)= A[tmem] * B[smem]: A is M lanes x K 16-bit values, two per
+// 32-bit column (even K index in the low half).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -314,6 +325,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   // cvt packs its first source into the upper half.
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two bf16 (one 32-bit word, low half first) widened to fp32 exactly.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Largest finite fp16 magnitude: bf16 values beyond it do not survive the
+// conversion to the fp16 tensor-core operands.
+constexpr float kF16Max = 65504.0f;
+
+// bf16x2 -> f16x2 (round to nearest even; exact for |x| in the fp16 normal
+// range).  Sets *overflow when a finite input does not fit fp16.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool* overflow) {
+  const float a = bf16_lo(w), b = bf16_hi(w);
+  if (fabsf(a) > kF16Max || fabsf(b) > kF16Max) *overflow = true;
+  return pack_f16x2(a, b);
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled

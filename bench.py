@@ -164,17 +164,24 @@ def dist_env():
     return ws, rank, local
 
 
-def count_launches(fn) -> int | None:
-    """Kernels of libattn_sink launched by one call of fn (CUDA activity trace)."""
+def count_launches(fn):
+    """Kernels of libattn_sink launched by one call of fn (CUDA activity trace):
+    (count, kernel names)."""
     try:
         from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
             fn()
             torch.cuda.synchronize()
-        names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
-        return sum(1 for n in names if "attn_sink" in n)
-    except Exception:
-        return None
+        names = []
+        try:
+            for e in prof.profiler.kineto_results.events():
+                names.append(e.name())
+        except Exception:
+            names = [e.name for e in prof.events()]
+        mine = [n for n in names if "attn_sink" in n and "kernel" in n]
+        return len(mine), sorted(set(mine))
+    except Exception as exc:  # profiler unavailable: report unknown
+        return None, [f"profiler error: {exc}"]
 
 
 def run_reference(args, w, case):
@@ -261,6 +268,7 @@ def main():
     p = binding.make_params(q.shape, k.shape, num_seqs=len(lengths) if packed else None,
                             max_seqlen_q=max(lengths), max_seqlen_k=max(lengths), **kw)
     out = torch.empty_like(q)
+    out_res = torch.empty_like(q)
     lse = torch.empty((w.heads_q, sum(lengths)), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dsink = torch.empty_like(sink)
@@ -270,13 +278,13 @@ def main():
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def fwd():
-        st = binding.attn_sink_fwd(p, q, k, v, sink, cu_arg, cu_arg, out, lse)
+        st = binding.attn_sink_fwd(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse)
         if st:
             raise binding.AttnSinkError(st, "attn_sink_fwd")
 
     def bwd():
-        st = binding.attn_sink_bwd(p, q, k, v, sink, cu_arg, cu_arg, out, lse, dout, dq, dk, dv,
-                                   dsink, workspace, workspace.numel())
+        st = binding.attn_sink_bwd(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse, dout, dq,
+                                   dk, dv, dsink, workspace, workspace.numel())
         if st:
             raise binding.AttnSinkError(st, "attn_sink_bwd")
 
@@ -285,7 +293,7 @@ def main():
         fwd()
         bwd()
     torch.cuda.synchronize()
-    launches_per_step = count_launches(lambda: (fwd(), bwd()))
+    launches_per_step, launch_names = count_launches(lambda: (fwd(), bwd()))
 
     n = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -321,6 +329,7 @@ def main():
     hs = sink.cpu().pin_memory()
     ho, hl, hdq, hdk, hdv, hds = (torch.empty(t.shape, dtype=t.dtype).pin_memory()
                                   for t in (out, lse, dq, dk, dv, dsink))
+    # the residual of out stays on the device (it only feeds the backward)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hs))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv, hds))
     e2e_steps = max(3, min(n, 20))
@@ -379,6 +388,7 @@ def main():
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": None if launches_per_step is None else launches_per_step * n,
         "gpu_launches_per_step": launches_per_step,
+        "gpu_kernels": launch_names,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

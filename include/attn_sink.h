@@ -99,47 +99,62 @@ typedef struct attn_sink_params {
 
 /*
  * Forward.  Writes out [T_q, H_q, 64] bf16 and lse [H_q, T_q] fp32.
+ * out_residual (optional, NULL to skip): [T_q, H_q, 64] bf16, the rounding
+ * residual of out (out + out_residual carries ~16 significand bits of O).
+ * Passing it to attn_sink_bwd makes the backward's D_i = rowsum(dO o O) use
+ * that O instead of the bf16 out, which matters where the softmax is peaked.
  * cu_seqlens_q and cu_seqlens_k are both NULL (dense) or both non-NULL (packed).
+ * Arithmetic: S = q k^T on the bf16 inputs (exact products, fp32 sums); P and
+ * v enter O = P v as fp16; O accumulates in fp32.  v must lie within the fp16
+ * range (|v| <= 65504), otherwise the device error word records
+ * ATTN_SINK_DEVERR_FP16_RANGE (0x400).
  * Passage: listing "带汇聚的注意力（GPT-OSS）" and section "数学公式" of the
  * euno.news page.  Returns an attn_sink_status.
  */
 int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k,
                   const void* v, const float* sink, const int* cu_seqlens_q,
-                  const int* cu_seqlens_k, void* out, float* lse, void* stream);
+                  const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                  void* stream);
 
 /*
  * Bytes of device workspace attn_sink_bwd needs for these params (0 if the
  * params are invalid).  The packed fields are used when num_seqs > 0, the
  * dense ones otherwise.  The workspace holds the row terms D [H_q, T_q], the
  * per-block dsink partials, the fp32 dq accumulator [T_q, H_q, 64] (bf16 dq
- * only) and, when the backward splits a GQA group over several CTAs (decided
- * from the shapes and the current device's SM count), fp32 dK/dV partials.
+ * only), fp16 copies of q, dout, k and v, and, when the backward splits a GQA
+ * group over several CTAs (decided from the shapes and the current device's SM
+ * count), fp32 dK/dV partials.
  * Query it on the device the backward will run on.
  */
 size_t attn_sink_bwd_workspace_size(const attn_sink_params* params);
 
 /*
- * Backward.  Reads q, k, v, sink, out and lse from the forward and dout; writes
- * dq, dk, dv (bf16 or fp32 per grad_dtype) and dsink [H_q] fp32.  dk and dv sum
- * over the query heads of each group.  dq, dk, dv and dsink are overwritten.
- * dsink is reduced in a fixed order (bitwise reproducible); dk and dv are too;
- * dq is accumulated with fp32 atomics and may differ in the last bits between
- * runs.  Passage: section "反向传播" of the euno.news page for dsink.
+ * Backward.  Reads q, k, v, sink, out (and optionally out_residual) and lse from
+ * the forward and dout; writes dq, dk, dv (bf16 or fp32 per grad_dtype) and
+ * dsink [H_q] fp32.  dk and dv sum over the query heads of each group.  dq, dk,
+ * dv and dsink are overwritten.  dsink is reduced in a fixed order (bitwise
+ * reproducible); dk and dv are too; dq is accumulated with fp32 atomics and may
+ * differ in the last bits between runs.
+ * Arithmetic: the five products run on fp16 copies of q, k, v, dout made in the
+ * workspace (exact for |x| <= 65504; beyond it the device error word records
+ * 0x400), with P and dS rounded to fp16 and fp32 accumulation.
+ * Passage: section "反向传播" of the euno.news page for dsink.
  * Returns an attn_sink_status.
  */
 int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k,
                   const void* v, const float* sink, const int* cu_seqlens_q,
-                  const int* cu_seqlens_k, const void* out, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, float* dsink,
-                  void* workspace, size_t workspace_bytes, void* stream);
+                  const int* cu_seqlens_k, const void* out, const void* out_residual,
+                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                  float* dsink, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* attn_sink_status_string(int status);
 
 /*
- * Synchronises `stream`, then reads and clears the device error word that a
- * kernel sets when it gives up on a bounded wait.  *code receives 0 when no
- * kernel timed out.  Returns ATTN_SINK_OK, or ATTN_SINK_ERR_CUDA when the
+ * Synchronises `stream`, then reads and clears the device error word.  *code
+ * receives 0 when nothing was recorded, 0x1xx / 0x2xx when a forward / backward
+ * kernel gave up on a bounded wait, 0x400 when an input was outside the fp16
+ * range of the tensor-core operands.  Returns ATTN_SINK_OK, or ATTN_SINK_ERR_CUDA when the
  * synchronisation itself failed.
  */
 int attn_sink_device_error(void* stream, int* code);

@@ -59,7 +59,7 @@ def assert_close(name, got, ref, max_abs=TOL_MAX_ABS, rel_fro=TOL_REL_FRO):
 
 
 def run_gpu(case: Case, *, grad_dtype: int = 0, with_bwd: bool = True, dense: bool = False,
-            cu_q=None, cu_k=None, q=None, k=None, v=None, dout=None):
+            cu_q=None, cu_k=None, q=None, k=None, v=None, dout=None, residual: bool = True):
     """Forward (+ backward) of a seeded case on cuda:0 through the C ABI."""
     dev = torch.device("cuda:0")
     w = case.workload
@@ -77,11 +77,11 @@ def run_gpu(case: Case, *, grad_dtype: int = 0, with_bwd: bool = True, dense: bo
         q4, do4 = q.view(b, n, *q.shape[1:]), do.view(b, n, *do.shape[1:])
         k4, v4 = k.view(b, nk, *k.shape[1:]), v.view(b, nk, *v.shape[1:])
         kw = dict(causal=w.causal, window=w.window, softmax_scale=w.scale)
-        out, lse = binding.forward(q4, k4, v4, sink, **kw)
+        out, lse, ores = binding.forward(q4, k4, v4, sink, residual=residual, **kw)
         res = dict(out=out.view(q.shape), lse=lse)
         if with_bwd:
             dq, dk, dv, dsink = binding.backward(q4, k4, v4, sink, out, lse, do4,
-                                                 grad_dtype=grad_dtype, **kw)
+                                                 out_residual=ores, grad_dtype=grad_dtype, **kw)
             res.update(dq=dq.view(q.shape), dk=dk.view(k.shape), dv=dv.view(v.shape), dsink=dsink)
     else:
         tq = torch.tensor(cq, dtype=torch.int32, device=dev)
@@ -90,11 +90,11 @@ def run_gpu(case: Case, *, grad_dtype: int = 0, with_bwd: bool = True, dense: bo
         lk = [ck[i + 1] - ck[i] for i in range(len(ck) - 1)]
         kw = dict(causal=w.causal, window=w.window, softmax_scale=w.scale, cu_seqlens_q=tq,
                   cu_seqlens_k=tk, max_seqlen_q=max(lq + [0]), max_seqlen_k=max(lk + [0]))
-        out, lse = binding.forward(q, k, v, sink, **kw)
+        out, lse, ores = binding.forward(q, k, v, sink, residual=residual, **kw)
         res = dict(out=out, lse=lse)
         if with_bwd:
             dq, dk, dv, dsink = binding.backward(q, k, v, sink, out, lse, do,
-                                                 grad_dtype=grad_dtype, **kw)
+                                                 out_residual=ores, grad_dtype=grad_dtype, **kw)
             res.update(dq=dq, dk=dk, dv=dv, dsink=dsink)
     torch.cuda.synchronize()
     st, code = binding.attn_sink_device_error()

@@ -53,17 +53,19 @@ FAKE = 0x7F0000000000       # never dereferenced: validation fails first
 FAKE_ODD = FAKE + 8
 
 
-def _fwd(p, q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, lse=FAKE):
-    return binding.attn_sink_fwd(p, q, k, v, sink, cu_q, cu_k, out, lse, stream=0)
+def _fwd(p, q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, res=None,
+         lse=FAKE):
+    return binding.attn_sink_fwd(p, q, k, v, sink, cu_q, cu_k, out, res, lse, stream=0)
 
 
 def _bwd(p, ws=FAKE, ws_bytes=1 << 40, **kw):
-    args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, lse=FAKE,
-                dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, dsink=FAKE)
+    args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, res=None,
+                lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, dsink=FAKE)
     args.update(kw)
     return binding.attn_sink_bwd(p, args["q"], args["k"], args["v"], args["sink"], args["cu_q"],
-                                 args["cu_k"], args["out"], args["lse"], args["dout"], args["dq"],
-                                 args["dk"], args["dv"], args["dsink"], ws, ws_bytes, stream=0)
+                                 args["cu_k"], args["out"], args["res"], args["lse"],
+                                 args["dout"], args["dq"], args["dk"], args["dv"], args["dsink"],
+                                 ws, ws_bytes, stream=0)
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -94,7 +96,10 @@ def test_invalid_params_rejected_on_host(field, value, status):
 
 def test_null_and_misaligned_pointers():
     p = _dense()
-    assert binding.attn_sink_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 0) == INVALID
+    assert binding.attn_sink_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE,
+                                 0) == INVALID
+    assert _fwd(p, res=FAKE_ODD) == INVALID
+    assert _bwd(p, res=FAKE + 2) == INVALID
     assert _fwd(p, q=None) == INVALID
     assert _fwd(p, sink=None) == INVALID
     assert _fwd(p, out=None) == INVALID
@@ -136,8 +141,8 @@ def test_workspace_size():
     n_bf16 = binding.attn_sink_bwd_workspace_size(p)
     t, h = 2000, 64
     assert n_bf16 % 256 == 0
-    # at least D, the partials and the fp32 dq accumulator
-    assert n_bf16 >= t * h * 4 + t * h * 64 * 4
+    # at least D, the partials, the fp32 dq accumulator and the fp16 copies
+    assert n_bf16 >= t * h * 4 + t * h * 64 * 4 + 2 * t * h * 64 * 2 + 2 * t * 8 * 64 * 2
     p.grad_dtype = 1
     n_fp32 = binding.attn_sink_bwd_workspace_size(p)
     assert n_fp32 < n_bf16       # fp32 dq is accumulated in place
