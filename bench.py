@@ -179,6 +179,9 @@ def count_launches(fn):
         except Exception:
             names = [e.name for e in prof.events()]
         mine = [n for n in names if "attn_sink" in n and "kernel" in n]
+        if not mine:
+            sys.stderr.write("launch count: no library kernel among %d trace events: %s\n"
+                             % (len(names), sorted(set(names))[:40]))
         return len(mine), sorted(set(mine))
     except Exception as exc:  # profiler unavailable: report unknown
         return None, [f"profiler error: {exc}"]
@@ -226,6 +229,9 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=6.0,
                     help="seconds of CPU oracle work per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu", action="store_true",
+                    help="minimal run for a profiler: no e2e leg, no CPU baseline, no clock "
+                         "sampling, no launch count")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -293,12 +299,16 @@ def main():
         fwd()
         bwd()
     torch.cuda.synchronize()
-    launches_per_step, launch_names = count_launches(lambda: (fwd(), bwd()))
+    if args.ncu:
+        launches_per_step, launch_names = None, []
+    else:
+        launches_per_step, launch_names = count_launches(lambda: (fwd(), bwd()))
 
     n = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
+    if not args.ncu:
+        sampler.start()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -332,7 +342,7 @@ def main():
     # the residual of out stays on the device (it only feeds the backward)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hs))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv, hds))
-    e2e_steps = max(3, min(n, 20))
+    e2e_steps = 0 if args.ncu else max(3, min(n, 20))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -348,7 +358,7 @@ def main():
             h.copy_(d_, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / max(e2e_steps, 1)
     st, code = binding.attn_sink_device_error()
     if st != 0 or code != 0:
         raise RuntimeError(f"device error word {code:#x}")
@@ -392,7 +402,7 @@ def main():
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.ncu:
         line["cpu_baseline"] = cpu_oracle_rate(w, case, budget_s=args.cpu_budget)
         line["cpu_baseline"].pop("seconds", None)
     if rank == 0:
