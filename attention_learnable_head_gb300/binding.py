@@ -1,7 +1,8 @@
 """ctypes binding of libattn_sink.so.
 
 ``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_bwd_workspace_size``,
-``attn_sink_status_string`` and ``attn_sink_device_error`` mirror the C entry
+``attn_sink_status_string``, ``attn_sink_device_error`` and
+``attn_sink_launch_count`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -53,7 +54,7 @@ def header_functions() -> list[str]:
     """Names of the functions include/attn_sink.h declares."""
     text = open(os.path.join(INCLUDE, "attn_sink.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(attn_sink_\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^(?:[A-Za-z_]\w*[\s*]+)+(attn_sink_\w+)\s*\(", text, flags=re.M)
 
 
 def lib():
@@ -80,6 +81,8 @@ def lib():
     L.attn_sink_status_string.restype = ctypes.c_char_p
     L.attn_sink_device_error.argtypes = [c_void_p, ctypes.POINTER(c_int)]
     L.attn_sink_device_error.restype = c_int
+    L.attn_sink_launch_count.argtypes = []
+    L.attn_sink_launch_count.restype = ctypes.c_ulonglong
     _LIB = L
     return L
 
@@ -128,6 +131,10 @@ def attn_sink_bwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlen
 
 def attn_sink_status_string(status: int) -> str:
     return lib().attn_sink_status_string(int(status)).decode()
+
+
+def attn_sink_launch_count() -> int:
+    return int(lib().attn_sink_launch_count())
 
 
 def attn_sink_device_error(stream=None) -> tuple[int, int]:

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -20,6 +21,15 @@ namespace {
 using namespace attn_sink;
 
 constexpr int kMaxDevices = 64;
+
+// Kernels this library has launched in this process (successful launches).
+std::atomic<unsigned long long> g_launches{0};
+
+inline bool launched() {
+  if (cudaGetLastError() != cudaSuccess) return false;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return true;
+}
 
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -279,7 +289,7 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   if (fp.n_qblocks == 0) return ATTN_SINK_OK;
   dim3 grid(params->heads_q, g.num_seqs, fp.n_qblocks);
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
-  return cudaGetLastError() == cudaSuccess ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+  return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
 }
 
 size_t attn_sink_bwd_workspace_size(const attn_sink_params* params) {
@@ -349,7 +359,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     pp.heads_q = params->heads_q;
     pp.n_blocks = L.n_blocks;
     attn_sink_bwd_pre_kernel<<<dim3(L.n_blocks, params->heads_q), 256, 0, s>>>(pp);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+    if (!launched()) return ATTN_SINK_ERR_CUDA;
   }
   if (g.total_k > 0) {
     const size_t n8 = (size_t)g.total_k * params->heads_kv * kHeadDim / 8;
@@ -357,7 +367,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     attn_sink_kv_convert_kernel<<<blocks, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), k16, v16, n8,
         err);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+    if (!launched()) return ATTN_SINK_ERR_CUDA;
   }
   // 2. main loop: dK, dV (and their split partials), dQ accumulation
   const int n_ktiles = (g.max_k + kBlockN - 1) / kBlockN;
@@ -403,13 +413,13 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     bp.grad_fp32 = params->grad_dtype;
     dim3 grid(params->heads_kv * L.split, g.num_seqs, n_ktiles);
     attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+    if (!launched()) return ATTN_SINK_ERR_CUDA;
     if (L.split > 1) {
       const size_t n4 = (size_t)g.total_k * params->heads_kv * kHeadDim / 4;
       const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)sms * 8);
       attn_sink_dkdv_reduce_kernel<<<blocks, 256, 0, s>>>(bp.dk_part, bp.dv_part, L.split, n4,
                                                           scale, dk, dv, params->grad_dtype);
-      if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+      if (!launched()) return ATTN_SINK_ERR_CUDA;
     }
   }
   // 3. dq (bf16) from the fp32 accumulator
@@ -418,16 +428,20 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
     attn_sink_dq_convert_kernel<<<blocks, 256, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                        n8);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_SINK_ERR_CUDA;
+    if (!launched()) return ATTN_SINK_ERR_CUDA;
   }
   // 4. dsink
   if (g.total_q > 0) {
     attn_sink_dsink_reduce_kernel<<<params->heads_q, 256, 0, s>>>(partials, L.n_blocks, dsink);
-  } else {
-    if (cudaMemsetAsync(dsink, 0, sizeof(float) * params->heads_q, s) != cudaSuccess)
-      return ATTN_SINK_ERR_CUDA;
+    return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+  if (cudaMemsetAsync(dsink, 0, sizeof(float) * params->heads_q, s) != cudaSuccess)
+    return ATTN_SINK_ERR_CUDA;
+  return ATTN_SINK_OK;
+}
+
+unsigned long long attn_sink_launch_count(void) {
+  return g_launches.load(std::memory_order_relaxed);
 }
 
 int attn_sink_device_error(void* stream, int* code) {

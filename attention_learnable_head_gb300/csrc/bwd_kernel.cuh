@@ -7,18 +7,20 @@
 //               because lse includes the sink), fp16 copies of q and dout for the
 //               tensor cores, and zeroes the fp32 dq accumulator.
 //   kv_convert  fp16 copies of k and v.
-//   bwd_main    key/value-stationary: one CTA per (kv head, sequence, 128 keys).
-//               Loops over the query heads of the GQA group and the query tiles
-//               that can see these keys; per step five tcgen05 MMAs, all on
-//               fp16 operands (the inputs convert exactly; P and dS keep 11
-//               significand bits instead of bf16's 8):
-//                 S^T  = K Q^T        dP^T = V dO^T            (TMEM, fp32)
+//   bwd_main    key/value-stationary: one CTA per (kv head, GQA slice, sequence,
+//               128 keys).  Loops over the query heads of its slice and the
+//               query tiles that can see these keys; per step (128 queries, in
+//               two halves of 64) five tcgen05 MMAs, all on fp16 operands (the
+//               inputs convert exactly; P and dS keep 11 significand bits):
+//                 S^T  = K Q^T        dP^T = V dO^T            (TMEM, fp32, per half)
 //                 P^T  = exp(S^T * scale - lse)  dS^T = P^T o (dP^T - D)
-//                 dV  += P^T dO       (A = P^T from TMEM)
-//                 dK  += dS^T Q       (A = dS^T from SMEM, K-major)
-//                 dQ   = dS K         (A = dS^T from SMEM read MN-major)
-//               dK and dV stay in TMEM for the whole loop; dQ is added into the
-//               fp32 accumulator with vector atomics by a dedicated warpgroup.
+//                 dV  += P^T dO       dK += dS^T Q             (per half, K = 64)
+//                 dQ   = dS K         (A = dS^T read MN-major, once per step)
+//               Two compute warpgroups own one query half each, so the tensor
+//               cores run one half's products while the other half's exponentials
+//               are computed.  dK and dV stay in TMEM for the whole loop; dQ is
+//               added into the fp32 accumulator with vector atomics by a
+//               dedicated warpgroup.
 //   dsink_reduce  fixed-order tree over the partials (bitwise reproducible).
 //   dq_convert  fp32 accumulator -> bf16 dq.
 #pragma once
@@ -29,14 +31,18 @@
 namespace attn_sink {
 
 constexpr int kBwdStages = 2;
-constexpr int kBwdThreads = 320;   // warps 0-3 compute, 4 TMA, 5 MMA, 6-9 dQ
+// warps 0-3 compute queries 0-63 of a step, 4-7 queries 64-127, 8 TMA, 9 MMA, 10-13 dQ
+constexpr int kBwdThreads = 448;
+constexpr int kBwdProducerWarp = 8;
+constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdDqWarp0 = 10;
 constexpr int kPreRows = 128;      // rows per bwd_pre CTA
-constexpr int kBwdSmemBytes =
-    1024 + 2 * (int)kTileBytes + kBwdStages * 2 * (int)kTileBytes + (int)kPTileBytes;
+// K, V, kBwdStages x (Q, dO), P^T, 2 x dS^T
+constexpr int kBwdSmemBytes = 1024 + 2 * (int)kTileBytes + kBwdStages * 2 * (int)kTileBytes +
+                              3 * (int)kPTileBytes;
 
-// TMEM columns of bwd_main
-constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
-                   kColPT = 448;
+// TMEM columns of bwd_main (S^T / dP^T: query half hh at +64 hh)
+constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
 
 struct BwdParams {
   CUtensorMap tm_q;    // [T_q][H_q][64] fp16 copy of q
@@ -258,8 +264,9 @@ __device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, 
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full, s_full, p_full, mma2_done, dq_free, drained;
+  __shared__ __align__(8) uint64_t kv_full, mma2_done, dq_free, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2];
   __shared__ float s_lse2[kBwdStages][kBlockM];   // lse * log2(e); +inf hides the row
   __shared__ float s_D[kBwdStages][kBlockM];
   __shared__ uint32_t tmem_base_sh;
@@ -273,7 +280,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   const int ktile = blockIdx.z;            // low key tiles carry the most work: first
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
   const int j0 = ktile * kBlockN;
-  if (j0 >= sp.nk) return;                  // uniform per CTA
+  if (j0 >= sp.nk) return;                 // uniform per CTA
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int off = sp.nk - sp.nq;
@@ -287,15 +294,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   }
   const int qt_first = q_lo / kBlockM;
   const int nqt = (q_hi > q_lo) ? ((q_hi + kBlockM - 1) / kBlockM - qt_first) : 0;
-  const int num = nqt * hpc;                // steps: (query head) x (query tile)
-
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sK = smem;
-  uint8_t* sV = sK + kTileBytes;
-  uint8_t* sQ = sV + kTileBytes;                      // kBwdStages tiles
-  uint8_t* sdO = sQ + kBwdStages * kTileBytes;        // kBwdStages tiles
-  uint8_t* sdS = sdO + kBwdStages * kTileBytes;       // [128 keys][128 queries] fp16
+  const int num = nqt * hpc;               // steps: (query head) x (query tile)
 
   if (num == 0) {
     // No query sees these keys: dK = dV = 0.
@@ -310,11 +309,18 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     return;
   }
 
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + kTileBytes;
+  uint8_t* sQ = sV + kTileBytes;                      // kBwdStages tiles
+  uint8_t* sdO = sQ + kBwdStages * kTileBytes;        // kBwdStages tiles
+  uint8_t* sPT = sdO + kBwdStages * kTileBytes;       // [128 keys][128 queries] fp16
+  uint8_t* sdS = sPT + kPTileBytes;                   // 2 x [128 keys][128 queries] fp16
+
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&kv_full, 1);
-    mbar_init(&s_full, 1);
-    mbar_init(&p_full, kBlockN);
     mbar_init(&mma2_done, 1);
     mbar_init(&dq_free, kBlockM);
     mbar_init(&drained, 1);
@@ -322,9 +328,13 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 producer lanes (lse / D)
       mbar_init(&q_empty[s], 1);
     }
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(&s_full[hh], 1);
+      mbar_init(&p_full[hh], kBlockN);
+    }
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == kBwdMmaWarp) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
@@ -333,7 +343,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 4) {
+  if (warp == kBwdProducerWarp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -384,51 +394,73 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       for (int m = max(0, issued - kBwdStages); m < issued; ++m)
         mbar_wait(&q_full[m % kBwdStages], (m / kBwdStages) & 1, nullptr);
     }
-  } else if (warp == 5) {
+  } else if (warp == kBwdMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM, false, false);  // S^T, dP^T
+      const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM / 2, false, false);
       const uint32_t id_dvdk = make_idesc(kFmtF16, kBlockN, kHeadDim, false, true);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aS = smem_u32(sdS);
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sPT);
+      // S^T / dP^T for the query half hh of step m (64 queries, N = 64).
+      auto issue_s = [&](int m, int hh) {
+        const int st = m % kBwdStages;
+        const uint32_t aQ = smem_u32(sQ + st * kTileBytes) + hh * (kTileBytes / 2);
+        const uint32_t aO = smem_u32(sdO + st * kTileBytes) + hh * (kTileBytes / 2);
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_ss(tmem + kColST + 64 * hh, make_sdesc_sw128(aK + 32 * k, 16, 1024),
+                 make_sdesc_sw128(aQ + 32 * k, 16, 1024), id_s, k > 0);
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_ss(tmem + kColDPT + 64 * hh, make_sdesc_sw128(aV + 32 * k, 16, 1024),
+                 make_sdesc_sw128(aO + 32 * k, 16, 1024), id_s, k > 0);
+        mma_commit(&s_full[hh]);
+      };
+      bool ok = mbar_wait(&kv_full, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
       for (int m = 0; ok && m < num; ++m) {
         const int st = m % kBwdStages;
-        if (!mbar_wait(&q_full[st], (m / kBwdStages) & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
         const uint32_t aQ = smem_u32(sQ + st * kTileBytes);
         const uint32_t aO = smem_u32(sdO + st * kTileBytes);
-        #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kColST, make_sdesc_sw128(aK + 32 * k, 16, 1024),
-                      make_sdesc_sw128(aQ + 32 * k, 16, 1024), id_s, k > 0);
-        #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kColDPT, make_sdesc_sw128(aV + 32 * k, 16, 1024),
-                      make_sdesc_sw128(aO + 32 * k, 16, 1024), id_s, k > 0);
-        mma_commit(&s_full);
-        if (!mbar_wait(&p_full, m & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // dV += P^T dO  (A: P^T in TMEM, K = query index; B: dO tile read MN-major)
-        #pragma unroll
-        for (int k = 0; k < kBlockM / 16; ++k)
-          mma_ts(tmem + kColDV, tmem + kColPT + 8 * k,
-                      make_sdesc_sw128(aO + k * 2048, 16384, 1024), id_dvdk, (m > 0 || k > 0));
-        // dK += dS^T Q  (A: dS^T in SMEM, K-major over queries; B: Q read MN-major)
-        #pragma unroll
-        for (int k = 0; k < kBlockM / 16; ++k)
-          mma_ss(tmem + kColDK,
-                      make_sdesc_sw128(aS + (k >> 2) * kTileBytes + (k & 3) * 32, 16, 1024),
-                      make_sdesc_sw128(aQ + k * 2048, 16384, 1024), id_dvdk, (m > 0 || k > 0));
-        if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // dQ = dS K  (A: dS^T SMEM read MN-major, M = queries; B: K read MN-major)
-        #pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k)
-          mma_ss(tmem + kColDQ, make_sdesc_sw128(aS + k * 2048, 16384, 1024),
-                      make_sdesc_sw128(aK + k * 2048, 16384, 1024), id_dq, k > 0);
-        mma_commit(&mma2_done);
-        mma_commit(&q_empty[st]);
+        const uint32_t aS = smem_u32(sdS + (m & 1) * kPTileBytes);
+        const bool more = m + 1 < num;
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&p_full[hh], m & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // dV += P^T dO and dK += dS^T Q over this half's 64 queries (K = 64)
+          #pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + kColDV, make_sdesc_sw128(aP + hh * kTileBytes + 32 * k, 16, 1024),
+                   make_sdesc_sw128(aO + hh * (kTileBytes / 2) + k * 2048, 16384, 1024),
+                   id_dvdk, (m > 0 || hh > 0 || k > 0));
+          #pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + kColDK, make_sdesc_sw128(aS + hh * kTileBytes + 32 * k, 16, 1024),
+                   make_sdesc_sw128(aQ + hh * (kTileBytes / 2) + k * 2048, 16384, 1024),
+                   id_dvdk, (m > 0 || hh > 0 || k > 0));
+          if (hh == 1) {
+            if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
+            #pragma unroll
+            for (int k = 0; k < kBlockN / 16; ++k)
+              mma_ss(tmem + kColDQ, make_sdesc_sw128(aS + k * 2048, 16384, 1024),
+                     make_sdesc_sw128(aK + k * 2048, 16384, 1024), id_dq, k > 0);
+            mma_commit(&mma2_done);
+            mma_commit(&q_empty[st]);
+          }
+          if (more) {
+            // next step's half hh: its S^T / dP^T columns were read by this half
+            if (!mbar_wait(&q_full[(m + 1) % kBwdStages], ((m + 1) / kBwdStages) & 1,
+                           &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(m + 1, hh);
+          }
+        }
       }
       if (!ok) {
         abort_flag = 1;
@@ -437,35 +469,37 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mma_commit(&drained);
       mbar_wait(&drained, 0, nullptr);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ---------------------------------------------------------------- compute warps
-    const int r = tid;                               // key row in tile = TMEM lane
+    // warpgroup hh handles queries [64 hh, 64 hh + 64) of every step
+    const int hh = warp >> 2;
+    const int r = tid & 127;                        // key row in tile = TMEM lane
     const int j = j0 + r;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
-    const uint32_t sbase = smem_u32(sdS);
+    const uint32_t pbase = smem_u32(sPT) + hh * kTileBytes;
+    const int imin = p.causal ? j - off : 0;
+    const int imax = (p.causal && p.window > 0) ? j - off + p.window - 1 : sp.nq - 1;
+    const bool key_ok = j < sp.nk;
     bool ok = true;
     for (int m = 0; m < num; ++m) {
       const int st = m % kBwdStages;
-      const int i0 = (qt_first + m % nqt) * kBlockM;
+      const int i0 = (qt_first + m % nqt) * kBlockM + 64 * hh;   // first query of this half
       // q_full: the producer's lse / D rows of this step are in SMEM.
+      // s_full: this half's S^T / dP^T, and every earlier MMA (the readers of
+      // the P^T half and of this step's dS^T buffer) has completed.
       if (!mbar_wait_warp(&q_full[st], (m / kBwdStages) & 1, &abort_flag) ||
-          !mbar_wait_warp(&s_full, m & 1, &abort_flag)) { ok = false; break; }
-      // The previous step's dV/dK/dQ MMAs have read P^T and dS^T.
-      if (m > 0 && !mbar_wait_warp(&mma2_done, (m - 1) & 1, &abort_flag)) { ok = false; break; }
+          !mbar_wait_warp(&s_full[hh], m & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const bool need_mask = (j0 + kBlockN > sp.nk) || (i0 + kBlockM > sp.nq) ||
+      const bool need_mask = (j0 + kBlockN > sp.nk) || (i0 + 64 > sp.nq) ||
                              (p.causal && (j0 + kBlockN - 1 > i0 + off ||
-                                           (p.window > 0 && j0 <= i0 + kBlockM - 1 + off - p.window)));
-      // query rows this key is visible to: [imin, imax]
-      const int imin = p.causal ? j - off : 0;
-      const int imax = (p.causal && p.window > 0) ? j - off + p.window - 1 : sp.nq - 1;
-      const bool key_ok = j < sp.nk;
-      #pragma unroll 1
-      for (int c = 0; c < kBlockM; c += 32) {
+                                           (p.window > 0 && j0 <= i0 + 63 + off - p.window)));
+      const uint32_t sbase = smem_u32(sdS + (m & 1) * kPTileBytes) + hh * kTileBytes;
+      #pragma unroll
+      for (int c = 0; c < 64; c += 32) {
         uint32_t sr[32], dr[32];
-        tmem_ld_x32(tmem + lane_base + kColST + c, sr);
-        tmem_ld_x32(tmem + lane_base + kColDPT + c, dr);
+        tmem_ld_x32(tmem + lane_base + kColST + 64 * hh + c, sr);
+        tmem_ld_x32(tmem + lane_base + kColDPT + 64 * hh + c, dr);
         tmem_ld_wait();
         uint32_t pk[16], dk[16];
         #pragma unroll
@@ -473,10 +507,10 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           float pv[2], dv[2];
           #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int ci = c + e + u;
+            const int ci = 64 * hh + c + e + u;           // query within the step tile
             float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -s_lse2[st][ci]));
             if (need_mask) {
-              const int i = i0 + ci;
+              const int i = i0 + c + e + u;
               if (!key_ok || i < imin || i > imax || i >= sp.nq) pe = 0.0f;
             }
             pv[u] = pe;
@@ -485,40 +519,40 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
           dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
         }
-        tmem_st_x16(tmem + lane_base + kColPT + (c >> 1), pk);
-        // dS^T row r, queries c..c+31: 4 chunks of 16 bytes in sub-tile c/64
-        const uint32_t tb = sbase + (c >> 6) * kTileBytes;
+        // row r, queries c..c+31 of this half: 4 chunks of 16 bytes
         #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          st_shared_v4(tb + sw128_offset(r, ((c & 63) >> 3) + u), dk[4 * u], dk[4 * u + 1],
-                       dk[4 * u + 2], dk[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t o = sw128_offset(r, (c >> 3) + u);
+          st_shared_v4(pbase + o, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          st_shared_v4(sbase + o, dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
       }
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive(&p_full[hh]);
     }
-    if (ok && !mbar_wait_warp(&mma2_done, (num - 1) & 1, &abort_flag)) ok = false;
+    // `drained` completes once, after the MMA warp's last commit: every MMA into
+    // dK / dV has landed.  (A parity wait on the per-step barriers could be two
+    // phases behind here and pass early.)
+    if (ok && !mbar_wait_warp(&drained, 0, &abort_flag)) ok = false;
     if (!ok) {
       abort_flag = 1;
       atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 3);
     } else {
       tc_fence_after();
-      // Epilogue: dK (times the softmax scale) and dV for this key row.
-      const bool valid = j < sp.nk;
-      const size_t row = (size_t)(sp.k0 + j);
-      #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        float v[kHeadDim];
-        const uint32_t col = which == 0 ? kColDK : kColDV;
-        tmem_ld_x32(tmem + lane_base + col, reinterpret_cast<uint32_t*>(v));
-        tmem_ld_x32(tmem + lane_base + col + 32, reinterpret_cast<uint32_t*>(v + 32));
-        tmem_ld_wait();
-        if (valid) store_kv_grad_row(p, part, row, g, which, v, which == 0 ? p.scale : 1.0f);
-      }
+      // Epilogue: warpgroup 0 stores dV, warpgroup 1 dK (times the softmax scale).
+      const int which = hh == 0 ? 1 : 0;
+      float v[kHeadDim];
+      const uint32_t col = which == 0 ? kColDK : kColDV;
+      tmem_ld_x32(tmem + lane_base + col, reinterpret_cast<uint32_t*>(v));
+      tmem_ld_x32(tmem + lane_base + col + 32, reinterpret_cast<uint32_t*>(v + 32));
+      tmem_ld_wait();
+      if (key_ok)
+        store_kv_grad_row(p, part, (size_t)(sp.k0 + j), g, which, v,
+                          which == 0 ? p.scale : 1.0f);
     }
-  } else {
-    // ---------------------------------------------------------------- dQ warps (6-9)
+  } else if (warp >= kBwdDqWarp0) {
+    // ---------------------------------------------------------------- dQ warps
     const int r = 32 * (warp & 3) + lane;            // query row in tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     bool ok = true;
@@ -553,7 +587,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kBwdMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -260,8 +260,15 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         const int a = lo + n;
         return kr[x].num > 0 && a >= kr[x].lo && a < kr[x].lo + kr[x].num;
       };
-      for (int x = 0; ok && x < kFwdTiles; ++x)
-        if (kr[x].num > 0) ok = issue_s(x, kr[x].lo - lo);
+      // Stagger the tiles: S_B(first) is issued once tile A's first P is ready,
+      // so B's softmax overlaps A's MMAs instead of competing with A's for MUFU.
+      bool b_started = kr[1].num == 0;
+      if (kr[0].num > 0) {
+        ok = issue_s(0, kr[0].lo - lo);
+      } else {
+        ok = issue_s(1, kr[1].lo - lo);
+        b_started = true;
+      }
       for (int n = 0; ok && n < num; ++n) {
         const int st = n % kFwdStages;
         #pragma unroll
@@ -282,7 +289,11 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
             mma_ts(tO, tP + 8 * k, make_sdesc_sw128(aV + k * 2048, 16384, 1024), idesc_o,
                         (local > 0 || k > 0));
           mma_commit(&pv_done[x]);
-          if (in_range(x, n + 1)) ok = issue_s(x, n + 1);
+          if (!b_started) {
+            ok = issue_s(1, kr[1].lo - lo);
+            b_started = true;
+          }
+          if (ok && in_range(x, n + 1)) ok = issue_s(x, n + 1);
         }
         if (ok) mma_commit(&kv_empty[st]);
       }
@@ -347,18 +358,19 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       const bool need_mask = (j0 + kBlockN > sp.nk) ||
                              (p.causal && (j0 + kBlockN - 1 > tile_r0 + off ||
                                            (p.window > 0 && j0 <= tile_r1 + off - p.window)));
-      // pass 1: row max (S read from TMEM 64 columns at a time)
+      // Row max over both 64-column halves of S; the second half stays in
+      // registers for the exponentials, the first is read again afterwards.
+      uint32_t a[64];
       float mx = -INFINITY;
       #pragma unroll
-      for (int c = 0; c < kBlockN; c += 64) {
-        uint32_t a[64];
-        tmem_ld_x32(tS + c, a);
-        tmem_ld_x32(tS + c + 32, a + 32);
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld_x32(tS + 64 * half, a);
+        tmem_ld_x32(tS + 64 * half + 32, a + 32);
         tmem_ld_wait();
         if (need_mask) {
           #pragma unroll
           for (int e = 0; e < 64; ++e) {
-            const int j = j0 + c + e;
+            const int j = j0 + 64 * half + e;
             if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
           }
         }
@@ -388,30 +400,36 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           }
         }
       }
-      // pass 2: P = exp2(S * scale * log2 e - m), bf16, into TMEM P_x
+      // P = exp2(S * scale * log2 e - m), fp16, into TMEM P_x: second half from
+      // registers, then the first half read again.
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       float rowsum = 0.0f;
       #pragma unroll
-      for (int c = 0; c < kBlockN; c += 32) {
-        uint32_t a[32];
-        tmem_ld_x32(tS + c, a);
-        tmem_ld_wait();
-        if (need_mask) {
-          #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = j0 + c + e;
-            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+      for (int half = 1; half >= 0; --half) {
+        if (half == 0) {
+          tmem_ld_x32(tS, a);
+          tmem_ld_x32(tS + 32, a + 32);
+          tmem_ld_wait();
+          if (need_mask) {
+            #pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const int j = j0 + e;
+              if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+            }
           }
         }
-        uint32_t pk[16];
         #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(a[e]), sl2, -m_use));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(a[e + 1]), sl2, -m_use));
-          rowsum += e0 + e1;
-          pk[e >> 1] = pack_f16x2(e0, e1);
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t pk[16];
+          #pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float e0 = ex2_approx(fmaf(__uint_as_float(a[c + e]), sl2, -m_use));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use));
+            rowsum += e0 + e1;
+            pk[e >> 1] = pack_f16x2(e0, e1);
+          }
+          tmem_st_x16(tP + ((64 * half + c) >> 1), pk);
         }
-        tmem_st_x16(tP + (c >> 1), pk);
       }
       l = l * alpha + rowsum;
       tmem_st_wait();

@@ -164,27 +164,11 @@ def dist_env():
     return ws, rank, local
 
 
-def count_launches(fn):
-    """Kernels of libattn_sink launched by one call of fn (CUDA activity trace):
-    (count, kernel names)."""
-    try:
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-            fn()
-            torch.cuda.synchronize()
-        names = []
-        try:
-            for e in prof.profiler.kineto_results.events():
-                names.append(e.name())
-        except Exception:
-            names = [e.name for e in prof.events()]
-        mine = [n for n in names if "attn_sink" in n and "kernel" in n]
-        if not mine:
-            sys.stderr.write("launch count: no library kernel among %d trace events: %s\n"
-                             % (len(names), sorted(set(names))[:40]))
-        return len(mine), sorted(set(mine))
-    except Exception as exc:  # profiler unavailable: report unknown
-        return None, [f"profiler error: {exc}"]
+def count_launches(binding, fn) -> int:
+    """Kernels libattn_sink launches during fn (the library's own launch counter)."""
+    n0 = binding.attn_sink_launch_count()
+    fn()
+    return binding.attn_sink_launch_count() - n0
 
 
 def run_reference(args, w, case):
@@ -299,10 +283,7 @@ def main():
         fwd()
         bwd()
     torch.cuda.synchronize()
-    if args.ncu:
-        launches_per_step, launch_names = None, []
-    else:
-        launches_per_step, launch_names = count_launches(lambda: (fwd(), bwd()))
+    launches_per_step = count_launches(binding, lambda: (fwd(), bwd()))
 
     n = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -312,6 +293,7 @@ def main():
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = binding.attn_sink_launch_count()
     wall0 = time.perf_counter()
     for i in range(n):
         flush.fill_(i & 0xFF)
@@ -322,6 +304,7 @@ def main():
         ev[i][2].record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    launches_timed = binding.attn_sink_launch_count() - launches0
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -396,9 +379,8 @@ def main():
                          "hbm_gbs": alg["fwd_bytes"] / (fwd_t * 1e-3) / 1e9},
         "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": None if launches_per_step is None else launches_per_step * n,
+        "gpu_launches": launches_timed,
         "gpu_launches_per_step": launches_per_step,
-        "gpu_kernels": launch_names,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

@@ -41,8 +41,9 @@
  * caller (params is a host pointer read during the call only).  The library
  * allocates nothing.  Calls are asynchronous on `stream` (a cudaStream_t;
  * NULL = legacy default stream) and never synchronise the host.  All calls are
- * thread-safe; the only global state is the cached driver entry point for
- * tensor-map encoding, initialised once.  Outputs are overwritten, never
+ * thread-safe; the global state is the cached driver entry point for
+ * tensor-map encoding (initialised once), per-device launch attributes and a
+ * launch counter.  Outputs are overwritten, never
  * accumulated into.  Device pointers of q, k, v, out, dout, dq, dk, dv must be
  * 16-byte aligned; the workspace must be 256-byte aligned.
  *
@@ -158,6 +159,13 @@ const char* attn_sink_status_string(int status);
  * synchronisation itself failed.
  */
 int attn_sink_device_error(void* stream, int* code);
+
+/*
+ * Number of kernels this library has launched in this process so far (a
+ * host-side counter, incremented after every successful launch).  The
+ * difference across a region counts the library's GPU launches in it.
+ */
+unsigned long long attn_sink_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,8 @@ def _lib():
 def test_exports_every_declared_symbol():
     names = binding.header_functions()
     assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
-                          "attn_sink_status_string", "attn_sink_device_error"}
+                          "attn_sink_status_string", "attn_sink_device_error",
+                          "attn_sink_launch_count"}
     lib = binding.lib()
     for n in names:
         assert hasattr(lib, n), n
@@ -131,9 +132,12 @@ def test_packed_mode_checks():
 
 
 def test_empty_problem_is_a_no_op():
-    # Nothing to compute: returns OK without touching the device.
+    # Nothing to compute: returns OK without touching the device or launching.
+    n0 = binding.attn_sink_launch_count()
     assert _fwd(_dense(batch=0)) == OK
     assert _fwd(_dense(seqlen_q=0)) == OK
+    assert _fwd(_dense(head_dim=32)) == UNSUPPORTED
+    assert binding.attn_sink_launch_count() == n0
 
 
 def test_workspace_size():
