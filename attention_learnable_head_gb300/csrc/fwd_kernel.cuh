@@ -49,6 +49,10 @@ constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (kFwdTiles + 2 * kFwdStag
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
+// Exponentials of P: one pair in kFwdPolyEvery is evaluated with the FMA-pipe
+// polynomial (exp2_poly) instead of MUFU ex2, to balance the two pipes
+// (0 = all on MUFU).
+constexpr int kFwdPolyEvery = 4;
 
 struct FwdParams {
   CUtensorMap tm_q;   // [T_q][H_q][64] bf16, box 64 x 1 x 128, 128B swizzle
@@ -423,8 +427,12 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           uint32_t pk[16];
           #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(a[c + e]), sl2, -m_use));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use));
+            const float x0 = fmaf(__uint_as_float(a[c + e]), sl2, -m_use);
+            const float x1 = fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use);
+            // One pair in kFwdPolyEvery goes to the FMA pipe, the rest to MUFU.
+            const bool poly = kFwdPolyEvery > 0 && (e >> 1) % kFwdPolyEvery == kFwdPolyEvery - 1;
+            const float e0 = poly ? exp2_poly(x0) : ex2_approx(x0);
+            const float e1 = poly ? exp2_poly(x1) : ex2_approx(x1);
             rowsum += e0 + e1;
             pk[e >> 1] = pack_f16x2(e0, e1);
           }
