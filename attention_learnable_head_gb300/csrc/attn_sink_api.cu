@@ -137,12 +137,15 @@ int validate(const attn_sink_params* p, const int* cu_q, const int* cu_k, Geomet
   return ATTN_SINK_OK;
 }
 
+// 3-D map over a [tokens][heads][64] tensor with a (128 bytes) x 1 x 128-row box
+// and 128-byte swizzle: 64 columns of a 16-bit type, or 32 of fp32.
 int encode_rows(CUtensorMap* m, const void* ptr, int tokens, int heads,
                 CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   if (!load_encode()) return ATTN_SINK_ERR_CUDA;
+  const cuuint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
-  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kBlockM};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * esize, (cuuint64_t)heads * kHeadDim * esize};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)kBlockM};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, dtype, 3, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -386,6 +389,10 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     if ((st = encode_rows(&bp.tm_k, k16, g.total_k, params->heads_kv, f16)) != ATTN_SINK_OK)
       return st;
     if ((st = encode_rows(&bp.tm_v, v16, g.total_k, params->heads_kv, f16)) != ATTN_SINK_OK)
+      return st;
+    const void* dqp = g.total_q > 0 ? (const void*)dq_acc : (const void*)k16;
+    if ((st = encode_rows(&bp.tm_dq, dqp, tq, hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) !=
+        ATTN_SINK_OK)
       return st;
     bp.cu_q = cu_seqlens_q;
     bp.cu_k = cu_seqlens_k;

@@ -37,18 +37,25 @@ constexpr int kBwdProducerWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdDqWarp0 = 10;
 constexpr int kPreRows = 128;      // rows per bwd_pre CTA
-// K, V, kBwdStages x (Q, dO), P^T, 2 x dS^T
+constexpr uint32_t kDqStageBytes = kBlockM * kHeadDim * 4;   // 32 KB fp32 dQ tile
+// K, V, kBwdStages x (Q, dO), 2 x dS^T, the dQ staging tile
 constexpr int kBwdSmemBytes = 1024 + 2 * (int)kTileBytes + kBwdStages * 2 * (int)kTileBytes +
-                              3 * (int)kPTileBytes;
+                              2 * (int)kPTileBytes + (int)kDqStageBytes;
 
 // TMEM columns of bwd_main (S^T / dP^T: query half hh at +64 hh)
-constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+// Dynamic + static shared memory must stay within the 227 KB a CTA may use.
+static_assert(kBwdSmemBytes + 4096 <= 232448, "backward shared memory over the per-CTA limit");
+
+// P^T (fp16, two per column): query half hh at 448 + 32 hh.
+constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
+                   kColPT = 448;
 
 struct BwdParams {
   CUtensorMap tm_q;    // [T_q][H_q][64] fp16 copy of q
   CUtensorMap tm_do;   // [T_q][H_q][64] fp16 copy of dout
   CUtensorMap tm_k;    // [T_k][H_kv][64] fp16 copy of k
   CUtensorMap tm_v;    // fp16 copy of v
+  CUtensorMap tm_dq;   // [T_q][H_q][64] fp32 dq accumulator, box 32 x 1 x 128, 128B swizzle
   const int* cu_q;
   const int* cu_k;
   const float* lse;    // [H_q][T_q]
@@ -267,7 +274,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   __shared__ __align__(8) uint64_t kv_full, mma2_done, dq_free, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];
-  __shared__ float s_lse2[kBwdStages][kBlockM];   // lse * log2(e); +inf hides the row
+  __shared__ float s_lse[kBwdStages][kBlockM];    // lse rows of the step (natural log)
   __shared__ float s_D[kBwdStages][kBlockM];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -315,8 +322,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint8_t* sV = sK + kTileBytes;
   uint8_t* sQ = sV + kTileBytes;                      // kBwdStages tiles
   uint8_t* sdO = sQ + kBwdStages * kTileBytes;        // kBwdStages tiles
-  uint8_t* sPT = sdO + kBwdStages * kTileBytes;       // [128 keys][128 queries] fp16
-  uint8_t* sdS = sPT + kPTileBytes;                   // 2 x [128 keys][128 queries] fp16
+  uint8_t* sdS = sdO + kBwdStages * kTileBytes;       // 2 x [128 keys][128 queries] fp16
+  uint8_t* sdQ = sdS + 2 * kPTileBytes;                // 2 x [128 queries][32] fp32, swizzled
 
   if (tid == 0) {
     abort_flag = 0;
@@ -325,7 +332,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     mbar_init(&dq_free, kBlockM);
     mbar_init(&drained, 1);
     for (int s = 0; s < kBwdStages; ++s) {
-      mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 producer lanes (lse / D)
+      mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 lanes' cp.async (lse / D)
       mbar_init(&q_empty[s], 1);
     }
     for (int hh = 0; hh < 2; ++hh) {
@@ -372,21 +379,16 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tma_load_3d(&p.tm_q, &q_full[st], sQ + st * kTileBytes, 0, h, sp.q0 + i0);
         tma_load_3d(&p.tm_do, &q_full[st], sdO + st * kTileBytes, 0, h, sp.q0 + i0);
       }
+      // lse / D of the step's 128 query rows, copied asynchronously; rows past
+      // the sequence read a valid row and are masked by the compute warps.
       #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = lane + 32 * u;
-        const int i = i0 + t;
-        float l2 = INFINITY, dd = 0.0f;
-        if (i < sp.nq) {
-          const size_t idx = (size_t)h * p.total_q + sp.q0 + i;
-          const float lse = p.lse[idx];
-          l2 = (lse > -INFINITY) ? lse * kLog2e : INFINITY;
-          dd = p.D[idx];
-        }
-        s_lse2[st][t] = l2;
-        s_D[st][t] = dd;
+        const size_t idx = (size_t)h * p.total_q + sp.q0 + min(i0 + t, sp.nq - 1);
+        cp_async_4(smem_u32(&s_lse[st][t]), p.lse + idx);
+        cp_async_4(smem_u32(&s_D[st][t]), p.D + idx);
       }
-      mbar_arrive(&q_full[st]);
+      cp_async_mbar_arrive_noinc(&q_full[st]);
       issued = m + 1;
     }
     if (abort_flag && lane == 0) {
@@ -400,7 +402,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM / 2, false, false);
       const uint32_t id_dvdk = make_idesc(kFmtF16, kBlockN, kHeadDim, false, true);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sPT);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       // S^T / dP^T for the query half hh of step m (64 queries, N = 64).
       auto issue_s = [&](int m, int hh) {
         const int st = m % kBwdStages;
@@ -434,7 +436,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           // dV += P^T dO and dK += dS^T Q over this half's 64 queries (K = 64)
           #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + kColDV, make_sdesc_sw128(aP + hh * kTileBytes + 32 * k, 16, 1024),
+            mma_ts(tmem + kColDV, tmem + kColPT + 32 * hh + 8 * k,
                    make_sdesc_sw128(aO + hh * (kTileBytes / 2) + k * 2048, 16384, 1024),
                    id_dvdk, (m > 0 || hh > 0 || k > 0));
           #pragma unroll
@@ -477,7 +479,6 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const int j = j0 + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
-    const uint32_t pbase = smem_u32(sPT) + hh * kTileBytes;
     const int imin = p.causal ? j - off : 0;
     const int imax = (p.causal && p.window > 0) ? j - off + p.window - 1 : sp.nq - 1;
     const bool key_ok = j < sp.nk;
@@ -508,7 +509,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int ci = 64 * hh + c + e + u;           // query within the step tile
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -s_lse2[st][ci]));
+            float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -s_lse[st][ci] * kLog2e));
             if (need_mask) {
               const int i = i0 + c + e + u;
               if (!key_ok || i < imin || i > imax || i >= sp.nq) pe = 0.0f;
@@ -519,14 +520,14 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
           dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
         }
-        // row r, queries c..c+31 of this half: 4 chunks of 16 bytes
+        tmem_st_x16(tmem + lane_base + kColPT + 32 * hh + (c >> 1), pk);
+        // dS^T row r, queries c..c+31 of this half: 4 chunks of 16 bytes
         #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t o = sw128_offset(r, (c >> 3) + u);
-          st_shared_v4(pbase + o, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          st_shared_v4(sbase + o, dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(sbase + sw128_offset(r, (c >> 3) + u), dk[4 * u], dk[4 * u + 1],
+                       dk[4 * u + 2], dk[4 * u + 3]);
       }
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[hh]);
@@ -553,13 +554,24 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     }
   } else if (warp >= kBwdDqWarp0) {
     // ---------------------------------------------------------------- dQ warps
+    // Each step's dQ tile (128 queries x 64, fp32, times the softmax scale) is
+    // staged in SMEM (two 128-byte-swizzled halves of 32 columns) and added to the
+    // fp32 accumulator with two TMA reduce-adds.  Rows past the sequence end are
+    // exact zeros (their dS is masked), so adding them into the next sequence's
+    // rows changes nothing.
     const int r = 32 * (warp & 3) + lane;            // query row in tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const bool leader = (warp == kBwdDqWarp0 && lane == 0);
+    const uint32_t stage = smem_u32(sdQ);
     bool ok = true;
     for (int m = 0; m < num; ++m) {
       const int h = h_first + m / nqt;
       const int i0 = (qt_first + m % nqt) * kBlockM;
-      if (!mbar_wait_warp(&mma2_done, m & 1, &abort_flag)) { ok = false; break; }
+      const bool waited = mbar_wait_warp(&mma2_done, m & 1, &abort_flag);
+      // the previous step's reduce-adds have read the staging tile
+      if (leader) bulk_wait_group_read0();
+      // all four warps agree on the wait's outcome (and leave together)
+      if (!named_barrier_and(1, 128, waited)) { ok = false; break; }
       tc_fence_after();
       uint32_t v[64];
       tmem_ld_x32(tmem + lane_base + kColDQ, v);
@@ -567,18 +579,27 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&dq_free);
-      const int i = i0 + r;
-      if (i < sp.nq) {
-        float4* dst = reinterpret_cast<float4*>(
-            p.dq_acc + ((size_t)(sp.q0 + i) * p.heads_q + h) * kHeadDim);
+      #pragma unroll
+      for (int half = 0; half < 2; ++half) {
         #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          atomicAdd(dst + u, make_float4(__uint_as_float(v[4 * u]) * p.scale,
-                                         __uint_as_float(v[4 * u + 1]) * p.scale,
-                                         __uint_as_float(v[4 * u + 2]) * p.scale,
-                                         __uint_as_float(v[4 * u + 3]) * p.scale));
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* w = v + 32 * half + 4 * c;
+          st_shared_v4(stage + half * (kDqStageBytes / 2) + sw128_offset(r, c),
+                       __float_as_uint(__uint_as_float(w[0]) * p.scale),
+                       __float_as_uint(__uint_as_float(w[1]) * p.scale),
+                       __float_as_uint(__uint_as_float(w[2]) * p.scale),
+                       __float_as_uint(__uint_as_float(w[3]) * p.scale));
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
+      if (leader) {
+        tma_reduce_add_3d(&p.tm_dq, sdQ, 0, h, sp.q0 + i0);
+        tma_reduce_add_3d(&p.tm_dq, sdQ + kDqStageBytes / 2, 32, h, sp.q0 + i0);
+        bulk_commit_group();
       }
     }
+    if (leader) bulk_wait_group0();
     if (!ok) {
       abort_flag = 1;
       if (lane == 0) atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 4);

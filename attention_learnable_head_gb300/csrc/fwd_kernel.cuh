@@ -52,7 +52,7 @@ constexpr float kRescaleThreshold = 8.0f;
 // Exponentials of P: one pair in kFwdPolyEvery is evaluated with the FMA-pipe
 // polynomial (exp2_poly) instead of MUFU ex2, to balance the two pipes
 // (0 = all on MUFU).
-constexpr int kFwdPolyEvery = 4;
+constexpr int kFwdPolyEvery = 0;
 
 struct FwdParams {
   CUtensorMap tm_q;   // [T_q][H_q][64] bf16, box 64 x 1 x 128, 128B swizzle
@@ -430,7 +430,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
             const float x0 = fmaf(__uint_as_float(a[c + e]), sl2, -m_use);
             const float x1 = fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use);
             // One pair in kFwdPolyEvery goes to the FMA pipe, the rest to MUFU.
-            const bool poly = kFwdPolyEvery > 0 && (e >> 1) % kFwdPolyEvery == kFwdPolyEvery - 1;
+            constexpr int kEvery = kFwdPolyEvery > 0 ? kFwdPolyEvery : 1;
+            const bool poly = kFwdPolyEvery > 0 && (e >> 1) % kEvery == kEvery - 1;
             const float e0 = poly ? exp2_poly(x0) : ex2_approx(x0);
             const float e1 = poly ? exp2_poly(x1) : ex2_approx(x1);
             rowsum += e0 + e1;
