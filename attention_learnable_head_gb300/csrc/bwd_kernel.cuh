@@ -402,20 +402,27 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM / 2, false, false);
       const uint32_t id_dvdk = make_idesc(kFmtF16, kBlockN, kHeadDim, false, true);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      // Shared-memory descriptors, built once; an operand at byte offset o from
+      // a base is that base's descriptor plus o / 16 (the start-address field).
+      const uint64_t dK_k = make_sdesc_sw128(smem_u32(sK), 16, 1024);      // K, K-major
+      const uint64_t dK_mn = make_sdesc_sw128(smem_u32(sK), 16384, 1024);  // K, MN-major
+      const uint64_t dV_k = make_sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dQ_k = make_sdesc_sw128(smem_u32(sQ), 16, 1024);      // stage 0
+      const uint64_t dQ_mn = make_sdesc_sw128(smem_u32(sQ), 16384, 1024);
+      const uint64_t dO_k = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
+      const uint64_t dO_mn = make_sdesc_sw128(smem_u32(sdO), 16384, 1024);
+      const uint64_t dS_k = make_sdesc_sw128(smem_u32(sdS), 16, 1024);     // buffer 0
+      const uint64_t dS_mn = make_sdesc_sw128(smem_u32(sdS), 16384, 1024);
+      constexpr uint32_t kTileU = kTileBytes >> 4, kPTileU = kPTileBytes >> 4;
       // S^T / dP^T for the query half hh of step m (64 queries, N = 64).
       auto issue_s = [&](int m, int hh) {
-        const int st = m % kBwdStages;
-        const uint32_t aQ = smem_u32(sQ + st * kTileBytes) + hh * (kTileBytes / 2);
-        const uint32_t aO = smem_u32(sdO + st * kTileBytes) + hh * (kTileBytes / 2);
+        const uint32_t qo = (m % kBwdStages) * kTileU + hh * (kTileU / 2);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kColST + 64 * hh, make_sdesc_sw128(aK + 32 * k, 16, 1024),
-                 make_sdesc_sw128(aQ + 32 * k, 16, 1024), id_s, k > 0);
+          mma_ss(tmem + kColST + 64 * hh, dK_k + 2 * k, dQ_k + qo + 2 * k, id_s, k > 0);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kColDPT + 64 * hh, make_sdesc_sw128(aV + 32 * k, 16, 1024),
-                 make_sdesc_sw128(aO + 32 * k, 16, 1024), id_s, k > 0);
+          mma_ss(tmem + kColDPT + 64 * hh, dV_k + 2 * k, dO_k + qo + 2 * k, id_s, k > 0);
         mma_commit(&s_full[hh]);
       };
       bool ok = mbar_wait(&kv_full, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
@@ -426,23 +433,21 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       }
       for (int m = 0; ok && m < num; ++m) {
         const int st = m % kBwdStages;
-        const uint32_t aQ = smem_u32(sQ + st * kTileBytes);
-        const uint32_t aO = smem_u32(sdO + st * kTileBytes);
-        const uint32_t aS = smem_u32(sdS + (m & 1) * kPTileBytes);
+        const uint32_t so = (m & 1) * kPTileU;            // dS^T buffer of this step
         const bool more = m + 1 < num;
         for (int hh = 0; hh < 2; ++hh) {
           if (!mbar_wait(&p_full[hh], m & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
-          // dV += P^T dO and dK += dS^T Q over this half's 64 queries (K = 64)
+          // dV += P^T dO and dK += dS^T Q over this half's 64 queries (K = 64);
+          // B operands step 16 query rows (2048 bytes) per k.
+          const uint32_t ho = st * kTileU + hh * (kTileU / 2);
           #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kColDV, tmem + kColPT + 32 * hh + 8 * k,
-                   make_sdesc_sw128(aO + hh * (kTileBytes / 2) + k * 2048, 16384, 1024),
+            mma_ts(tmem + kColDV, tmem + kColPT + 32 * hh + 8 * k, dO_mn + ho + 128 * k,
                    id_dvdk, (m > 0 || hh > 0 || k > 0));
           #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + kColDK, make_sdesc_sw128(aS + hh * kTileBytes + 32 * k, 16, 1024),
-                   make_sdesc_sw128(aQ + hh * (kTileBytes / 2) + k * 2048, 16384, 1024),
+            mma_ss(tmem + kColDK, dS_k + so + hh * kTileU + 2 * k, dQ_mn + ho + 128 * k,
                    id_dvdk, (m > 0 || hh > 0 || k > 0));
           if (hh == 1) {
             if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
@@ -450,8 +455,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
             // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
             #pragma unroll
             for (int k = 0; k < kBlockN / 16; ++k)
-              mma_ss(tmem + kColDQ, make_sdesc_sw128(aS + k * 2048, 16384, 1024),
-                     make_sdesc_sw128(aK + k * 2048, 16384, 1024), id_dq, k > 0);
+              mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
             mma_commit(&mma2_done);
             mma_commit(&q_empty[st]);
           }

@@ -246,17 +246,21 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
       const KeyRange kr[kFwdTiles] = {kr_a, kr_b};
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
+      // Shared-memory descriptors, built once; an operand at byte offset o from a
+      // base is the base's descriptor plus o / 16 (the start-address field).
+      const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16384, 1024);   // MN-major
+      constexpr uint32_t kTileU = kTileBytes >> 4;
       // S_x(n) = Q_x K_n^T into S_x; n is a union index.
       auto issue_s = [&](int x, int n) -> bool {
         const int st = n % kFwdStages;
         if (!mbar_wait(&k_full[st], (n / kFwdStages) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ + x * kTileBytes);
-        const uint32_t aK = smem_u32(sK + st * kTileBytes);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + x * 128, make_sdesc_sw128(aQ + 32 * k, 16, 1024),
-                      make_sdesc_sw128(aK + 32 * k, 16, 1024), idesc_s, k > 0);
+          mma_ss(tmem + x * 128, dQ0 + x * kTileU + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s,
+                 k > 0);
         mma_commit(&s_full[x]);
         return true;
       };
@@ -285,13 +289,11 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
             break;
           }
           tc_fence_after();
-          const uint32_t aV = smem_u32(sV + st * kTileBytes);
           const uint32_t tP = tmem + 384 + x * 64;
           const uint32_t tO = tmem + 256 + x * 64;
           #pragma unroll
           for (int k = 0; k < kBlockN / 16; ++k)
-            mma_ts(tO, tP + 8 * k, make_sdesc_sw128(aV + k * 2048, 16384, 1024), idesc_o,
-                        (local > 0 || k > 0));
+            mma_ts(tO, tP + 8 * k, dV0 + st * kTileU + 128 * k, idesc_o, (local > 0 || k > 0));
           mma_commit(&pv_done[x]);
           if (!b_started) {
             ok = issue_s(1, kr[1].lo - lo);
