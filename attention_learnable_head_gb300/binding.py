@@ -1,6 +1,7 @@
 """ctypes binding of libattn_sink.so.
 
-``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_bwd_workspace_size``,
+``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_fwd_workspace_size``,
+``attn_sink_bwd_workspace_size``,
 ``attn_sink_status_string``, ``attn_sink_device_error`` and
 ``attn_sink_launch_count`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
@@ -69,7 +70,9 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     P = ctypes.POINTER(AttnSinkParams)
     L.attn_sink_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                c_void_p, c_void_p, c_void_p, c_void_p]
+                                c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    L.attn_sink_fwd_workspace_size.argtypes = [P]
+    L.attn_sink_fwd_workspace_size.restype = c_size_t
     L.attn_sink_fwd.restype = c_int
     L.attn_sink_bwd_workspace_size.argtypes = [P]
     L.attn_sink_bwd_workspace_size.restype = c_size_t
@@ -109,10 +112,15 @@ def _stream(stream) -> int | None:
 
 # ----------------------------------------------------------------------------- C entry points
 def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out,
-                  out_residual, lse, stream=None) -> int:
+                  out_residual, lse, workspace, workspace_bytes: int, stream=None) -> int:
     return lib().attn_sink_fwd(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
-                               _ptr(out_residual), _ptr(lse), _stream(stream))
+                               _ptr(out_residual), _ptr(lse), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream))
+
+
+def attn_sink_fwd_workspace_size(params: AttnSinkParams) -> int:
+    return int(lib().attn_sink_fwd_workspace_size(_pref(params)))
 
 
 def attn_sink_bwd_workspace_size(params: AttnSinkParams) -> int:
@@ -190,8 +198,10 @@ def forward(q, k, v, sink, *, causal: bool = True, window: int = 0,
     out = torch.empty_like(q)
     res = torch.empty_like(q) if residual else None
     lse = torch.empty((q.shape[-2], _lse_len(q)), dtype=torch.float32, device=q.device)
-    _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, res, lse, stream),
-           "attn_sink_fwd")
+    nbytes = attn_sink_fwd_workspace_size(p)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, res, lse, ws,
+                         ws.numel(), stream), "attn_sink_fwd")
     return out, lse, res
 
 

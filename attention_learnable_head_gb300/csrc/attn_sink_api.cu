@@ -156,6 +156,11 @@ int encode_rows(CUtensorMap* m, const void* ptr, int tokens, int heads,
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Forward workspace: the fp16 copy of v.
+size_t fwd_workspace_bytes(const attn_sink_params* p, const Geometry& g) {
+  return align256((size_t)g.total_k * p->heads_kv * kHeadDim * 2);
+}
+
 // How many CTAs share one (kv head, key tile) in the backward pass.  Splitting
 // the GQA group shortens the longest CTA when there are too few key tiles to
 // fill the GPU; the split partials are summed in a fixed order afterwards.
@@ -247,11 +252,16 @@ const char* attn_sink_status_string(int status) {
 
 int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
                   const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                  void* out, void* out_residual, float* lse, void* stream) {
+                  void* out, void* out_residual, float* lse, void* workspace,
+                  size_t workspace_bytes, void* stream) {
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
   if (g.num_seqs == 0 || g.total_q == 0) return ATTN_SINK_OK;   // nothing to compute
+  const size_t v16_bytes = fwd_workspace_bytes(params, g);
+  if (v16_bytes > 0 && (workspace == nullptr || workspace_bytes < v16_bytes ||
+                        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return ATTN_SINK_ERR_WORKSPACE;
   if (q == nullptr || sink == nullptr || out == nullptr || lse == nullptr)
     return ATTN_SINK_ERR_INVALID_ARG;
   if (g.total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_SINK_ERR_INVALID_ARG;
@@ -267,12 +277,21 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   // An empty key tensor is never read (every tile has no key); its map only
   // needs a valid address.
   const void* kp = g.total_k > 0 ? k : q;
-  const void* vp = g.total_k > 0 ? v : q;
+  const void* vp = g.total_k > 0 ? workspace : q;
   const int tk = g.total_k > 0 ? g.total_k : 1;
   const int hk = g.total_k > 0 ? params->heads_kv : 1;
   if ((st = encode_rows(&fp.tm_q, q, g.total_q, params->heads_q)) != ATTN_SINK_OK) return st;
   if ((st = encode_rows(&fp.tm_k, kp, tk, hk)) != ATTN_SINK_OK) return st;
-  if ((st = encode_rows(&fp.tm_v, vp, tk, hk)) != ATTN_SINK_OK) return st;
+  if ((st = encode_rows(&fp.tm_v, vp, tk, hk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != ATTN_SINK_OK)
+    return st;
+  if (g.total_k > 0) {
+    // fp16 copy of v for the P V products
+    const size_t n8 = (size_t)g.total_k * params->heads_kv * kHeadDim / 8;
+    const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
+    attn_sink_convert_f16_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(v), static_cast<uint16_t*>(workspace), n8, err);
+    if (!launched()) return ATTN_SINK_ERR_CUDA;
+  }
   fp.cu_q = cu_seqlens_q;
   fp.cu_k = cu_seqlens_k;
   fp.sink = sink;
@@ -293,6 +312,17 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   dim3 grid(params->heads_q, g.num_seqs, fp.n_qblocks);
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
   return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
+size_t attn_sink_fwd_workspace_size(const attn_sink_params* params) {
+  if (params == nullptr) return 0;
+  static const int kMarker = 0;
+  const bool packed = params->num_seqs > 0;
+  Geometry g;
+  if (validate(params, packed ? &kMarker : nullptr, packed ? &kMarker : nullptr, &g) !=
+      ATTN_SINK_OK)
+    return 0;
+  return fwd_workspace_bytes(params, g);
 }
 
 size_t attn_sink_bwd_workspace_size(const attn_sink_params* params) {

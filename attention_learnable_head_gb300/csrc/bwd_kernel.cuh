@@ -157,6 +157,22 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
   }
 }
 
+// ------------------------------------------------------------------ convert_f16
+// fp16 copy of one bf16 tensor (n8 = elements / 8), for the forward's v.
+__global__ void __launch_bounds__(256) attn_sink_convert_f16_kernel(const __nv_bfloat16* x,
+                                                                    uint16_t* x16, size_t n8,
+                                                                    int* err) {
+  bool overflow = false;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 a = reinterpret_cast<const uint4*>(x)[i];
+    reinterpret_cast<uint4*>(x16)[i] =
+        make_uint4(bf16x2_to_f16x2(a.x, &overflow), bf16x2_to_f16x2(a.y, &overflow),
+                   bf16x2_to_f16x2(a.z, &overflow), bf16x2_to_f16x2(a.w, &overflow));
+  }
+  if (overflow) atomicCAS(err, 0, DEVERR_FP16_RANGE);
+}
+
 // ------------------------------------------------------------------ kv_convert
 // fp16 copies of k and v (n8 = elements / 8 of each).
 __global__ void __launch_bounds__(256) attn_sink_kv_convert_kernel(

@@ -22,14 +22,18 @@
 // when a row's max grows by more than kRescaleThreshold (log2 units); P stays
 // below 2^threshold, and out/lse are exact because l and O use the same max.
 //
-// Warp roles (352 threads):
+// Warp roles (320 threads):
 //   warps 0-3  softmax + epilogue of tile A (thread t owns row t = TMEM lane t)
 //   warps 4-7  softmax + epilogue of tile B
 //   warp 8     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
 //   warp 9     MMA issuer (one lane) and TMEM owner
-//   warp 10    converts each landed V tile from bf16 to fp16 in place
-// TMEM columns: S_A 0, S_B 128 (128 fp32 each), O_A 256, O_B 320 (64 each),
-//               P_A 384, P_B 448 (128 fp16 packed in 64 columns each).
+// TMEM columns: S_A 0, S_B 128 (128 fp32 each; P_x, 128 fp16 two per column, is
+// written over the first 64 columns of S_x once S_x has been read), O_A 256,
+// O_B 320 (64 fp32 each), Q_A 384, Q_B 416 (64 bf16 two per column: the A
+// operand of S = Q K^T, so only K is read from shared memory).
+// P_x overwrites S_x safely: PV_x(n) is issued before S_x(n+1) by the same
+// thread, and tcgen05 MMAs from one thread execute in issue order.
+// v is read as an fp16 copy (converted into the workspace before the launch).
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -41,7 +45,7 @@ constexpr int kBlockN = 128;   // keys per tile
 constexpr int kHeadDim = 64;
 constexpr int kFwdTiles = 2;   // query tiles per CTA
 constexpr int kFwdStages = 4;
-constexpr int kFwdThreads = 352;
+constexpr int kFwdThreads = 320;
 constexpr int kFwdRowsPerCta = kFwdTiles * kBlockM;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
 constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
@@ -49,10 +53,7 @@ constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (kFwdTiles + 2 * kFwdStag
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
-// Exponentials of P: one pair in kFwdPolyEvery is evaluated with the FMA-pipe
-// polynomial (exp2_poly) instead of MUFU ex2, to balance the two pipes
-// (0 = all on MUFU).
-constexpr int kFwdPolyEvery = 0;
+constexpr uint32_t kColQ = 384;      // Q_x at kColQ + 32 x
 
 struct FwdParams {
   CUtensorMap tm_q;   // [T_q][H_q][64] bf16, box 64 x 1 x 128, 128B swizzle
@@ -120,7 +121,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, mma_drained;
   __shared__ __align__(8) uint64_t k_full[kFwdStages], v_full[kFwdStages], kv_empty[kFwdStages];
-  __shared__ __align__(8) uint64_t v_conv[kFwdStages];
+  __shared__ __align__(8) uint64_t q_tmem;
   __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -185,8 +186,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
-      mbar_init(&v_conv[s], 32);
     }
+    mbar_init(&q_tmem, kFwdTiles * kBlockM);
     for (int x = 0; x < kFwdTiles; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], kBlockM);
@@ -245,10 +246,10 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
       const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
       const KeyRange kr[kFwdTiles] = {kr_a, kr_b};
-      bool ok = mbar_wait(&q_full, 0, &abort_flag);
+      // Q_A / Q_B are in TMEM once both softmax warpgroups have copied them there.
+      bool ok = mbar_wait(&q_tmem, 0, &abort_flag);
       // Shared-memory descriptors, built once; an operand at byte offset o from a
       // base is the base's descriptor plus o / 16 (the start-address field).
-      const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16384, 1024);   // MN-major
       constexpr uint32_t kTileU = kTileBytes >> 4;
@@ -259,8 +260,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         tc_fence_after();
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + x * 128, dQ0 + x * kTileU + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s,
-                 k > 0);
+          mma_ts(tmem + x * 128, tmem + kColQ + 32 * x + 8 * k, dK0 + st * kTileU + 2 * k,
+                 idesc_s, k > 0);
         mma_commit(&s_full[x]);
         return true;
       };
@@ -284,12 +285,12 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           if (!ok || !in_range(x, n)) continue;
           const int local = lo + n - kr[x].lo;
           if (!mbar_wait(&p_full[x], local & 1, &abort_flag) ||
-              !mbar_wait(&v_conv[st], (n / kFwdStages) & 1, &abort_flag)) {
+              !mbar_wait(&v_full[st], (n / kFwdStages) & 1, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t tP = tmem + 384 + x * 64;
+          const uint32_t tP = tmem + x * 128;       // P_x over the first half of S_x
           const uint32_t tO = tmem + 256 + x * 64;
           #pragma unroll
           for (int k = 0; k < kBlockN / 16; ++k)
@@ -311,32 +312,6 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       mma_commit(&mma_drained);
       mbar_wait(&mma_drained, 0, nullptr);
     }
-  } else if (warp == 10) {
-    // ---------------------------------------------------------------- V converter
-    bool overflow = false;
-    for (int it = 0; it < num; ++it) {
-      const int st = it % kFwdStages;
-      if (!mbar_wait_warp(&v_full[st], (it / kFwdStages) & 1, &abort_flag)) {
-        if (lane == 0) {
-          abort_flag = 1;
-          atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 4);
-        }
-        break;
-      }
-      uint4* tile = reinterpret_cast<uint4*>(sV + st * kTileBytes);
-      #pragma unroll 4
-      for (int c = lane; c < (int)(kTileBytes / 16); c += 32) {
-        uint4 w = tile[c];
-        w.x = bf16x2_to_f16x2(w.x, &overflow);
-        w.y = bf16x2_to_f16x2(w.y, &overflow);
-        w.z = bf16x2_to_f16x2(w.z, &overflow);
-        w.w = bf16x2_to_f16x2(w.w, &overflow);
-        tile[c] = w;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&v_conv[st]);
-    }
-    if (overflow) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
   } else {
     // ---------------------------------------------------------------- softmax warps
     const int x = warp >> 2;                 // tile 0 (A) or 1 (B)
@@ -346,7 +321,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + x * 128 + lane_base;
     const uint32_t tO = tmem + 256 + x * 64 + lane_base;
-    const uint32_t tP = tmem + 384 + x * 64 + lane_base;
+    const uint32_t tP = tmem + x * 128 + lane_base;         // P_x over S_x columns 0..63
     const int off = sp.nk - sp.nq;
     const int tile_r0 = i0 + x * kBlockM;
     const int tile_r1 = min(tile_r0 + kBlockM, sp.nq) - 1;
@@ -356,16 +331,33 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     const float sl2 = p.scale_log2;
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
-    bool ok = true;
-    for (int it = 0; it < kx.num; ++it) {
+    // Q_x row r into TMEM (the A operand of S = Q K^T): the swizzled SMEM row
+    // holds 8 chunks of 8 bf16, i.e. the 32 packed columns in order.
+    bool ok = mbar_wait_warp(&q_full, 0, &abort_flag);
+    if (ok) {
+      uint32_t qw[32];
+      const uint32_t qrow = smem_u32(sQ + x * kTileBytes);
+      #pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 w;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "r"(qrow + sw128_offset(r, c)));
+        qw[4 * c] = w.x; qw[4 * c + 1] = w.y; qw[4 * c + 2] = w.z; qw[4 * c + 3] = w.w;
+      }
+      tmem_st_x32(tmem + kColQ + 32 * x + lane_base, qw);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(&q_tmem);
+    for (int it = 0; ok && it < kx.num; ++it) {
       if (!mbar_wait_warp(&s_full[x], it & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
       const int j0 = (kx.lo + it) * kBlockN;
       const bool need_mask = (j0 + kBlockN > sp.nk) ||
                              (p.causal && (j0 + kBlockN - 1 > tile_r0 + off ||
                                            (p.window > 0 && j0 <= tile_r1 + off - p.window)));
-      // Row max over both 64-column halves of S; the second half stays in
-      // registers for the exponentials, the first is read again afterwards.
+      // Row max over S (two 64-column halves, three-input max).
       uint32_t a[64];
       float mx = -INFINITY;
       #pragma unroll
@@ -381,7 +373,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           }
         }
         #pragma unroll
-        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(a[e]));
+        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
       }
       mx *= sl2;
       // Lazy rescale: move the max only when it grows by more than the threshold.
@@ -406,22 +398,21 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           }
         }
       }
-      // P = exp2(S * scale * log2 e - m), fp16, into TMEM P_x: second half from
-      // registers, then the first half read again.
+      // P = exp2(S * scale * log2 e - m), fp16, into TMEM P_x (over S_x columns
+      // 0..63): half 0 of S is read again and goes to P columns 0..31 (S columns
+      // already consumed), then half 1 to P columns 32..63 (also S half 0).
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       float rowsum = 0.0f;
       #pragma unroll
-      for (int half = 1; half >= 0; --half) {
-        if (half == 0) {
-          tmem_ld_x32(tS, a);
-          tmem_ld_x32(tS + 32, a + 32);
-          tmem_ld_wait();
-          if (need_mask) {
-            #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-              const int j = j0 + e;
-              if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
-            }
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld_x32(tS + 64 * half, a);
+        tmem_ld_x32(tS + 64 * half + 32, a + 32);
+        tmem_ld_wait();
+        if (need_mask) {
+          #pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int j = j0 + 64 * half + e;
+            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
           }
         }
         #pragma unroll
@@ -429,13 +420,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           uint32_t pk[16];
           #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            const float x0 = fmaf(__uint_as_float(a[c + e]), sl2, -m_use);
-            const float x1 = fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use);
-            // One pair in kFwdPolyEvery goes to the FMA pipe, the rest to MUFU.
-            constexpr int kEvery = kFwdPolyEvery > 0 ? kFwdPolyEvery : 1;
-            const bool poly = kFwdPolyEvery > 0 && (e >> 1) % kEvery == kEvery - 1;
-            const float e0 = poly ? exp2_poly(x0) : ex2_approx(x0);
-            const float e1 = poly ? exp2_poly(x1) : ex2_approx(x1);
+            const float e0 = ex2_approx(fmaf(__uint_as_float(a[c + e]), sl2, -m_use));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use));
             rowsum += e0 + e1;
             pk[e >> 1] = pack_f16x2(e0, e1);
           }

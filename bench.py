@@ -264,11 +264,14 @@ def main():
     dsink = torch.empty_like(sink)
     nws = binding.attn_sink_bwd_workspace_size(p)
     workspace = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+    fws = torch.empty(max(binding.attn_sink_fwd_workspace_size(p), 1), dtype=torch.uint8,
+                      device=dev)
     cu_arg = cu if packed else None
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def fwd():
-        st = binding.attn_sink_fwd(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse)
+        st = binding.attn_sink_fwd(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse, fws,
+                                   fws.numel())
         if st:
             raise binding.AttnSinkError(st, "attn_sink_fwd")
 

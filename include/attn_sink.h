@@ -106,7 +106,8 @@ typedef struct attn_sink_params {
  * that O instead of the bf16 out, which matters where the softmax is peaked.
  * cu_seqlens_q and cu_seqlens_k are both NULL (dense) or both non-NULL (packed).
  * Arithmetic: S = q k^T on the bf16 inputs (exact products, fp32 sums); P and
- * v enter O = P v as fp16; O accumulates in fp32.  v must lie within the fp16
+ * v enter O = P v as fp16 (v is converted into the workspace first); O
+ * accumulates in fp32.  v must lie within the fp16
  * range (|v| <= 65504), otherwise the device error word records
  * ATTN_SINK_DEVERR_FP16_RANGE (0x400).
  * Passage: listing "带汇聚的注意力（GPT-OSS）" and section "数学公式" of the
@@ -115,7 +116,16 @@ typedef struct attn_sink_params {
 int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k,
                   const void* v, const float* sink, const int* cu_seqlens_q,
                   const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
-                  void* stream);
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of device workspace attn_sink_fwd needs (0 if the params are invalid):
+ * an fp16 copy of v [T_k, H_kv, 64] for the tensor cores.  Same conventions as
+ * attn_sink_bwd_workspace_size (packed fields when num_seqs > 0).  A workspace
+ * that is missing, too small or not 256-byte aligned returns
+ * ATTN_SINK_ERR_WORKSPACE.
+ */
+size_t attn_sink_fwd_workspace_size(const attn_sink_params* params);
 
 /*
  * Bytes of device workspace attn_sink_bwd needs for these params (0 if the

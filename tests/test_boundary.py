@@ -21,6 +21,7 @@ def _lib():
 def test_exports_every_declared_symbol():
     names = binding.header_functions()
     assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
+                          "attn_sink_fwd_workspace_size",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -55,8 +56,9 @@ FAKE_ODD = FAKE + 8
 
 
 def _fwd(p, q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, res=None,
-         lse=FAKE):
-    return binding.attn_sink_fwd(p, q, k, v, sink, cu_q, cu_k, out, res, lse, stream=0)
+         lse=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    return binding.attn_sink_fwd(p, q, k, v, sink, cu_q, cu_k, out, res, lse, ws, ws_bytes,
+                                 stream=0)
 
 
 def _bwd(p, ws=FAKE, ws_bytes=1 << 40, **kw):
@@ -93,12 +95,13 @@ def test_invalid_params_rejected_on_host(field, value, status):
     assert _bwd(p) == status
     if field not in ("num_seqs",):
         assert binding.attn_sink_bwd_workspace_size(p) == 0
+        assert binding.attn_sink_fwd_workspace_size(p) == 0
 
 
 def test_null_and_misaligned_pointers():
     p = _dense()
     assert binding.attn_sink_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE,
-                                 0) == INVALID
+                                 FAKE, 1 << 40, 0) == INVALID
     assert _fwd(p, res=FAKE_ODD) == INVALID
     assert _bwd(p, res=FAKE + 2) == INVALID
     assert _fwd(p, q=None) == INVALID
@@ -131,6 +134,13 @@ def test_packed_mode_checks():
     assert binding.attn_sink_bwd_workspace_size(p) > 0
 
 
+def test_forward_workspace_checked_on_host():
+    p = _dense()
+    assert _fwd(p, ws=None) == 3
+    assert _fwd(p, ws_bytes=16) == 3
+    assert _fwd(p, ws=FAKE + 16) == 3     # not 256-byte aligned
+
+
 def test_empty_problem_is_a_no_op():
     # Nothing to compute: returns OK without touching the device or launching.
     n0 = binding.attn_sink_launch_count()
@@ -151,6 +161,10 @@ def test_workspace_size():
     n_fp32 = binding.attn_sink_bwd_workspace_size(p)
     assert n_fp32 < n_bf16       # fp32 dq is accumulated in place
     assert binding.attn_sink_bwd_workspace_size(None) == 0
+    # forward: the fp16 copy of v
+    p.grad_dtype = 0
+    assert binding.attn_sink_fwd_workspace_size(p) == 2000 * 8 * 64 * 2
+    assert binding.attn_sink_fwd_workspace_size(None) == 0
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
