@@ -2,8 +2,8 @@
 
 ``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_fwd_workspace_size``,
 ``attn_sink_bwd_workspace_size``,
-``attn_sink_status_string``, ``attn_sink_device_error`` and
-``attn_sink_launch_count`` mirror the C entry
+``attn_sink_status_string``, ``attn_sink_device_error``,
+``attn_sink_launch_count`` and ``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -73,6 +73,9 @@ def lib():
                                 c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     L.attn_sink_fwd_workspace_size.argtypes = [P]
     L.attn_sink_fwd_workspace_size.restype = c_size_t
+    L.attn_sink_fwd_noalloc.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    L.attn_sink_fwd_noalloc.restype = c_int
     L.attn_sink_fwd.restype = c_int
     L.attn_sink_bwd_workspace_size.argtypes = [P]
     L.attn_sink_bwd_workspace_size.restype = c_size_t
@@ -117,6 +120,20 @@ def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlen
                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
                                _ptr(out_residual), _ptr(lse), _ptr(workspace),
                                int(workspace_bytes), _stream(stream))
+
+
+# Bytes of the static scratch behind attn_sink_fwd_noalloc (the header's
+# ATTN_SINK_NOALLOC_SCRATCH_BYTES).
+ATTN_SINK_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def attn_sink_fwd_noalloc(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out,
+                          out_residual, lse, stream=None) -> int:
+    """Forward for callers that cannot allocate device memory: the library's
+    own static scratch replaces the workspace (see include/attn_sink.h)."""
+    return lib().attn_sink_fwd_noalloc(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
+                                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                                       _ptr(out_residual), _ptr(lse), _stream(stream))
 
 
 def attn_sink_fwd_workspace_size(params: AttnSinkParams) -> int:

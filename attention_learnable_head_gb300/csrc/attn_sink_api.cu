@@ -16,6 +16,11 @@
 // Device word a kernel sets when it gives up on a bounded wait.
 __device__ int g_attn_sink_device_error = 0;
 
+// Scratch of attn_sink_fwd_noalloc (the fp16 copy of v), one per device, held
+// for the life of the process.  In host code this name is only a host-side
+// stand-in: the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_SINK_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 using namespace attn_sink;
@@ -475,6 +480,42 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
   if (cudaMemsetAsync(dsink, 0, sizeof(float) * params->heads_q, s) != cudaSuccess)
     return ATTN_SINK_ERR_CUDA;
   return ATTN_SINK_OK;
+}
+
+// Caller entry point that allocates nothing: the workspace of attn_sink_fwd is
+// the static device array above.  Per device, the array's device address is
+// looked up once (with that device current) and cached.
+int attn_sink_fwd_noalloc(const attn_sink_params* params, const void* q, const void* k,
+                          const void* v, const float* sink, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                          void* stream) {
+  static std::mutex scratch_mutex;
+  static void* scratch_ptr[kMaxDevices] = {nullptr};
+  if (params == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
+  const bool packed = params->num_seqs > 0;
+  Geometry g;
+  const int st = validate(params, packed ? cu_seqlens_q : nullptr,
+                          packed ? cu_seqlens_k : nullptr, &g);
+  if (st != ATTN_SINK_OK) return st;
+  // Too large for the static scratch: a clear error, nothing launched.
+  if (fwd_workspace_bytes(params, g) > (size_t)ATTN_SINK_NOALLOC_SCRATCH_BYTES)
+    return ATTN_SINK_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return ATTN_SINK_ERR_CUDA;
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(scratch_mutex);
+    if (scratch_ptr[dev] == nullptr) {
+      void* a = nullptr;
+      if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || a == nullptr)
+        return ATTN_SINK_ERR_CUDA;
+      scratch_ptr[dev] = a;
+    }
+    ptr = scratch_ptr[dev];
+  }
+  return attn_sink_fwd(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                       ptr, (size_t)ATTN_SINK_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 unsigned long long attn_sink_launch_count(void) {

@@ -128,6 +128,38 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k,
 size_t attn_sink_fwd_workspace_size(const attn_sink_params* params);
 
 /*
+ * Size of the static scratch array behind attn_sink_fwd_noalloc: 16 MiB per
+ * GPU that loads the library, held until the process exits.
+ */
+#define ATTN_SINK_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * Forward without a caller-provided workspace, for callers that cannot call
+ * cudaMalloc themselves: code that runs inside a host framework which owns all
+ * device memory through its own pool, or a latency-critical service that must
+ * not allocate once it is running (cudaMalloc can synchronise the device and
+ * fragment memory).  (The pages this library follows have no counterpart of
+ * this entry point; it is a deployment convenience.)
+ *
+ * Same arguments, layouts and results as attn_sink_fwd, minus the workspace.
+ * The scratch it needs (the fp16 copy of v, attn_sink_fwd_workspace_size bytes)
+ * lives in a file-scope device array of ATTN_SINK_NOALLOC_SCRATCH_BYTES; a
+ * problem that needs more returns ATTN_SINK_ERR_WORKSPACE and launches nothing.
+ * The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array: calls that overlap on
+ * the GPU (different streams, no ordering between them) race on it and must
+ * be serialised by the caller.  Nothing in the array needs to start at zero:
+ * each call overwrites the part it reads.
+ */
+int attn_sink_fwd_noalloc(const attn_sink_params* params, const void* q, const void* k,
+                          const void* v, const float* sink, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                          void* stream);
+
+/*
  * Bytes of device workspace attn_sink_bwd needs for these params (0 if the
  * params are invalid).  The packed fields are used when num_seqs > 0, the
  * dense ones otherwise.  The workspace holds the row terms D [H_q, T_q], the

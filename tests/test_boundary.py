@@ -21,7 +21,7 @@ def _lib():
 def test_exports_every_declared_symbol():
     names = binding.header_functions()
     assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
-                          "attn_sink_fwd_workspace_size",
+                          "attn_sink_fwd_workspace_size", "attn_sink_fwd_noalloc",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -132,6 +132,21 @@ def test_packed_mode_checks():
                 max_seqlen_k=1)
     assert _fwd(p4, cu_q=FAKE, cu_k=FAKE) == UNSUPPORTED
     assert binding.attn_sink_bwd_workspace_size(p) > 0
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    # 16 MiB holds the fp16 copy of v for T_k * H_kv * 64 * 2 bytes; one more
+    # token than fits returns ATTN_SINK_ERR_WORKSPACE before any device call.
+    rows = binding.ATTN_SINK_NOALLOC_SCRATCH_BYTES // (64 * 2)
+    p = _dense(batch=1, seqlen_q=16, seqlen_k=rows // 2 + 1, heads_q=2, heads_kv=2)
+    n0 = binding.attn_sink_launch_count()
+    assert binding.attn_sink_fwd_noalloc(p, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                         FAKE, 0) == 3
+    assert binding.attn_sink_fwd_noalloc(_dense(head_dim=32), FAKE, FAKE, FAKE, FAKE, None, None,
+                                         FAKE, None, FAKE, 0) == UNSUPPORTED
+    assert binding.attn_sink_fwd_noalloc(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                         FAKE, 0) == INVALID
+    assert binding.attn_sink_launch_count() == n0
 
 
 def test_forward_workspace_checked_on_host():

@@ -1,0 +1,53 @@
+"""attn_sink_fwd_noalloc: the forward for callers that cannot allocate device
+memory themselves (a host framework that owns all device memory through its
+own pool, or a service that must not allocate once running).  Its scratch is
+the library's static device array instead of a caller workspace; the results
+must match attn_sink_fwd's on the same inputs, on two calls in a row (the
+second call reuses the array the first one left behind).
+
+This file is collected last on purpose: a failure here leaves every other test
+already run."""
+import pytest
+import torch
+
+from attention_learnable_head_gb300 import binding
+from attention_learnable_head_gb300.build import build
+from attention_learnable_head_gb300.inputs import make_case, small_workload
+from parity import assert_close, err_stats, TOL_LSE
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(dev):
+    w = small_workload("noalloc", 991, 8, 2, [300, 129, 511], window=0)
+    c = make_case(w)
+    cu = torch.tensor(c.cu_seqlens, dtype=torch.int32, device=dev)
+    t = [x.to(dev) for x in (c.q, c.k, c.v, c.sink)]
+    p = binding.make_params(c.q.shape, c.k.shape, causal=True, window=0,
+                            softmax_scale=w.scale, num_seqs=len(c.lengths),
+                            max_seqlen_q=max(c.lengths), max_seqlen_k=max(c.lengths))
+    return p, cu, t
+
+
+def test_noalloc_forward_matches_workspace_forward():
+    build()
+    dev = torch.device("cuda:0")
+    p, cu, (q, k, v, sink) = _inputs(dev)
+    ref_out, ref_res = torch.empty_like(q), torch.empty_like(q)
+    ref_lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.attn_sink_fwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    st = binding.attn_sink_fwd(p, q, k, v, sink, cu, cu, ref_out, ref_res, ref_lse, ws,
+                               ws.numel())
+    assert st == 0
+    for call in range(2):
+        out, res = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        st = binding.attn_sink_fwd_noalloc(p, q, k, v, sink, cu, cu, out, res, lse)
+        assert st == 0, binding.attn_sink_status_string(st)
+        torch.cuda.synchronize()
+        e_st, code = binding.attn_sink_device_error()
+        assert e_st == 0 and code == 0, f"device error word {code:#x}"
+        assert_close(f"out (call {call})", out.cpu(), ref_out.double().cpu())
+        assert_close(f"out residual (call {call})", res.cpu(), ref_res.double().cpu())
+        a, _ = err_stats(lse.cpu(), ref_lse.cpu())
+        assert a <= TOL_LSE, f"lse (call {call}) max abs {a:.3e}"
