@@ -3,7 +3,8 @@
 ``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_fwd_workspace_size``,
 ``attn_sink_bwd_workspace_size``,
 ``attn_sink_status_string``, ``attn_sink_device_error``,
-``attn_sink_launch_count`` and ``attn_sink_fwd_noalloc`` mirror the C entry
+``attn_sink_launch_count``, ``attn_sink_last_cuda_error`` and
+``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -44,8 +45,11 @@ class AttnSinkParams(ctypes.Structure):
 class AttnSinkError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
+        extra = ""
+        if status == 4:
+            extra = f", last CUDA error {attn_sink_last_cuda_error()}"
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
-                         f"({attn_sink_status_string(status)})")
+                         f"({attn_sink_status_string(status)}{extra})")
 
 
 _LIB = None
@@ -87,6 +91,8 @@ def lib():
     L.attn_sink_status_string.restype = ctypes.c_char_p
     L.attn_sink_device_error.argtypes = [c_void_p, ctypes.POINTER(c_int)]
     L.attn_sink_device_error.restype = c_int
+    L.attn_sink_last_cuda_error.argtypes = []
+    L.attn_sink_last_cuda_error.restype = c_int
     L.attn_sink_launch_count.argtypes = []
     L.attn_sink_launch_count.restype = ctypes.c_ulonglong
     _LIB = L
@@ -156,6 +162,10 @@ def attn_sink_bwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlen
 
 def attn_sink_status_string(status: int) -> str:
     return lib().attn_sink_status_string(int(status)).decode()
+
+
+def attn_sink_last_cuda_error() -> int:
+    return int(lib().attn_sink_last_cuda_error())
 
 
 def attn_sink_launch_count() -> int:

@@ -30,8 +30,15 @@ constexpr int kMaxDevices = 64;
 // Kernels this library has launched in this process (successful launches).
 std::atomic<unsigned long long> g_launches{0};
 
+// The most recent CUDA error a call of this library ran into (0 = none).
+std::atomic<int> g_last_cuda_error{0};
+
 inline bool launched() {
-  if (cudaGetLastError() != cudaSuccess) return false;
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    g_last_cuda_error.store((int)e, std::memory_order_relaxed);
+    return false;
+  }
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return true;
 }
@@ -517,6 +524,8 @@ int attn_sink_fwd_noalloc(const attn_sink_params* params, const void* q, const v
   return attn_sink_fwd(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
                        ptr, (size_t)ATTN_SINK_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+int attn_sink_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
 
 unsigned long long attn_sink_launch_count(void) {
   return g_launches.load(std::memory_order_relaxed);

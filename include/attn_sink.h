@@ -209,6 +209,13 @@ int attn_sink_device_error(void* stream, int* code);
  */
 unsigned long long attn_sink_launch_count(void);
 
+/*
+ * The cudaError_t value of the most recent failed kernel launch of this
+ * library in this process (0 when none failed), to explain an
+ * ATTN_SINK_ERR_CUDA status.
+ */
+int attn_sink_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

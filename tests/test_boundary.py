@@ -22,6 +22,7 @@ def test_exports_every_declared_symbol():
     names = binding.header_functions()
     assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
                           "attn_sink_fwd_workspace_size", "attn_sink_fwd_noalloc",
+                          "attn_sink_last_cuda_error",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
