@@ -22,11 +22,12 @@
 // when a row's max grows by more than kRescaleThreshold (log2 units); P stays
 // below 2^threshold, and out/lse are exact because l and O use the same max.
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax + epilogue of tile A (thread t owns row t = TMEM lane t)
-//   warps 4-7  softmax + epilogue of tile B
-//   warp 8     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
-//   warp 9     MMA issuer (one lane) and TMEM owner
+// Warp roles (576 threads):
+//   warps 0-7   softmax + epilogue of tile A: warps 0-3 take S columns 0-63,
+//               warps 4-7 columns 64-127 (thread t owns row t = TMEM lane t)
+//   warps 8-15  the same for tile B
+//   warp 16     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
+//   warp 17     MMA issuer (one lane) and TMEM owner
 // TMEM columns: S_A 0, S_B 128 (128 fp32 each; P_x, 128 fp16 two per column, is
 // written over the first 64 columns of S_x once S_x has been read), O_A 256,
 // O_B 320 (64 fp32 each), Q_A 384, Q_B 416 (64 bf16 two per column: the A
@@ -45,7 +46,9 @@ constexpr int kBlockN = 128;   // keys per tile
 constexpr int kHeadDim = 64;
 constexpr int kFwdTiles = 2;   // query tiles per CTA
 constexpr int kFwdStages = 4;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 576;    // 16 softmax warps, TMA warp, MMA warp
+constexpr int kFwdTmaWarp = 16;
+constexpr int kFwdMmaWarp = 17;
 constexpr int kFwdRowsPerCta = kFwdTiles * kBlockM;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
 constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
@@ -116,7 +119,9 @@ __device__ __forceinline__ KeyRange key_tiles(int r0, int r1, const SeqSpan& sp,
   return kr;
 }
 
-__global__ void __launch_bounds__(kFwdThreads, 1)
+// Registers are split per SM sub-partition (16384 each); with 18 warps one of the
+// four hosts 5 warps, so a thread may use at most 102: 96 is used.
+__global__ void __maxnreg__(96)
 attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, mma_drained;
@@ -125,6 +130,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
+  __shared__ float s_red_max[kFwdTiles][2][2][kBlockM];   // [tile][iteration parity][half][row]
+  __shared__ float s_red_l[kFwdTiles][2][kBlockM];        // [tile][half][row]
 
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
@@ -187,15 +194,15 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(&q_tmem, kFwdTiles * kBlockM);
+    mbar_init(&q_tmem, 2 * kFwdTiles * kBlockM);
     for (int x = 0; x < kFwdTiles; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], kBlockM);
+      mbar_init(&p_full[x], 2 * kBlockM);
       mbar_init(&pv_done[x], 1);
     }
     fence_mbarrier_init();
   }
-  if (warp == 9) {
+  if (warp == kFwdMmaWarp) {
     tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
@@ -204,7 +211,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 8) {
+  if (warp == kFwdTmaWarp) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -240,7 +247,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kFwdMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
@@ -314,173 +321,178 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else {
     // ---------------------------------------------------------------- softmax warps
-    const int x = warp >> 2;                 // tile 0 (A) or 1 (B)
-    const int r = tid & 127;                 // row within the tile = TMEM lane
+    // Tile x = warp / 8.  Half c = (warp / 4) & 1 owns S columns [64c, 64c + 64),
+    // P columns [32c, 32c + 32) and O columns [32c, 32c + 32) of the tile's rows
+    // (thread = row = TMEM lane).  The two halves of a tile exchange row maxima
+    // and sums through shared memory behind the tile's named barrier; every exit
+    // decision is taken at that barrier, so both halves always reach the same
+    // barriers.
+    const int x = warp >> 3;
+    const int c = (warp >> 2) & 1;
+    const int r = tid & 127;
     const int i = i0 + x * kBlockM + r;      // row within the sequence
     const KeyRange kx = x == 0 ? kr_a : kr_b;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + lane_base;
-    const uint32_t tO = tmem + 256 + x * 64 + lane_base;
-    const uint32_t tP = tmem + x * 128 + lane_base;         // P_x over S_x columns 0..63
+    const uint32_t tS = tmem + x * 128 + 64 * c + lane_base;
+    const uint32_t tO = tmem + 256 + x * 64 + 32 * c + lane_base;
+    const uint32_t tP = tmem + x * 128 + 32 * c + lane_base;   // P over S columns 0..63
+    const uint32_t bar_id = 1 + x;
     const int off = sp.nk - sp.nq;
     const int tile_r0 = i0 + x * kBlockM;
     const int tile_r1 = min(tile_r0 + kBlockM, sp.nq) - 1;
     const bool sink_finite = sink_h > -INFINITY;
     float m = sink_finite ? sink_h * kLog2e : -INFINITY;   // running max, log2 domain
-    float l = sink_finite ? 1.0f : 0.0f;                    // running sum, sink term = 1
+    // running sum of this half's columns; the sink's term (1) is counted in half 0
+    float l = (sink_finite && c == 0) ? 1.0f : 0.0f;
     const float sl2 = p.scale_log2;
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
-    // Q_x row r into TMEM (the A operand of S = Q K^T): the swizzled SMEM row
-    // holds 8 chunks of 8 bf16, i.e. the 32 packed columns in order.
+    // Q_x row r into TMEM (the A operand of S = Q K^T), by half 0: the swizzled
+    // SMEM row holds 8 chunks of 8 bf16, i.e. the 32 packed columns in order.
     bool ok = mbar_wait_warp(&q_full, 0, &abort_flag);
-    if (ok) {
+    if (ok && c == 0) {
       uint32_t qw[32];
       const uint32_t qrow = smem_u32(sQ + x * kTileBytes);
       #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 8; ++cc) {
         uint4 w;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                     : "r"(qrow + sw128_offset(r, c)));
-        qw[4 * c] = w.x; qw[4 * c + 1] = w.y; qw[4 * c + 2] = w.z; qw[4 * c + 3] = w.w;
+                     : "r"(qrow + sw128_offset(r, cc)));
+        qw[4 * cc] = w.x; qw[4 * cc + 1] = w.y; qw[4 * cc + 2] = w.z; qw[4 * cc + 3] = w.w;
       }
       tmem_st_x32(tmem + kColQ + 32 * x + lane_base, qw);
       tmem_st_wait();
     }
     tc_fence_before();
     mbar_arrive(&q_tmem);
-    for (int it = 0; ok && it < kx.num; ++it) {
-      if (!mbar_wait_warp(&s_full[x], it & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int j0 = (kx.lo + it) * kBlockN;
-      const bool need_mask = (j0 + kBlockN > sp.nk) ||
-                             (p.causal && (j0 + kBlockN - 1 > tile_r0 + off ||
-                                           (p.window > 0 && j0 <= tile_r1 + off - p.window)));
-      // Row max over S (two 64-column halves, three-input max).
+    for (int it = 0; it < kx.num; ++it) {
+      const bool got_s = ok && mbar_wait_warp(&s_full[x], it & 1, &abort_flag);
+      const int j0 = (kx.lo + it) * kBlockN + 64 * c;          // first key of this half
       uint32_t a[64];
-      float mx = -INFINITY;
-      #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld_x32(tS + 64 * half, a);
-        tmem_ld_x32(tS + 64 * half + 32, a + 32);
+      float pmax = -INFINITY;
+      if (got_s) {
+        tc_fence_after();
+        tmem_ld_x32(tS, a);
+        tmem_ld_x32(tS + 32, a + 32);
         tmem_ld_wait();
+        const bool need_mask = (j0 + 64 > sp.nk) ||
+                               (p.causal && (j0 + 63 > tile_r0 + off ||
+                                             (p.window > 0 && j0 <= tile_r1 + off - p.window)));
         if (need_mask) {
           #pragma unroll
           for (int e = 0; e < 64; ++e) {
-            const int j = j0 + 64 * half + e;
+            const int j = j0 + e;
             if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
           }
         }
         #pragma unroll
-        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+        for (int e = 0; e < 64; e += 2)
+          pmax = fmax3(pmax, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
       }
-      mx *= sl2;
-      // Lazy rescale: move the max only when it grows by more than the threshold.
+      s_red_max[x][it & 1][c][r] = pmax;
+      // S columns of both halves are in registers before either half writes P
+      // over S columns 0..63.
+      tc_fence_before();
+      if (!named_barrier_and(bar_id, 2 * kBlockM, got_s)) { ok = false; break; }
+      tc_fence_after();
+      const float mx = fmaxf(pmax, s_red_max[x][it & 1][c ^ 1][r]) * sl2;
+      // Lazy rescale: move the max only when it grows by more than the threshold
+      // (both halves take the same decision from the same values).
       float alpha = 1.0f;
       if (mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY)) {
         alpha = ex2_approx(m - mx);
         m = mx;
       }
       // PV of the previous key tile has finished: O may be rescaled, P_x reused.
+      // A failed wait is carried to the next barrier (never a one-sided exit).
       if (it > 0) {
-        if (!mbar_wait_warp(&pv_done[x], (it - 1) & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-          #pragma unroll
-          for (int c = 0; c < kHeadDim; c += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + c, o);
-            tmem_ld_wait();
+        if (!mbar_wait_warp(&pv_done[x], (it - 1) & 1, &abort_flag)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
             #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_x32(tO + c, o);
+            for (int q0 = 0; q0 < 32; q0 += 16) {
+              uint32_t o[16];
+              tmem_ld_x16(tO + q0, o);
+              tmem_ld_wait();
+              #pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st_x16(tO + q0, o);
+            }
           }
         }
       }
-      // P = exp2(S * scale * log2 e - m), fp16, into TMEM P_x (over S_x columns
-      // 0..63): half 0 of S is read again and goes to P columns 0..31 (S columns
-      // already consumed), then half 1 to P columns 32..63 (also S half 0).
+      // P = exp2(S * scale * log2 e - m), fp16, into this half's P columns.
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       float rowsum = 0.0f;
       #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld_x32(tS + 64 * half, a);
-        tmem_ld_x32(tS + 64 * half + 32, a + 32);
-        tmem_ld_wait();
-        if (need_mask) {
-          #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int j = j0 + 64 * half + e;
-            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
-          }
-        }
+      for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t pk[16];
         #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t pk[16];
-          #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(a[c + e]), sl2, -m_use));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(a[c + e + 1]), sl2, -m_use));
-            rowsum += e0 + e1;
-            pk[e >> 1] = pack_f16x2(e0, e1);
-          }
-          tmem_st_x16(tP + ((64 * half + c) >> 1), pk);
+        for (int e = 0; e < 32; e += 2) {
+          const float e0 = ex2_approx(fmaf(__uint_as_float(a[cc + e]), sl2, -m_use));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(a[cc + e + 1]), sl2, -m_use));
+          rowsum += e0 + e1;
+          pk[e >> 1] = pack_f16x2(e0, e1);
         }
+        tmem_st_x16(tP + (cc >> 1), pk);
       }
       l = l * alpha + rowsum;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[x]);
     }
-    if (ok && kx.num > 0 && !mbar_wait_warp(&pv_done[x], (kx.num - 1) & 1, &abort_flag))
-      ok = false;
-    if (!ok) {
+    // the last PV has landed in O
+    bool fin = ok;
+    if (fin && kx.num > 0) fin = mbar_wait_warp(&pv_done[x], (kx.num - 1) & 1, &abort_flag);
+    s_red_l[x][c][r] = l;
+    fin = named_barrier_and(bar_id, 2 * kBlockM, fin);
+    if (!fin) {
       abort_flag = 1;
       atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 3);
     } else {
       tc_fence_after();
-      const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+      const float lt = l + s_red_l[x][c ^ 1][r];
+      const float inv_l = (lt > 0.0f) ? 1.0f / lt : 0.0f;
       const bool valid = i < sp.nq;
       const size_t row = (size_t)(sp.q0 + i);
-      #pragma unroll
-      for (int c = 0; c < kHeadDim; c += 32) {
-        uint32_t o[32];
-        if (kx.num > 0) {
-          tmem_ld_x32(tO + c, o);
-          tmem_ld_wait();
-        } else {
-          #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (valid) {
-          const size_t base = (row * p.heads_q + h) * kHeadDim + c;
-          uint4* dst = reinterpret_cast<uint4*>(p.out + base);
-          uint4* dlo = p.out_lo ? reinterpret_cast<uint4*>(p.out_lo + base) : nullptr;
-          #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float f[8];
-            uint32_t hi[4], lo[4];
-            #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * u + e]) * inv_l;
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-              lo[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
-            }
-            dst[u] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            if (dlo) dlo[u] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-        }
+      uint32_t o[32];
+      if (kx.num > 0) {
+        tmem_ld_x32(tO, o);
+        tmem_ld_wait();
+      } else {
+        #pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
-      if (valid)
-        p.lse[(size_t)h * p.total_q + row] = (l > 0.0f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      if (valid) {
+        const size_t base = (row * p.heads_q + h) * kHeadDim + 32 * c;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + base);
+        uint4* dlo = p.out_lo ? reinterpret_cast<uint4*>(p.out_lo + base) : nullptr;
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float f[8];
+          uint32_t hi[4], lo[4];
+          #pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * u + e]) * inv_l;
+          #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+            lo[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
+          }
+          dst[u] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          if (dlo) dlo[u] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        if (c == 0)
+          p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kFwdMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
