@@ -3,7 +3,8 @@
 ``attn_sink_fwd``, ``attn_sink_bwd``, ``attn_sink_fwd_workspace_size``,
 ``attn_sink_bwd_workspace_size``,
 ``attn_sink_status_string``, ``attn_sink_device_error``,
-``attn_sink_launch_count``, ``attn_sink_last_cuda_error`` and
+``attn_sink_launch_count``, ``attn_sink_last_cuda_error``,
+``attn_sink_kernel_timing``, ``attn_sink_kernel_time`` and
 ``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
@@ -95,6 +96,11 @@ def lib():
     L.attn_sink_last_cuda_error.restype = c_int
     L.attn_sink_launch_count.argtypes = []
     L.attn_sink_launch_count.restype = ctypes.c_ulonglong
+    L.attn_sink_kernel_timing.argtypes = [c_int]
+    L.attn_sink_kernel_timing.restype = c_int
+    L.attn_sink_kernel_time.argtypes = [c_int, ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_ulonglong)]
+    L.attn_sink_kernel_time.restype = c_int
     _LIB = L
     return L
 
@@ -170,6 +176,22 @@ def attn_sink_last_cuda_error() -> int:
 
 def attn_sink_launch_count() -> int:
     return int(lib().attn_sink_launch_count())
+
+
+ATTN_SINK_KERNEL_FWD = 0
+ATTN_SINK_KERNEL_BWD_MAIN = 1
+
+
+def attn_sink_kernel_timing(on: bool) -> int:
+    return int(lib().attn_sink_kernel_timing(1 if on else 0))
+
+
+def attn_sink_kernel_time(kernel: int) -> tuple[int, float, int]:
+    """(status, summed milliseconds, launches) of `kernel` since its last read."""
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_ulonglong(0)
+    st = lib().attn_sink_kernel_time(int(kernel), ctypes.byref(ms), ctypes.byref(n))
+    return int(st), float(ms.value), int(n.value)
 
 
 def attn_sink_device_error(stream=None) -> tuple[int, int]:

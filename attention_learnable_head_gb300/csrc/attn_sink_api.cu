@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "attn_sink.h"
 #include "bwd_kernel.cuh"
@@ -41,6 +42,58 @@ inline bool launched() {
   }
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return true;
+}
+
+// Optional per-launch timing of the two main kernels (attn_sink_kernel_timing):
+// an event pair recorded on the launching stream around each launch, read back
+// and summed by attn_sink_kernel_time.  Events are reused through a pool.
+struct TimedLaunch {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_timing_mutex;
+std::atomic<bool> g_timing_on{false};
+std::vector<TimedLaunch> g_timing_pending;
+std::vector<cudaEvent_t> g_timing_pool;
+double g_timing_ms[ATTN_SINK_KERNEL_COUNT] = {0.0};
+unsigned long long g_timing_count[ATTN_SINK_KERNEL_COUNT] = {0};
+
+cudaEvent_t timing_event() {
+  if (!g_timing_pool.empty()) {
+    cudaEvent_t e = g_timing_pool.back();
+    g_timing_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+}
+
+// Records the start event of a timed launch; returns the pending record (or
+// kernel = -1 when timing is off or no event could be had).
+TimedLaunch timing_begin(int kernel, cudaStream_t s) {
+  TimedLaunch t{-1, nullptr, nullptr};
+  if (!g_timing_on.load(std::memory_order_relaxed)) return t;
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  t.start = timing_event();
+  t.stop = timing_event();
+  if (t.start == nullptr || t.stop == nullptr || cudaEventRecord(t.start, s) != cudaSuccess) {
+    if (t.start) g_timing_pool.push_back(t.start);
+    if (t.stop) g_timing_pool.push_back(t.stop);
+    return TimedLaunch{-1, nullptr, nullptr};
+  }
+  t.kernel = kernel;
+  return t;
+}
+
+void timing_end(const TimedLaunch& t, cudaStream_t s, bool ok) {
+  if (t.kernel < 0) return;
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  if (ok && cudaEventRecord(t.stop, s) == cudaSuccess) {
+    g_timing_pending.push_back(t);
+  } else {
+    g_timing_pool.push_back(t.start);
+    g_timing_pool.push_back(t.stop);
+  }
 }
 
 std::once_flag g_encode_once;
@@ -322,8 +375,11 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   fp.n_qblocks = (g.max_q + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
   if (fp.n_qblocks == 0) return ATTN_SINK_OK;
   dim3 grid(params->heads_q, g.num_seqs, fp.n_qblocks);
+  const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_FWD, static_cast<cudaStream_t>(stream));
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
-  return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+  const bool ok = launched();
+  timing_end(t, static_cast<cudaStream_t>(stream), ok);
+  return ok ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
 }
 
 size_t attn_sink_fwd_workspace_size(const attn_sink_params* params) {
@@ -461,8 +517,11 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     bp.n_ktiles = n_ktiles;
     bp.grad_fp32 = params->grad_dtype;
     dim3 grid(params->heads_kv * L.split, g.num_seqs, n_ktiles);
+    const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_BWD_MAIN, s);
     attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
-    if (!launched()) return ATTN_SINK_ERR_CUDA;
+    const bool ok = launched();
+    timing_end(t, s, ok);
+    if (!ok) return ATTN_SINK_ERR_CUDA;
     if (L.split > 1) {
       const size_t n4 = (size_t)g.total_k * params->heads_kv * kHeadDim / 4;
       const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)sms * 8);
@@ -523,6 +582,36 @@ int attn_sink_fwd_noalloc(const attn_sink_params* params, const void* q, const v
   }
   return attn_sink_fwd(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
                        ptr, (size_t)ATTN_SINK_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+int attn_sink_kernel_timing(int on) {
+  g_timing_on.store(on != 0, std::memory_order_relaxed);
+  return ATTN_SINK_OK;
+}
+
+int attn_sink_kernel_time(int kernel, double* total_ms, unsigned long long* launches) {
+  if (kernel < 0 || kernel >= ATTN_SINK_KERNEL_COUNT || total_ms == nullptr || launches == nullptr)
+    return ATTN_SINK_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  int status = ATTN_SINK_OK;
+  for (const TimedLaunch& t : g_timing_pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(t.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, t.start, t.stop) == cudaSuccess) {
+      g_timing_ms[t.kernel] += ms;
+      g_timing_count[t.kernel] += 1;
+    } else {
+      status = ATTN_SINK_ERR_CUDA;
+    }
+    g_timing_pool.push_back(t.start);
+    g_timing_pool.push_back(t.stop);
+  }
+  g_timing_pending.clear();
+  *total_ms = g_timing_ms[kernel];
+  *launches = g_timing_count[kernel];
+  g_timing_ms[kernel] = 0.0;
+  g_timing_count[kernel] = 0;
+  return status;
 }
 
 int attn_sink_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }

@@ -8,7 +8,8 @@ H_q=64, H_kv=8, d=64, N=4096, causal).  Prints one JSON line.
   python bench.py --impl reference ...   # the CPU float64 oracle, on host cores
 
 Timing: CUDA events on the launching stream around the fwd and bwd calls of
-each step; a 256 MiB buffer is written between steps (outside the events) so
+each step, and (recorded by the library on the same stream) around each launch
+of the forward kernel and the backward main kernel for the roofline; a 256 MiB buffer is written between steps (outside the events) so
 every step starts with a cold L2.  Under torchrun every rank runs its own
 replica (no collective in the data path); the step time is the max over ranks.
 """
@@ -63,6 +64,41 @@ def algorithmic(w, lengths):
                  + q_bytes + 2 * kv_bytes + hq * 4)                          # dq dk dv dsink
     return dict(pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, fwd_bytes=fwd_bytes,
                  bwd_bytes=bwd_bytes)
+
+
+KERNEL_SOURCES = {
+    "attn_sink_fwd_kernel": ("fwd_kernel.cuh", "sm103_ptx.cuh"),
+    "attn_sink_bwd_main_kernel": ("bwd_kernel.cuh", "sm103_ptx.cuh"),
+}
+
+
+def kernel_sources_hash(kernel: str) -> str:
+    """sha256 (first 16 hex digits) of the source files that define `kernel`."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "attention_learnable_head_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the ncu
+    counters summarised in profiles/dram_traffic.md, or None when none were taken
+    or the kernel's sources changed since (the table row carries their hash)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    want = kernel_sources_hash(kernel)
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 5 and cells[0] == kernel and cells[1] == workload:
+            try:
+                rd, wr = float(cells[2]), float(cells[3])
+            except ValueError:
+                continue
+            return rd + wr if cells[4] == want else None
+    return None
 
 
 def load_peaks():
@@ -281,12 +317,17 @@ def main():
         if st:
             raise binding.AttnSinkError(st, "attn_sink_bwd")
 
+    # per-kernel CUDA events (recorded by the library on the launching stream):
+    # on from the warm-up so the event pool is filled before the timed region
+    binding.attn_sink_kernel_timing(True)
     for _ in range(args.warmup):
         flush.fill_(1)
         fwd()
         bwd()
     torch.cuda.synchronize()
     launches_per_step = count_launches(binding, lambda: (fwd(), bwd()))
+    for kid in (binding.ATTN_SINK_KERNEL_FWD, binding.ATTN_SINK_KERNEL_BWD_MAIN):
+        binding.attn_sink_kernel_time(kid)   # discard the warm-up launches
 
     n = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -308,6 +349,15 @@ def main():
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches_timed = binding.attn_sink_launch_count() - launches0
+    binding.attn_sink_kernel_timing(False)
+    kst = {}
+    for kid in (binding.ATTN_SINK_KERNEL_FWD, binding.ATTN_SINK_KERNEL_BWD_MAIN):
+        st_k, ms_k, n_k = binding.attn_sink_kernel_time(kid)
+        if st_k != 0 or n_k != n:
+            raise RuntimeError(f"kernel timing: status {st_k}, {n_k} launches for {n} steps")
+        kst[kid] = ms_k / n_k
+    fwd_kernel_ms = kst[binding.ATTN_SINK_KERNEL_FWD]
+    bwd_main_ms = kst[binding.ATTN_SINK_KERNEL_BWD_MAIN]
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -316,9 +366,9 @@ def main():
     fwd_t, bwd_t = sum(fwd_ms) / n, sum(bwd_ms) / n
     step_ms = fwd_t + bwd_t
     if ws > 1:
-        tt = torch.tensor([step_ms, fwd_t, bwd_t], device=dev)
+        tt = torch.tensor([step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms, fwd_t, bwd_t = (float(x) for x in tt.tolist())
+        step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms = (float(x) for x in tt.tolist())
 
     # end to end through the C ABI with pinned host buffers, copies inside
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dout))
@@ -356,8 +406,15 @@ def main():
     bwd_tf = alg["bwd_flops"] / (bwd_t * 1e-3) / 1e12
     peaks, src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    dominant = "bwd" if bwd_t >= fwd_t else "fwd"
-    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
+    # the dominant kernel is the backward main kernel (all five backward
+    # products); its achieved rate is the backward's algorithmic flops over its
+    # own launch time, the forward kernel's likewise
+    bwd_main_tf = alg["bwd_flops"] / (bwd_main_ms * 1e-3) / 1e12
+    fwd_kernel_tf = alg["fwd_flops"] / (fwd_kernel_ms * 1e-3) / 1e12
+    if bwd_main_ms >= fwd_kernel_ms:
+        dom, dom_tf, dom_ms = "attn_sink_bwd_main_kernel", bwd_main_tf, bwd_main_ms
+    else:
+        dom, dom_tf, dom_ms = "attn_sink_fwd_kernel", fwd_kernel_tf, fwd_kernel_ms
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": n, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -371,17 +428,18 @@ def main():
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_ms": fwd_t, "bwd_ms": bwd_t,
         "frac_of_peak": value / peak, "fwd_frac_of_peak": fwd_tf / peak,
         "bwd_frac_of_peak": bwd_tf / peak, "peak_source": src,
-        "roofline": {"kernel": "attn_sink_bwd (bwd_pre + bwd_main + reductions)"
-                     if dominant == "bwd" else "attn_sink_fwd_kernel",
-                     "bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s",
-                     "frac": dom_tf / peak, "traffic": None,
-                     "peak_note": f"{src} dense bf16 burst"},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_tf, "peak": peak,
+                     "unit": "TFLOP/s", "frac": dom_tf / peak,
+                     "traffic": dram_traffic(dom, w.name), "kernel_ms": dom_ms,
+                     "peak_note": f"{src} dense bf16 burst (each kernel runs under 1 ms)"},
         "roofline_fwd": {"kernel": "attn_sink_fwd_kernel", "bound": "tensor",
-                         "achieved": fwd_tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": fwd_tf / peak,
-                         "hbm_gbs": alg["fwd_bytes"] / (fwd_t * 1e-3) / 1e9},
-        "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                         "achieved": fwd_kernel_tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": fwd_kernel_tf / peak, "kernel_ms": fwd_kernel_ms,
+                         "traffic": dram_traffic("attn_sink_fwd_kernel", w.name),
+                         "hbm_gbs": alg["fwd_bytes"] / (fwd_kernel_ms * 1e-3) / 1e9},
+        "e2e": None if args.ncu else {
+            "value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_timed,
         "gpu_launches_per_step": launches_per_step,
         "clocks": clocks,

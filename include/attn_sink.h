@@ -216,6 +216,31 @@ unsigned long long attn_sink_launch_count(void);
  */
 int attn_sink_last_cuda_error(void);
 
+/*
+ * Measurement hooks (no counterpart in the papers: they time this library's
+ * own kernels).  Kernel ids for attn_sink_kernel_time:
+ */
+#define ATTN_SINK_KERNEL_FWD 0      /* attn_sink_fwd_kernel (the whole forward product) */
+#define ATTN_SINK_KERNEL_BWD_MAIN 1 /* attn_sink_bwd_main_kernel (all five backward products) */
+#define ATTN_SINK_KERNEL_COUNT 2
+
+/*
+ * on != 0: from now on every launch of the two kernels above is bracketed by a
+ * pair of CUDA events recorded on the launching stream (the events belong to
+ * the library and are reused); on == 0 stops that.  Off at load.  Always
+ * returns ATTN_SINK_OK.
+ */
+int attn_sink_kernel_timing(int on);
+
+/*
+ * Waits for every bracketed launch recorded so far, then writes the summed
+ * duration in milliseconds (*total_ms) and the number of launches (*launches)
+ * of `kernel` since the previous read of that kernel, and resets both.
+ * ATTN_SINK_ERR_INVALID_ARG for a bad id or null pointer; ATTN_SINK_ERR_CUDA
+ * if an event could not be read (those launches are left out of the sums).
+ */
+int attn_sink_kernel_time(int kernel, double* total_ms, unsigned long long* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,8 @@ def test_exports_every_declared_symbol():
     names = binding.header_functions()
     assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
                           "attn_sink_fwd_workspace_size", "attn_sink_fwd_noalloc",
-                          "attn_sink_last_cuda_error",
+                          "attn_sink_last_cuda_error", "attn_sink_kernel_timing",
+                          "attn_sink_kernel_time",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -148,6 +149,17 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     assert binding.attn_sink_fwd_noalloc(None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None,
                                          FAKE, 0) == INVALID
     assert binding.attn_sink_launch_count() == n0
+
+
+def test_kernel_time_without_launches():
+    # No timed launch has happened in this process: zero sums, OK status; a bad
+    # id or a null pointer is an argument error.
+    assert binding.attn_sink_kernel_timing(False) == OK
+    for k in (binding.ATTN_SINK_KERNEL_FWD, binding.ATTN_SINK_KERNEL_BWD_MAIN):
+        assert binding.attn_sink_kernel_time(k) == (OK, 0.0, 0)
+    assert binding.attn_sink_kernel_time(2)[0] == INVALID
+    assert binding.attn_sink_kernel_time(-1)[0] == INVALID
+    assert binding.lib().attn_sink_kernel_time(0, None, None) == INVALID
 
 
 def test_forward_workspace_checked_on_host():
