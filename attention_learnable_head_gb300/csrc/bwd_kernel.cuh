@@ -18,9 +18,10 @@
 //                 dQ   = dS K         (A = dS^T read MN-major, once per step)
 //               Two compute warpgroups own one query half each, so the tensor
 //               cores run one half's products while the other half's exponentials
-//               are computed.  dK and dV stay in TMEM for the whole loop; dQ is
-//               added into the fp32 accumulator with vector atomics by a
-//               dedicated warpgroup.
+//               are computed.  dK and dV stay in TMEM for the whole loop; a
+//               dedicated warpgroup moves each step's dQ from TMEM into a
+//               swizzled shared-memory tile that a TMA reduce-add sums into
+//               the fp32 accumulator.
 //   dsink_reduce  fixed-order tree over the partials (bitwise reproducible).
 //   dq_convert  fp32 accumulator -> bf16 dq.
 #pragma once

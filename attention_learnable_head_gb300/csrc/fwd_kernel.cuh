@@ -2,13 +2,13 @@
 //
 // One CTA per (query head h, sequence, 256-row query block).  The block is two
 // 128-row tiles, A and B, that share every K/V tile and run in ping-pong: while
-// one softmax warpgroup turns its S tile into P, the tensor cores run the other
+// one tile's softmax turns its S tile into P, the tensor cores run the other
 // tile's MMAs.  Per tile and key tile:
-//   S = Q K^T (tcgen05, fp32 accumulators in TMEM),
+//   S = Q K^T (tcgen05, bf16 operands from SMEM, fp32 accumulators in TMEM),
 //   online softmax whose running max and sum start from the sink logit
 //   (m0 = sink[h] * log2 e, l0 = 1 in the exp2 domain),
 //   P (fp16) written to TMEM and consumed there by O += P V (tcgen05, A from
-//   TMEM, V converted to fp16 in SMEM by a converter warp),
+//   TMEM; V read as fp16 from SMEM, converted into the workspace before launch),
 // then out = O / l (bf16, plus optionally the bf16 residual O/l - out) and
 // lse = ln 2 * (m + log2 l), which includes the sink.  S = Q K^T multiplies the
 // bf16 inputs exactly; P and V go to the tensor cores as fp16 (11-bit
@@ -18,23 +18,28 @@
 // concat listing "带汇聚的注意力（GPT-OSS）" on the euno.news page, and the
 // P_ij / P_ih equations of its section "数学公式".
 //
-// Rescaling of O is lazy: the running max used for the exponentials only moves
-// when a row's max grows by more than kRescaleThreshold (log2 units); P stays
-// below 2^threshold, and out/lse are exact because l and O use the same max.
+// Each key tile's 128 columns are two halves of 64 (c = 0, 1) with their own
+// softmax warps, running max m_c, sum l_c and accumulator O_c = sum P V over
+// the half's keys, so the halves never wait for each other inside the loop.  A
+// row's halves are merged once, at the end, like two key blocks of a split
+// softmax: m = max(m_0, m_1), l = sum l_c 2^(m_c - m), O = sum O_c 2^(m_c - m).
+// The sink's term (1 at m = sink log2 e) is counted in half 0.
+//
+// Rescaling of O_c is lazy: the running max used for the exponentials only
+// moves when a row's max grows by more than kRescaleThreshold (log2 units); P
+// stays below 2^threshold, and out/lse are exact because l_c and O_c use the
+// same max.
 //
 // Warp roles (576 threads):
-//   warps 0-7   softmax + epilogue of tile A: warps 0-3 take S columns 0-63,
-//               warps 4-7 columns 64-127 (thread t owns row t = TMEM lane t)
-//   warps 8-15  the same for tile B
+//   warps 0-3   softmax of tile A, key half 0 (thread t owns row t = TMEM lane t)
+//   warps 4-7   tile A, key half 1;   warps 8-11 / 12-15: tile B, halves 0 / 1
 //   warp 16     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
 //   warp 17     MMA issuer (one lane) and TMEM owner
-// TMEM columns: S_A 0, S_B 128 (128 fp32 each; P_x, 128 fp16 two per column, is
-// written over the first 64 columns of S_x once S_x has been read), O_A 256,
-// O_B 320 (64 fp32 each), Q_A 384, Q_B 416 (64 bf16 two per column: the A
-// operand of S = Q K^T, so only K is read from shared memory).
-// P_x overwrites S_x safely: PV_x(n) is issued before S_x(n+1) by the same
+// TMEM columns: S_A 0, S_B 128 (128 fp32 each; P_xc, 64 fp16 two per column, is
+// written over the first 32 columns of half c of S_x once read), O_A0 256,
+// O_A1 320, O_B0 384, O_B1 448 (64 fp32 each).
+// P_xc overwrites S_x safely: PV_x(n) is issued before S_x(n+1) by the same
 // thread, and tcgen05 MMAs from one thread execute in issue order.
-// v is read as an fp16 copy (converted into the workspace before the launch).
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -56,7 +61,6 @@ constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (kFwdTiles + 2 * kFwdStag
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr uint32_t kColQ = 384;      // Q_x at kColQ + 32 x
 
 struct FwdParams {
   CUtensorMap tm_q;   // [T_q][H_q][64] bf16, box 64 x 1 x 128, 128B swizzle
@@ -125,13 +129,12 @@ __global__ void __maxnreg__(96)
 attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, mma_drained;
-  __shared__ __align__(8) uint64_t k_full[kFwdStages], v_full[kFwdStages], kv_empty[kFwdStages];
-  __shared__ __align__(8) uint64_t q_tmem;
-  __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles];
+  __shared__ __align__(8) uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
+  __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles][2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ float s_red_max[kFwdTiles][2][2][kBlockM];   // [tile][iteration parity][half][row]
-  __shared__ float s_red_l[kFwdTiles][2][kBlockM];        // [tile][half][row]
+  __shared__ float s_red_m[kFwdTiles][2][kBlockM];   // [tile][half][row], epilogue only
+  __shared__ float s_red_l[kFwdTiles][2][kBlockM];
 
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
@@ -190,15 +193,13 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     mbar_init(&q_full, 1);
     mbar_init(&mma_drained, 1);
     for (int s = 0; s < kFwdStages; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(&q_tmem, 2 * kFwdTiles * kBlockM);
     for (int x = 0; x < kFwdTiles; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], 2 * kBlockM);
-      mbar_init(&pv_done[x], 1);
+      for (int c = 0; c < 2; ++c) mbar_init(&pv_done[x][c], 1);
     }
     fence_mbarrier_init();
   }
@@ -231,10 +232,9 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           break;
         }
         const int row = sp.k0 + (lo + it) * kBlockN;
-        mbar_arrive_expect_tx(&k_full[st], kTileBytes);
-        tma_load_3d_hint(&p.tm_k, &k_full[st], sK + st * kTileBytes, 0, g, row, keep);
-        mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-        tma_load_3d_hint(&p.tm_v, &v_full[st], sV + st * kTileBytes, 0, g, row, keep);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
+        tma_load_3d_hint(&p.tm_k, &kv_full[st], sK + st * kTileBytes, 0, g, row, keep);
+        tma_load_3d_hint(&p.tm_v, &kv_full[st], sV + st * kTileBytes, 0, g, row, keep);
         issued = it + 1;
       }
       if (abort_flag) {
@@ -242,72 +242,97 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         mbar_wait(&q_full, 0, nullptr);
         for (int it = max(0, issued - kFwdStages); it < issued; ++it) {
           const int st = it % kFwdStages;
-          mbar_wait(&k_full[st], (it / kFwdStages) & 1, nullptr);
-          mbar_wait(&v_full[st], (it / kFwdStages) & 1, nullptr);
+          mbar_wait(&kv_full[st], (it / kFwdStages) & 1, nullptr);
         }
       }
     }
   } else if (warp == kFwdMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
+    // Per tile x and key tile n: S_x = Q_x K_n^T (M=N=128) into TMEM; the softmax
+    // of key half c (S_x columns [64c, 64c+64)) writes P_xc (fp16) over the first
+    // 32 of its columns, and O_xc += P_xc V_n[64c, 64c+64) (M=128, N=64, K=64, A
+    // from TMEM).  S_x(n+1) is issued right after PV_x0(n) and PV_x1(n): the same
+    // thread issues them and tcgen05 MMAs execute in issue order, so both P_xc are
+    // read before S_x(n+1) overwrites them.
+    // The tensor pipe holds little more than the MMA being executed, so every
+    // pause of this thread between MMAs (an mbarrier wait costs ~200 cycles even
+    // when the phase has already completed) leaves it idle: the thread waits once
+    // per key tile for K/V and once per tile for P, and issues 12 MMAs in a row.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
       const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
       const KeyRange kr[kFwdTiles] = {kr_a, kr_b};
-      // Q_A / Q_B are in TMEM once both softmax warpgroups have copied them there.
-      bool ok = mbar_wait(&q_tmem, 0, &abort_flag);
+      bool ok = mbar_wait(&q_full, 0, &abort_flag);
       // Shared-memory descriptors, built once; an operand at byte offset o from a
       // base is the base's descriptor plus o / 16 (the start-address field).
+      const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16384, 1024);   // MN-major
       constexpr uint32_t kTileU = kTileBytes >> 4;
-      // S_x(n) = Q_x K_n^T into S_x; n is a union index.
-      auto issue_s = [&](int x, int n) -> bool {
-        const int st = n % kFwdStages;
-        if (!mbar_wait(&k_full[st], (n / kFwdStages) & 1, &abort_flag)) return false;
+      constexpr uint32_t kHalfU = (64 * kHeadDim * 2) >> 4;   // 64 rows of V
+      // K/V of union key tiles [0, kv_seen] have landed (waited in order).
+      int kv_seen = -1;
+      auto kv_ready = [&](int n) -> bool {
+        for (int a = kv_seen + 1; a <= n; ++a) {
+          if (!mbar_wait(&kv_full[a % kFwdStages], (a / kFwdStages) & 1, &abort_flag))
+            return false;
+          kv_seen = a;
+        }
         tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int x, int n) {
+        const int st = n % kFwdStages;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ts(tmem + x * 128, tmem + kColQ + 32 * x + 8 * k, dK0 + st * kTileU + 2 * k,
-                 idesc_s, k > 0);
+          mma_ss(tmem + x * 128, dQ0 + x * kTileU + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s,
+                 k > 0);
         mma_commit(&s_full[x]);
-        return true;
       };
       auto in_range = [&](int x, int n) {
         const int a = lo + n;
         return kr[x].num > 0 && a >= kr[x].lo && a < kr[x].lo + kr[x].num;
       };
-      // Stagger the tiles: S_B(first) is issued once tile A's first P is ready,
-      // so B's softmax overlaps A's MMAs instead of competing with A's for MUFU.
-      bool b_started = kr[1].num == 0;
-      if (kr[0].num > 0) {
-        ok = issue_s(0, kr[0].lo - lo);
-      } else {
-        ok = issue_s(1, kr[1].lo - lo);
-        b_started = true;
+      // First S of every tile whose first key tile is within the ring's reach; a
+      // tile that starts later gets it at the top of its first step.
+      bool started[kFwdTiles];
+      #pragma unroll
+      for (int x = 0; x < kFwdTiles; ++x) {
+        started[x] = false;
+        if (ok && kr[x].num > 0 && kr[x].lo - lo < kFwdStages) {
+          ok = kv_ready(kr[x].lo - lo);
+          if (ok) issue_s(x, kr[x].lo - lo);
+          started[x] = true;
+        }
       }
       for (int n = 0; ok && n < num; ++n) {
         const int st = n % kFwdStages;
+        // K/V of the next key tile (for S(n+1)); V(n) was waited with K(n).
+        if (n + 1 < num && !kv_ready(n + 1)) { ok = false; break; }
         #pragma unroll
         for (int x = 0; x < kFwdTiles; ++x) {
-          if (!ok || !in_range(x, n)) continue;
+          if (!in_range(x, n)) continue;
           const int local = lo + n - kr[x].lo;
-          if (!mbar_wait(&p_full[x], local & 1, &abort_flag) ||
-              !mbar_wait(&v_full[st], (n / kFwdStages) & 1, &abort_flag)) {
-            ok = false;
-            break;
+          if (!started[x]) {
+            issue_s(x, n);
+            started[x] = true;
           }
+          if (!mbar_wait(&p_full[x], local & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t tP = tmem + x * 128;       // P_x over the first half of S_x
-          const uint32_t tO = tmem + 256 + x * 64;
           #pragma unroll
-          for (int k = 0; k < kBlockN / 16; ++k)
-            mma_ts(tO, tP + 8 * k, dV0 + st * kTileU + 128 * k, idesc_o, (local > 0 || k > 0));
-          mma_commit(&pv_done[x]);
-          if (!b_started) {
-            ok = issue_s(1, kr[1].lo - lo);
-            b_started = true;
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t tP = tmem + x * 128 + 64 * c;   // P_xc over S_x
+            const uint32_t tO = tmem + 256 + x * 128 + 64 * c;
+            #pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(tO, tP + 8 * k, dV0 + st * kTileU + c * kHalfU + 128 * k, idesc_o,
+                     (local > 0 || k > 0));
           }
-          if (ok && in_range(x, n + 1)) ok = issue_s(x, n + 1);
+          if (local == kr[x].num - 1) {
+            mma_commit(&pv_done[x][0]);
+            mma_commit(&pv_done[x][1]);
+          }
+          if (in_range(x, n + 1)) issue_s(x, n + 1);
         }
         if (ok) mma_commit(&kv_empty[st]);
       }
@@ -321,12 +346,11 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else {
     // ---------------------------------------------------------------- softmax warps
-    // Tile x = warp / 8.  Half c = (warp / 4) & 1 owns S columns [64c, 64c + 64),
-    // P columns [32c, 32c + 32) and O columns [32c, 32c + 32) of the tile's rows
-    // (thread = row = TMEM lane).  The two halves of a tile exchange row maxima
-    // and sums through shared memory behind the tile's named barrier; every exit
-    // decision is taken at that barrier, so both halves always reach the same
-    // barriers.
+    // Tile x = warp / 8, key half c = (warp / 4) & 1: S_x columns [64c, 64c+64).
+    // Thread = row = TMEM lane.  Each half keeps its own running max m, sum l and
+    // accumulator O_xc over the keys of its half, so the halves never wait for
+    // each other inside the loop; a row's two halves are merged once, in the
+    // epilogue (the same merge as two key blocks of a split softmax).
     const int x = warp >> 3;
     const int c = (warp >> 2) & 1;
     const int r = tid & 127;
@@ -334,51 +358,38 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     const KeyRange kx = x == 0 ? kr_a : kr_b;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + x * 128 + 64 * c + lane_base;
-    const uint32_t tO = tmem + 256 + x * 64 + 32 * c + lane_base;
-    const uint32_t tP = tmem + x * 128 + 32 * c + lane_base;   // P over S columns 0..63
+    const uint32_t tP = tS;                                     // P over S_xc
+    const uint32_t tOx = tmem + 256 + x * 128 + lane_base;      // O_x0; O_x1 at +64
+    const uint32_t tO = tOx + 64 * c;
     const uint32_t bar_id = 1 + x;
     const int off = sp.nk - sp.nq;
     const int tile_r0 = i0 + x * kBlockM;
     const int tile_r1 = min(tile_r0 + kBlockM, sp.nq) - 1;
     const bool sink_finite = sink_h > -INFINITY;
-    float m = sink_finite ? sink_h * kLog2e : -INFINITY;   // running max, log2 domain
-    // running sum of this half's columns; the sink's term (1) is counted in half 0
+    // running max (log2 domain) starts at the sink logit in both halves; the
+    // sink's term of the sum (1 at m = sink log2 e) is counted in half 0 only
+    float m = sink_finite ? sink_h * kLog2e : -INFINITY;
     float l = (sink_finite && c == 0) ? 1.0f : 0.0f;
     const float sl2 = p.scale_log2;
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
-    // Q_x row r into TMEM (the A operand of S = Q K^T), by half 0: the swizzled
-    // SMEM row holds 8 chunks of 8 bf16, i.e. the 32 packed columns in order.
-    bool ok = mbar_wait_warp(&q_full, 0, &abort_flag);
-    if (ok && c == 0) {
-      uint32_t qw[32];
-      const uint32_t qrow = smem_u32(sQ + x * kTileBytes);
-      #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint4 w;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                     : "r"(qrow + sw128_offset(r, cc)));
-        qw[4 * cc] = w.x; qw[4 * cc + 1] = w.y; qw[4 * cc + 2] = w.z; qw[4 * cc + 3] = w.w;
-      }
-      tmem_st_x32(tmem + kColQ + 32 * x + lane_base, qw);
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    mbar_arrive(&q_tmem);
+    bool ok = true;
     for (int it = 0; it < kx.num; ++it) {
-      const bool got_s = ok && mbar_wait_warp(&s_full[x], it & 1, &abort_flag);
+      if (!mbar_wait_warp(&s_full[x], it & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after();
       const int j0 = (kx.lo + it) * kBlockN + 64 * c;          // first key of this half
-      uint32_t a[64];
-      float pmax = -INFINITY;
-      if (got_s) {
-        tc_fence_after();
+      const bool need_mask = (j0 + 64 > sp.nk) ||
+                             (p.causal && (j0 + 63 > tile_r0 + off ||
+                                           (p.window > 0 && j0 <= tile_r1 + off - p.window)));
+      // Pass 1: row max over the 64 columns (four independent 3-input max chains).
+      // The exponentials re-read S from TMEM 32 columns at a time (pass 2), which
+      // keeps the registers live at once low enough to avoid spills.
+      float mx;
+      {
+        uint32_t a[64];
         tmem_ld_x32(tS, a);
         tmem_ld_x32(tS + 32, a + 32);
         tmem_ld_wait();
-        const bool need_mask = (j0 + 64 > sp.nk) ||
-                               (p.causal && (j0 + 63 > tile_r0 + off ||
-                                             (p.window > 0 && j0 <= tile_r1 + off - p.window)));
         if (need_mask) {
           #pragma unroll
           for (int e = 0; e < 64; ++e) {
@@ -386,67 +397,76 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
             if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
           }
         }
+        float q0 = __uint_as_float(a[0]), q1 = __uint_as_float(a[1]);
+        float q2 = __uint_as_float(a[2]), q3 = __uint_as_float(a[3]);
         #pragma unroll
-        for (int e = 0; e < 64; e += 2)
-          pmax = fmax3(pmax, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+        for (int e = 4; e < 64; e += 8) {
+          q0 = fmax3(q0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+          q1 = fmax3(q1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+          q2 = fmax3(q2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+          q3 = fmax3(q3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+        }
+        mx = fmaxf(fmax3(q0, q1, q2), q3) * sl2;
       }
-      s_red_max[x][it & 1][c][r] = pmax;
-      // S columns of both halves are in registers before either half writes P
-      // over S columns 0..63.
-      tc_fence_before();
-      if (!named_barrier_and(bar_id, 2 * kBlockM, got_s)) { ok = false; break; }
-      tc_fence_after();
-      const float mx = fmaxf(pmax, s_red_max[x][it & 1][c ^ 1][r]) * sl2;
-      // Lazy rescale: move the max only when it grows by more than the threshold
-      // (both halves take the same decision from the same values).
+      // Lazy rescale: the max only moves when it grows by more than the threshold.
       float alpha = 1.0f;
       if (mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY)) {
         alpha = ex2_approx(m - mx);
         m = mx;
       }
-      // PV of the previous key tile has finished: O may be rescaled, P_x reused.
-      // A failed wait is carried to the next barrier (never a one-sided exit).
-      if (it > 0) {
-        if (!mbar_wait_warp(&pv_done[x], (it - 1) & 1, &abort_flag)) {
-          ok = false;
-        } else {
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-            #pragma unroll
-            for (int q0 = 0; q0 < 32; q0 += 16) {
-              uint32_t o[16];
-              tmem_ld_x16(tO + q0, o);
-              tmem_ld_wait();
-              #pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st_x16(tO + q0, o);
-            }
-          }
+      // S_x(it) completing implies PV_xc(it - 1) completed (issued before it by
+      // the same thread): O_xc may be rescaled and P_xc overwritten.
+      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        #pragma unroll
+        for (int q = 0; q < 64; q += 16) {
+          uint32_t o[16];
+          tmem_ld_x16(tO + q, o);
+          tmem_ld_wait();
+          #pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_x16(tO + q, o);
         }
       }
-      // P = exp2(S * scale * log2 e - m), fp16, into this half's P columns.
+      // Pass 2: P = exp2(S * scale * log2 e - m), fp16, 32 columns at a time.  P of
+      // columns [32u, 32u + 32) goes to P columns [16u, 16u + 16), i.e. over S
+      // columns that this thread has already read (P_xc lies over the first 32
+      // columns of its half).
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      float rowsum = 0.0f;
+      float rs0 = 0.0f, rs1 = 0.0f;
       #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t a[32];
+        tmem_ld_x32(tS + cc, a);
+        tmem_ld_wait();
+        if (need_mask) {
+          #pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = j0 + cc + e;
+            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+          }
+        }
         uint32_t pk[16];
         #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(a[cc + e]), sl2, -m_use));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(a[cc + e + 1]), sl2, -m_use));
-          rowsum += e0 + e1;
+          const float e0 = ex2_approx(fmaf(__uint_as_float(a[e]), sl2, -m_use));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(a[e + 1]), sl2, -m_use));
+          rs0 += e0;
+          rs1 += e1;
           pk[e >> 1] = pack_f16x2(e0, e1);
         }
         tmem_st_x16(tP + (cc >> 1), pk);
       }
-      l = l * alpha + rowsum;
+      l = l * alpha + (rs0 + rs1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[x]);
     }
-    // the last PV has landed in O
+    // Both halves' last PV have landed in O_x0 / O_x1.
     bool fin = ok;
-    if (fin && kx.num > 0) fin = mbar_wait_warp(&pv_done[x], (kx.num - 1) & 1, &abort_flag);
+    if (fin && kx.num > 0)
+      fin = mbar_wait_warp(&pv_done[x][0], 0, &abort_flag) &&
+            mbar_wait_warp(&pv_done[x][1], 0, &abort_flag);
+    s_red_m[x][c][r] = m;
     s_red_l[x][c][r] = l;
     fin = named_barrier_and(bar_id, 2 * kBlockM, fin);
     if (!fin) {
@@ -454,19 +474,27 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 3);
     } else {
       tc_fence_after();
-      const float lt = l + s_red_l[x][c ^ 1][r];
+      // merge the halves: m_t = max(m_0, m_1), weights 2^(m_c - m_t)
+      const float m0 = s_red_m[x][0][r], m1 = s_red_m[x][1][r];
+      const float mt = fmaxf(m0, m1);
+      const float w0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - mt);
+      const float w1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - mt);
+      const float lt = s_red_l[x][0][r] * w0 + s_red_l[x][1][r] * w1;
       const float inv_l = (lt > 0.0f) ? 1.0f / lt : 0.0f;
       const bool valid = i < sp.nq;
       const size_t row = (size_t)(sp.q0 + i);
-      uint32_t o[32];
+      // this half writes output columns [32c, 32c + 32)
+      uint32_t o0[32], o1[32];
       if (kx.num > 0) {
-        tmem_ld_x32(tO, o);
+        tmem_ld_x32(tOx + 32 * c, o0);
+        tmem_ld_x32(tOx + 64 + 32 * c, o1);
         tmem_ld_wait();
       } else {
         #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
+        for (int e = 0; e < 32; ++e) { o0[e] = 0u; o1[e] = 0u; }
       }
       if (valid) {
+        const float s0 = w0 * inv_l, s1 = w1 * inv_l;
         const size_t base = (row * p.heads_q + h) * kHeadDim + 32 * c;
         uint4* dst = reinterpret_cast<uint4*>(p.out + base);
         uint4* dlo = p.out_lo ? reinterpret_cast<uint4*>(p.out_lo + base) : nullptr;
@@ -475,7 +503,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           float f[8];
           uint32_t hi[4], lo[4];
           #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * u + e]) * inv_l;
+          for (int e = 0; e < 8; ++e)
+            f[e] = __uint_as_float(o0[8 * u + e]) * s0 + __uint_as_float(o1[8 * u + e]) * s1;
           #pragma unroll
           for (int e = 0; e < 4; ++e) {
             hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
@@ -485,7 +514,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           if (dlo) dlo[u] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         if (c == 0)
-          p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+          p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (mt + __log2f(lt)) * kLn2 : -INFINITY;
       }
     }
   }

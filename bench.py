@@ -73,12 +73,18 @@ KERNEL_SOURCES = {
 
 
 def kernel_sources_hash(kernel: str) -> str:
-    """sha256 (first 16 hex digits) of the source files that define `kernel`."""
+    """sha256 (first 16 hex digits) of the code of the source files that define
+    `kernel`: comments removed and whitespace collapsed, so that only a change
+    of code counts."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "attention_learnable_head_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "attention_learnable_head_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -284,10 +290,7 @@ def main():
     sink = case.sink.to(dev)
     packed = w.is_varlen
     kw = dict(causal=w.causal, window=w.window, softmax_scale=w.scale)
-    if packed:
-        kw.update(cu_seqlens_q=cu, cu_seqlens_k=cu, max_seqlen_q=max(lengths),
-                  max_seqlen_k=max(lengths))
-    else:
+    if not packed:
         b, n = len(lengths), lengths[0]
         q, dout = q.view(b, n, *q.shape[1:]), dout.view(b, n, *dout.shape[1:])
         k, v = k.view(b, n, *k.shape[1:]), v.view(b, n, *v.shape[1:])
