@@ -285,6 +285,34 @@ __device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, 
   }
 }
 
+// P^T and dS^T of 32 queries of one key row (thread = key), fp16-packed:
+//   P  = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
+//   dS = P (dP - D)
+// With kMask, entries whose (query, key) pair is not visible, or whose row or
+// key lies past the sequence, are exact zeros.
+template <bool kMask>
+__device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t* dr,
+                                              const float* lse_row, const float* d_row,
+                                              float sl2, int i_first, int imin, int imax,
+                                              int nq, bool key_ok, uint32_t* pk, uint32_t* dk) {
+  #pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float pv[2], dv[2];
+    #pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -lse_row[e + u] * kLog2e));
+      if (kMask) {
+        const int i = i_first + e + u;
+        if (!key_ok || i < imin || i > imax || i >= nq) pe = 0.0f;
+      }
+      pv[u] = pe;
+      dv[u] = pe * (__uint_as_float(dr[e + u]) - d_row[e + u]);
+    }
+    pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
+    dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
+  }
+}
+
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -524,23 +552,14 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tmem_ld_x32(tmem + lane_base + kColDPT + 64 * hh + c, dr);
         tmem_ld_wait();
         uint32_t pk[16], dk[16];
-        #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
-          #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int ci = 64 * hh + c + e + u;           // query within the step tile
-            float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -s_lse[st][ci] * kLog2e));
-            if (need_mask) {
-              const int i = i0 + c + e + u;
-              if (!key_ok || i < imin || i > imax || i >= sp.nq) pe = 0.0f;
-            }
-            pv[u] = pe;
-            dv[u] = pe * (__uint_as_float(dr[e + u]) - s_D[st][ci]);
-          }
-          pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
-          dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
-        }
+        // The mask test is hoisted out of the element loop (a branch per element
+        // keeps the compiler from interleaving the elements' exponentials).
+        if (need_mask)
+          bwd_pds_chunk<true>(sr, dr, &s_lse[st][64 * hh + c], &s_D[st][64 * hh + c], sl2,
+                              i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
+        else
+          bwd_pds_chunk<false>(sr, dr, &s_lse[st][64 * hh + c], &s_D[st][64 * hh + c], sl2,
+                               i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
         tmem_st_x16(tmem + lane_base + kColPT + 32 * hh + (c >> 1), pk);
         // dS^T row r, queries c..c+31 of this half: 4 chunks of 16 bytes
         #pragma unroll

@@ -381,33 +381,30 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       const bool need_mask = (j0 + 64 > sp.nk) ||
                              (p.causal && (j0 + 63 > tile_r0 + off ||
                                            (p.window > 0 && j0 <= tile_r1 + off - p.window)));
-      // Pass 1: row max over the 64 columns (four independent 3-input max chains).
-      // The exponentials re-read S from TMEM 32 columns at a time (pass 2), which
-      // keeps the registers live at once low enough to avoid spills.
-      float mx;
-      {
-        uint32_t a[64];
-        tmem_ld_x32(tS, a);
-        tmem_ld_x32(tS + 32, a + 32);
-        tmem_ld_wait();
-        if (need_mask) {
-          #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int j = j0 + e;
-            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
-          }
-        }
-        float q0 = __uint_as_float(a[0]), q1 = __uint_as_float(a[1]);
-        float q2 = __uint_as_float(a[2]), q3 = __uint_as_float(a[3]);
+      // S of this half, read from TMEM once (each tcgen05.ld competes with the
+      // MMAs for TMEM, so S is not read a second time for the exponentials).
+      uint32_t a[64];
+      tmem_ld_x32(tS, a);
+      tmem_ld_x32(tS + 32, a + 32);
+      tmem_ld_wait();
+      if (need_mask) {
         #pragma unroll
-        for (int e = 4; e < 64; e += 8) {
-          q0 = fmax3(q0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-          q1 = fmax3(q1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-          q2 = fmax3(q2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
-          q3 = fmax3(q3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+        for (int e = 0; e < 64; ++e) {
+          const int j = j0 + e;
+          if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
         }
-        mx = fmaxf(fmax3(q0, q1, q2), q3) * sl2;
       }
+      // row max over the 64 columns: four independent 3-input max chains
+      float q0 = __uint_as_float(a[0]), q1 = __uint_as_float(a[1]);
+      float q2 = __uint_as_float(a[2]), q3 = __uint_as_float(a[3]);
+      #pragma unroll
+      for (int e = 4; e < 64; e += 8) {
+        q0 = fmax3(q0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+        q1 = fmax3(q1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+        q2 = fmax3(q2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+        q3 = fmax3(q3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+      }
+      const float mx = fmaxf(fmax3(q0, q1, q2), q3) * sl2;
       // Lazy rescale: the max only moves when it grows by more than the threshold.
       float alpha = 1.0f;
       if (mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY)) {
@@ -427,29 +424,17 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           tmem_st_x16(tO + q, o);
         }
       }
-      // Pass 2: P = exp2(S * scale * log2 e - m), fp16, 32 columns at a time.  P of
-      // columns [32u, 32u + 32) goes to P columns [16u, 16u + 16), i.e. over S
-      // columns that this thread has already read (P_xc lies over the first 32
-      // columns of its half).
+      // P = exp2(S * scale * log2 e - m), fp16, over the first 32 columns of this
+      // half of S_x (already read into registers).
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       float rs0 = 0.0f, rs1 = 0.0f;
       #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t a[32];
-        tmem_ld_x32(tS + cc, a);
-        tmem_ld_wait();
-        if (need_mask) {
-          #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = j0 + cc + e;
-            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
-          }
-        }
         uint32_t pk[16];
         #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(a[e]), sl2, -m_use));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(a[e + 1]), sl2, -m_use));
+          const float e0 = ex2_approx(fmaf(__uint_as_float(a[cc + e]), sl2, -m_use));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(a[cc + e + 1]), sl2, -m_use));
           rs0 += e0;
           rs1 += e1;
           pk[e >> 1] = pack_f16x2(e0, e1);
