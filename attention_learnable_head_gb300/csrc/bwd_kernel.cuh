@@ -47,9 +47,11 @@ constexpr int kBwdSmemBytes = 1024 + 2 * (int)kTileBytes + kBwdStages * 2 * (int
 // Dynamic + static shared memory must stay within the 227 KB a CTA may use.
 static_assert(kBwdSmemBytes + 4096 <= 232448, "backward shared memory over the per-CTA limit");
 
-// P^T (fp16, two per column): query half hh at 448 + 32 hh.
+// P^T (fp16, two per column) of query half hh is written over the first 32
+// columns of that half of S^T once read.  K and V (fp16, two per column) are
+// copied into TMEM once, as the A operands of S^T = K Q^T and dP^T = V dO^T.
 constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 320, kColDQ = 384,
-                   kColPT = 448;
+                   kColK = 448, kColV = 480;
 
 struct BwdParams {
   CUtensorMap tm_q;    // [T_q][H_q][64] fp16 copy of q
@@ -316,7 +318,7 @@ __device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full, mma2_done, dq_free, drained;
+  __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, dq_free, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];
   __shared__ float s_lse[kBwdStages][kBlockM];    // lse rows of the step (natural log)
@@ -373,6 +375,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&kv_full, 1);
+    mbar_init(&kv_tmem, 2 * kBlockN);
     mbar_init(&mma2_done, 1);
     mbar_init(&dq_free, kBlockM);
     mbar_init(&drained, 1);
@@ -449,9 +452,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
       // Shared-memory descriptors, built once; an operand at byte offset o from
       // a base is that base's descriptor plus o / 16 (the start-address field).
-      const uint64_t dK_k = make_sdesc_sw128(smem_u32(sK), 16, 1024);      // K, K-major
       const uint64_t dK_mn = make_sdesc_sw128(smem_u32(sK), 16384, 1024);  // K, MN-major
-      const uint64_t dV_k = make_sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint64_t dQ_k = make_sdesc_sw128(smem_u32(sQ), 16, 1024);      // stage 0
       const uint64_t dQ_mn = make_sdesc_sw128(smem_u32(sQ), 16384, 1024);
       const uint64_t dO_k = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
@@ -464,13 +465,14 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         const uint32_t qo = (m % kBwdStages) * kTileU + hh * (kTileU / 2);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kColST + 64 * hh, dK_k + 2 * k, dQ_k + qo + 2 * k, id_s, k > 0);
+          mma_ts(tmem + kColST + 64 * hh, tmem + kColK + 8 * k, dQ_k + qo + 2 * k, id_s, k > 0);
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kColDPT + 64 * hh, dV_k + 2 * k, dO_k + qo + 2 * k, id_s, k > 0);
+          mma_ts(tmem + kColDPT + 64 * hh, tmem + kColV + 8 * k, dO_k + qo + 2 * k, id_s, k > 0);
         mma_commit(&s_full[hh]);
       };
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
+      // kv_tmem: K and V are in TMEM (the compute warps copied them from SMEM)
+      bool ok = mbar_wait(&kv_tmem, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -488,7 +490,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           const uint32_t ho = st * kTileU + hh * (kTileU / 2);
           #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kColDV, tmem + kColPT + 32 * hh + 8 * k, dO_mn + ho + 128 * k,
+            mma_ts(tmem + kColDV, tmem + kColST + 64 * hh + 8 * k, dO_mn + ho + 128 * k,
                    id_dvdk, (m > 0 || hh > 0 || k > 0));
           #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -506,8 +508,9 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           }
           if (more) {
             // next step's half hh: its S^T / dP^T columns were read by this half
-            if (!mbar_wait(&q_full[(m + 1) % kBwdStages], ((m + 1) / kBwdStages) & 1,
-                           &abort_flag)) { ok = false; break; }
+            // (Q / dO of the next step are waited for once, before its half 0)
+            if (hh == 0 && !mbar_wait(&q_full[(m + 1) % kBwdStages], ((m + 1) / kBwdStages) & 1,
+                                      &abort_flag)) { ok = false; break; }
             tc_fence_after();
             issue_s(m + 1, hh);
           }
@@ -531,8 +534,26 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const int imin = p.causal ? j - off : 0;
     const int imax = (p.causal && p.window > 0) ? j - off + p.window - 1 : sp.nq - 1;
     const bool key_ok = j < sp.nk;
-    bool ok = true;
-    for (int m = 0; m < num; ++m) {
+    // K (warpgroup 0) or V (warpgroup 1) row r into TMEM: the swizzled SMEM row
+    // holds 8 chunks of 8 fp16, i.e. the 32 packed columns in order.
+    bool ok = mbar_wait_warp(&kv_full, 0, &abort_flag);
+    if (ok) {
+      uint32_t w[32];
+      const uint32_t row = smem_u32(hh == 0 ? sK : sV);
+      #pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint4 q4;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(q4.x), "=r"(q4.y), "=r"(q4.z), "=r"(q4.w)
+                     : "r"(row + sw128_offset(r, cc)));
+        w[4 * cc] = q4.x; w[4 * cc + 1] = q4.y; w[4 * cc + 2] = q4.z; w[4 * cc + 3] = q4.w;
+      }
+      tmem_st_x32(tmem + lane_base + (hh == 0 ? kColK : kColV), w);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(&kv_tmem);
+    for (int m = 0; ok && m < num; ++m) {
       const int st = m % kBwdStages;
       const int i0 = (qt_first + m % nqt) * kBlockM + 64 * hh;   // first query of this half
       // q_full: the producer's lse / D rows of this step are in SMEM.
@@ -560,7 +581,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         else
           bwd_pds_chunk<false>(sr, dr, &s_lse[st][64 * hh + c], &s_D[st][64 * hh + c], sl2,
                                i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
-        tmem_st_x16(tmem + lane_base + kColPT + 32 * hh + (c >> 1), pk);
+        // P^T over S^T columns this thread has already read (chunk c -> c / 2)
+        tmem_st_x16(tmem + lane_base + kColST + 64 * hh + (c >> 1), pk);
         // dS^T row r, queries c..c+31 of this half: 4 chunks of 16 bytes
         #pragma unroll
         for (int u = 0; u < 4; ++u)
