@@ -266,7 +266,7 @@ BwdLayout bwd_layout(const attn_sink_params* p, const Geometry& g, int sm_count)
   L.split = choose_split(p, g, sm_count);
   size_t off = 0;
   L.off_D = off;
-  off += align256((size_t)p->heads_q * g.total_q * sizeof(float));
+  off += align256((size_t)p->heads_q * g.total_q * sizeof(float2));
   L.off_part = off;
   off += align256((size_t)p->heads_q * std::max(L.n_blocks, 1) * sizeof(float));
   L.off_dq = off;
@@ -431,7 +431,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     return ATTN_SINK_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* D = reinterpret_cast<float*>(ws + L.off_D);
+  float2* LD = reinterpret_cast<float2*>(ws + L.off_D);
   float* partials = reinterpret_cast<float*>(ws + L.off_part);
   float* dq_acc = params->grad_dtype == 1 ? static_cast<float*>(dq)
                                           : reinterpret_cast<float*>(ws + L.off_dq);
@@ -453,7 +453,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     pp.dout = static_cast<const __nv_bfloat16*>(dout);
     pp.lse = lse;
     pp.sink = sink;
-    pp.D = D;
+    pp.LD = LD;
     pp.partials = partials;
     pp.dq_acc = dq_acc;
     pp.total_q = g.total_q;
@@ -494,8 +494,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
       return st;
     bp.cu_q = cu_seqlens_q;
     bp.cu_k = cu_seqlens_k;
-    bp.lse = lse;
-    bp.D = D;
+    bp.LD = LD;
     bp.dq_acc = dq_acc;
     bp.dk = dk;
     bp.dv = dv;

@@ -61,8 +61,7 @@ struct BwdParams {
   CUtensorMap tm_dq;   // [T_q][H_q][64] fp32 dq accumulator, box 32 x 1 x 128, 128B swizzle
   const int* cu_q;
   const int* cu_k;
-  const float* lse;    // [H_q][T_q]
-  const float* D;      // [H_q][T_q]
+  const float2* LD;    // [H_q][T_q]: (lse * log2 e, D) per query row
   float* dq_acc;       // [T_q][H_q][64] fp32, pre-zeroed
   void* dk;            // [T_k][H_kv][64] bf16 or fp32 (split == 1)
   void* dv;
@@ -88,7 +87,7 @@ struct PreParams {
   const __nv_bfloat16* dout;
   const float* lse;
   const float* sink;
-  float* D;            // [H_q][T_q]
+  float2* LD;          // [H_q][T_q]: (lse * log2 e, D)
   float* partials;     // [H_q][n_blocks]
   float* dq_acc;       // [T_q][H_q][64]
   uint16_t* q16;       // [T_q][H_q][64] fp16 copy of q
@@ -138,8 +137,8 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
     d += __shfl_xor_sync(0xffffffffu, d, 2);
     d += __shfl_xor_sync(0xffffffffu, d, 4);
     if (sub == 0 && t < p.total_q) {
-      p.D[(size_t)h * p.total_q + t] = d;
       const float lse = p.lse[(size_t)h * p.total_q + t];
+      p.LD[(size_t)h * p.total_q + t] = make_float2(lse * kLog2e, d);
       // P_ih = exp(sink - lse); zero when the sink is -inf.
       if (sink_h > -INFINITY && lse > -INFINITY)
         acc -= ex2_approx((sink_h - lse) * kLog2e) * d;
@@ -290,11 +289,12 @@ __device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, 
 // P^T and dS^T of 32 queries of one key row (thread = key), fp16-packed:
 //   P  = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
 //   dS = P (dP - D)
+// ld_row holds (lse * log2 e, D) of the 32 queries.
 // With kMask, entries whose (query, key) pair is not visible, or whose row or
 // key lies past the sequence, are exact zeros.
 template <bool kMask>
 __device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t* dr,
-                                              const float* lse_row, const float* d_row,
+                                              const float2* ld_row,
                                               float sl2, int i_first, int imin, int imax,
                                               int nq, bool key_ok, uint32_t* pk, uint32_t* dk) {
   #pragma unroll
@@ -302,13 +302,14 @@ __device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t
     float pv[2], dv[2];
     #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -lse_row[e + u] * kLog2e));
+      const float2 ld = ld_row[e + u];
+      float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -ld.x));
       if (kMask) {
         const int i = i_first + e + u;
         if (!key_ok || i < imin || i > imax || i >= nq) pe = 0.0f;
       }
       pv[u] = pe;
-      dv[u] = pe * (__uint_as_float(dr[e + u]) - d_row[e + u]);
+      dv[u] = pe * (__uint_as_float(dr[e + u]) - ld.y);
     }
     pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
     dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
@@ -321,8 +322,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, dq_free, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];
-  __shared__ float s_lse[kBwdStages][kBlockM];    // lse rows of the step (natural log)
-  __shared__ float s_D[kBwdStages][kBlockM];
+  __shared__ float2 s_LD[kBwdStages][kBlockM];    // (lse * log2 e, D) of the step's rows
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -427,14 +427,13 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tma_load_3d(&p.tm_q, &q_full[st], sQ + st * kTileBytes, 0, h, sp.q0 + i0);
         tma_load_3d(&p.tm_do, &q_full[st], sdO + st * kTileBytes, 0, h, sp.q0 + i0);
       }
-      // lse / D of the step's 128 query rows, copied asynchronously; rows past
-      // the sequence read a valid row and are masked by the compute warps.
+      // (lse log2 e, D) of the step's 128 query rows, copied asynchronously; rows
+      // past the sequence read a valid row and are masked by the compute warps.
       #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = lane + 32 * u;
         const size_t idx = (size_t)h * p.total_q + sp.q0 + min(i0 + t, sp.nq - 1);
-        cp_async_4(smem_u32(&s_lse[st][t]), p.lse + idx);
-        cp_async_4(smem_u32(&s_D[st][t]), p.D + idx);
+        cp_async_8(smem_u32(&s_LD[st][t]), p.LD + idx);
       }
       cp_async_mbar_arrive_noinc(&q_full[st]);
       issued = m + 1;
@@ -576,10 +575,10 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         // The mask test is hoisted out of the element loop (a branch per element
         // keeps the compiler from interleaving the elements' exponentials).
         if (need_mask)
-          bwd_pds_chunk<true>(sr, dr, &s_lse[st][64 * hh + c], &s_D[st][64 * hh + c], sl2,
+          bwd_pds_chunk<true>(sr, dr, &s_LD[st][64 * hh + c], sl2,
                               i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
         else
-          bwd_pds_chunk<false>(sr, dr, &s_lse[st][64 * hh + c], &s_D[st][64 * hh + c], sl2,
+          bwd_pds_chunk<false>(sr, dr, &s_LD[st][64 * hh + c], sl2,
                                i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
         // P^T over S^T columns this thread has already read (chunk c -> c / 2)
         tmem_st_x16(tmem + lane_base + kColST + 64 * hh + (c >> 1), pk);

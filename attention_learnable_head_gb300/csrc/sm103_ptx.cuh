@@ -183,6 +183,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 8-byte asynchronous global -> shared copy (both addresses 8-byte aligned).
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 // noinc: the arrival is already counted in the barrier's expected count.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
