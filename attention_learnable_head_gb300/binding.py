@@ -4,8 +4,8 @@
 ``attn_sink_bwd_workspace_size``,
 ``attn_sink_status_string``, ``attn_sink_device_error``,
 ``attn_sink_launch_count``, ``attn_sink_last_cuda_error``,
-``attn_sink_kernel_timing``, ``attn_sink_kernel_time`` and
-``attn_sink_fwd_noalloc`` mirror the C entry
+``attn_sink_kernel_timing``, ``attn_sink_kernel_time``, ``attn_sink_fwd_chunk``,
+``attn_sink_merge`` and ``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -82,6 +82,13 @@ def lib():
                                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     L.attn_sink_fwd_noalloc.restype = c_int
     L.attn_sink_fwd.restype = c_int
+    L.attn_sink_fwd_chunk.argtypes = [P, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                      c_void_p]
+    L.attn_sink_fwd_chunk.restype = c_int
+    L.attn_sink_merge.argtypes = [c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    L.attn_sink_merge.restype = c_int
     L.attn_sink_bwd_workspace_size.argtypes = [P]
     L.attn_sink_bwd_workspace_size.restype = c_size_t
     L.attn_sink_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -132,6 +139,24 @@ def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlen
                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
                                _ptr(out_residual), _ptr(lse), _ptr(workspace),
                                int(workspace_bytes), _stream(stream))
+
+
+def attn_sink_fwd_chunk(params: AttnSinkParams, q_pos0: int, q, k, v, cu_seqlens_q,
+                        cu_seqlens_k, out, out_residual, lse, workspace, workspace_bytes: int,
+                        stream=None) -> int:
+    return lib().attn_sink_fwd_chunk(_pref(params), int(q_pos0), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                                     _ptr(out_residual), _ptr(lse), _ptr(workspace),
+                                     int(workspace_bytes), _stream(stream))
+
+
+def attn_sink_merge(num_chunks: int, total_q: int, heads_q: int, head_dim: int, o_parts,
+                    o_residual_parts, lse_parts, sink, out, out_residual, lse,
+                    stream=None) -> int:
+    return lib().attn_sink_merge(int(num_chunks), int(total_q), int(heads_q), int(head_dim),
+                                 _ptr(o_parts), _ptr(o_residual_parts), _ptr(lse_parts),
+                                 _ptr(sink), _ptr(out), _ptr(out_residual), _ptr(lse),
+                                 _stream(stream))
 
 
 # Bytes of the static scratch behind attn_sink_fwd_noalloc (the header's
@@ -251,6 +276,40 @@ def forward(q, k, v, sink, *, causal: bool = True, window: int = 0,
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, res, lse, ws,
                          ws.numel(), stream), "attn_sink_fwd")
+    return out, lse, res
+
+
+def forward_chunk(q, k, v, q_pos0: int, *, causal: bool = True, window: int = 0,
+                  softmax_scale: float | None = None, cu_seqlens_q=None, cu_seqlens_k=None,
+                  max_seqlen_q: int | None = None, max_seqlen_k: int | None = None,
+                  residual: bool = True, stream=None):
+    """(out, lse, out_residual) of the queries over one key chunk, without the
+    sink (attn_sink_fwd_chunk); k, v hold the chunk's keys."""
+    num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
+                    num_seqs=num_seqs, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+    out = torch.empty_like(q)
+    res = torch.empty_like(q) if residual else None
+    lse = torch.empty((q.shape[-2], _lse_len(q)), dtype=torch.float32, device=q.device)
+    nbytes = attn_sink_fwd_workspace_size(p)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(attn_sink_fwd_chunk(p, q_pos0, q, k, v, cu_seqlens_q, cu_seqlens_k, out, res, lse,
+                               ws, ws.numel(), stream), "attn_sink_fwd_chunk")
+    return out, lse, res
+
+
+def merge(outs, lses, sink, *, residuals=None, stream=None):
+    """(out, lse, out_residual) of the whole key sequence from the chunks'
+    results (attn_sink_merge): outs like q, lses [H_q, T_q], residuals optional."""
+    o = torch.stack(list(outs)).contiguous()
+    ls = torch.stack(list(lses)).contiguous()
+    r = None if residuals is None else torch.stack(list(residuals)).contiguous()
+    out = torch.empty_like(o[0])
+    res = torch.empty_like(o[0])
+    lse = torch.empty_like(ls[0])
+    heads, d = o.shape[-2], o.shape[-1]
+    _check(attn_sink_merge(o.shape[0], ls.shape[-1], heads, d, o, r, ls, sink, out, res, lse,
+                           stream), "attn_sink_merge")
     return out, lse, res
 
 

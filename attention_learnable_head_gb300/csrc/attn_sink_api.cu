@@ -13,6 +13,7 @@
 #include "attn_sink.h"
 #include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
+#include "merge_kernel.cuh"
 
 // Device word a kernel sets when it gives up on a bounded wait.
 __device__ int g_attn_sink_device_error = 0;
@@ -315,10 +316,16 @@ const char* attn_sink_status_string(int status) {
   }
 }
 
-int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
-                  const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                  void* out, void* out_residual, float* lse, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward, with or without the sink; `chunk` selects key-chunk mode (no
+// sink, query row i at key position i + q_pos0 in every sequence).
+int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const void* v,
+             const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k, void* out,
+             void* out_residual, float* lse, void* workspace, size_t workspace_bytes,
+             void* stream, bool chunk, int q_pos0) {
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -327,9 +334,10 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   if (v16_bytes > 0 && (workspace == nullptr || workspace_bytes < v16_bytes ||
                         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return ATTN_SINK_ERR_WORKSPACE;
-  if (q == nullptr || sink == nullptr || out == nullptr || lse == nullptr)
+  if (q == nullptr || (!chunk && sink == nullptr) || out == nullptr || lse == nullptr)
     return ATTN_SINK_ERR_INVALID_ARG;
   if (g.total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_SINK_ERR_INVALID_ARG;
+  if (chunk && (q_pos0 > (1 << 30) || q_pos0 < -(1 << 30))) return ATTN_SINK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(out_residual))
     return ATTN_SINK_ERR_INVALID_ARG;
@@ -372,6 +380,8 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   fp.causal = params->causal;
   fp.window = params->window > 0 ? params->window : 0;
   fp.scale_log2 = params->softmax_scale * kLog2e;
+  fp.chunk = chunk ? 1 : 0;
+  fp.q_pos0 = chunk ? q_pos0 : 0;
   fp.n_qblocks = (g.max_q + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
   if (fp.n_qblocks == 0) return ATTN_SINK_OK;
   dim3 grid(params->heads_q, g.num_seqs, fp.n_qblocks);
@@ -380,6 +390,59 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
   const bool ok = launched();
   timing_end(t, static_cast<cudaStream_t>(stream), ok);
   return ok ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
+                  const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  void* out, void* out_residual, float* lse, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  return fwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  workspace, workspace_bytes, stream, false, 0);
+}
+
+int attn_sink_fwd_chunk(const attn_sink_params* params, int q_pos0, const void* q,
+                        const void* k, const void* v, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(params, q, k, v, nullptr, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  workspace, workspace_bytes, stream, true, q_pos0);
+}
+
+int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, const void* o_parts,
+                    const void* o_residual_parts, const float* lse_parts, const float* sink,
+                    void* out, void* out_residual, float* lse, void* stream) {
+  if (num_chunks < 1 || total_q < 0 || heads_q < 1) return ATTN_SINK_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
+  if (total_q == 0) return ATTN_SINK_OK;
+  if (o_parts == nullptr || lse_parts == nullptr || sink == nullptr || out == nullptr ||
+      lse == nullptr)
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o_residual_parts) || !aligned16(out) ||
+      !aligned16(out_residual))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  int sms = 0;
+  int* err = nullptr;
+  int st;
+  if ((st = device_state(&sms, &err)) != ATTN_SINK_OK) return st;
+  MergeParams mp;
+  mp.o_parts = static_cast<const __nv_bfloat16*>(o_parts);
+  mp.res_parts = static_cast<const __nv_bfloat16*>(o_residual_parts);
+  mp.lse_parts = lse_parts;
+  mp.sink = sink;
+  mp.out = static_cast<__nv_bfloat16*>(out);
+  mp.out_lo = static_cast<__nv_bfloat16*>(out_residual);
+  mp.lse = lse;
+  mp.num_chunks = num_chunks;
+  mp.total_q = total_q;
+  mp.heads_q = heads_q;
+  const size_t pairs = (size_t)total_q * heads_q;
+  const int blocks = (int)std::min<size_t>((pairs + 31) / 32, (size_t)sms * 8);
+  attn_sink_merge_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(mp);
+  return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
 }
 
 size_t attn_sink_fwd_workspace_size(const attn_sink_params* params) {

@@ -79,6 +79,10 @@ struct FwdParams {
   int causal, window;
   float scale_log2;   // softmax_scale * log2(e)
   int n_qblocks;      // 256-row query blocks of the longest sequence
+  // Key-chunk mode: no sink term, and query row i of every sequence sits at key
+  // position i + q_pos0 (the default is bottom-right: q_pos0 = N_k - N_q).
+  int chunk;
+  int q_pos0;
 };
 
 struct SeqSpan {
@@ -107,11 +111,10 @@ struct KeyRange {
   int lo, num;
 };
 
-__device__ __forceinline__ KeyRange key_tiles(int r0, int r1, const SeqSpan& sp, int causal,
-                                              int window) {
+__device__ __forceinline__ KeyRange key_tiles(int r0, int r1, const SeqSpan& sp, int off,
+                                              int causal, int window) {
   KeyRange kr{0, 0};
   if (r1 < r0) return kr;
-  const int off = sp.nk - sp.nq;
   int kv_lo = 0, kv_hi = sp.nk;
   if (causal) {
     kv_hi = min(sp.nk, r1 + off + 1);
@@ -146,9 +149,11 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const bool has_b = i0 + kBlockM < sp.nq;
-  const KeyRange kr_a = key_tiles(i0, min(i0 + kBlockM, sp.nq) - 1, sp, p.causal, p.window);
+  // key position of query row 0 (bottom-right alignment unless chunk mode sets it)
+  const int off = p.chunk ? p.q_pos0 : sp.nk - sp.nq;
+  const KeyRange kr_a = key_tiles(i0, min(i0 + kBlockM, sp.nq) - 1, sp, off, p.causal, p.window);
   const KeyRange kr_b = has_b ? key_tiles(i0 + kBlockM, min(i0 + 2 * kBlockM, sp.nq) - 1, sp,
-                                          p.causal, p.window)
+                                          off, p.causal, p.window)
                               : KeyRange{0, 0};
   // union of the two tiles' key ranges
   int lo, hi;
@@ -161,7 +166,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     lo = kr_b.lo; hi = kr_b.lo + kr_b.num;
   }
   const int num = (kr_a.num > 0 || kr_b.num > 0) ? hi - lo : 0;
-  const float sink_h = __ldg(p.sink + h);
+  // chunk mode: no sink (its logit is -inf, i.e. absent from the normaliser)
+  const float sink_h = p.chunk ? -INFINITY : __ldg(p.sink + h);
 
   if (num == 0) {
     // No row of this block sees a key: out = 0, lse = sink (the sink alone).
@@ -362,7 +368,6 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     const uint32_t tOx = tmem + 256 + x * 128 + lane_base;      // O_x0; O_x1 at +64
     const uint32_t tO = tOx + 64 * c;
     const uint32_t bar_id = 1 + x;
-    const int off = sp.nk - sp.nq;
     const int tile_r0 = i0 + x * kBlockM;
     const int tile_r1 = min(tile_r0 + kBlockM, sp.nq) - 1;
     const bool sink_finite = sink_h > -INFINITY;

@@ -119,6 +119,50 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k,
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Forward over one chunk of the keys, without the sink: for sequence
+ * parallelism, where each piece of a long key sequence is attended separately
+ * and the pieces are combined by attn_sink_merge.  Passage: the keryc.com page
+ * on GPT-OSS agentic RL fixes, section "Solutions implemented by the team"
+ * (sequence parallelism compatible with attention sinks), and the concat
+ * listing "带汇聚的注意力（GPT-OSS）" of the euno.news page (the sink column
+ * must enter the softmax once, so a chunk carries none).
+ * k, v hold the chunk's keys (params->seqlen_k / cu_seqlens_k describe the
+ * chunk).  q_pos0: key index within the chunk aligned with query row 0 of
+ * every sequence: row i sees chunk key j iff j <= i + q_pos0 (causal) and
+ * j > i + q_pos0 - W (window W > 0).  For the chunk that starts at key k0 of
+ * a key sequence of length N_k queried by N_q rows, q_pos0 = N_k - N_q - k0;
+ * |q_pos0| <= 2^30.  Ignored when params->causal = 0.
+ * Writes out [T_q, H_q, 64] bf16 (attention over the chunk alone, normalised
+ * within it), optional out_residual, and lse [H_q, T_q] = log sum_j exp(S_ij)
+ * over the chunk (-inf, with out = 0, for rows that see no key of it).
+ * Workspace, layouts, precision and errors as attn_sink_fwd; sink is not used.
+ */
+int attn_sink_fwd_chunk(const attn_sink_params* params, int q_pos0, const void* q,
+                        const void* k, const void* v, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Sink-aware merge of num_chunks results of attn_sink_fwd_chunk over the
+ * chunks of one key sequence:
+ *   Z = sum_c exp(lse_c) + exp(sink[h]),  out = sum_c exp(lse_c - log Z) out_c,
+ *   lse = log Z,
+ * i.e. the attention of the whole key sequence with the sink counted once
+ * (concat listing "带汇聚的注意力（GPT-OSS）" and section "数学公式" of the
+ * euno.news page).  Device pointers: o_parts [C, T_q, H_q, 64] bf16 (the
+ * chunks' out, stacked), o_residual_parts likewise or NULL, lse_parts
+ * [C, H_q, T_q] fp32, sink [H_q] fp32; writes out [T_q, H_q, 64] bf16, its
+ * optional residual out_residual, and lse [H_q, T_q] (-inf with out = 0 when
+ * no chunk has a visible key and the sink is -inf).  head_dim must be 64
+ * (ATTN_SINK_ERR_UNSUPPORTED otherwise); num_chunks >= 1, heads_q >= 1 and
+ * 16-byte aligned tensors, else ATTN_SINK_ERR_INVALID_ARG.  total_q = 0 is a
+ * no-op.  The merge runs in fp32.
+ */
+int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, const void* o_parts,
+                    const void* o_residual_parts, const float* lse_parts, const float* sink,
+                    void* out, void* out_residual, float* lse, void* stream);
+
+/*
  * Bytes of device workspace attn_sink_fwd needs (0 if the params are invalid):
  * an fp16 copy of v [T_k, H_kv, 64] for the tensor cores.  Same conventions as
  * attn_sink_bwd_workspace_size (packed fields when num_seqs > 0).  A workspace

@@ -23,7 +23,7 @@ def test_exports_every_declared_symbol():
     assert set(names) == {"attn_sink_fwd", "attn_sink_bwd", "attn_sink_bwd_workspace_size",
                           "attn_sink_fwd_workspace_size", "attn_sink_fwd_noalloc",
                           "attn_sink_last_cuda_error", "attn_sink_kernel_timing",
-                          "attn_sink_kernel_time",
+                          "attn_sink_kernel_time", "attn_sink_fwd_chunk", "attn_sink_merge",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -160,6 +160,46 @@ def test_kernel_time_without_launches():
     assert binding.attn_sink_kernel_time(2)[0] == INVALID
     assert binding.attn_sink_kernel_time(-1)[0] == INVALID
     assert binding.lib().attn_sink_kernel_time(0, None, None) == INVALID
+
+
+def _chunk(p, q_pos0=0, q=FAKE, k=FAKE, v=FAKE, out=FAKE, res=None, lse=FAKE, ws=FAKE,
+           ws_bytes=1 << 40):
+    return binding.attn_sink_fwd_chunk(p, q_pos0, q, k, v, None, None, out, res, lse, ws,
+                                       ws_bytes, stream=0)
+
+
+def _merge(c=2, t=16, h=4, d=64, o=FAKE, r=None, ls=FAKE, sink=FAKE, out=FAKE, res=None,
+           lse=FAKE):
+    return binding.attn_sink_merge(c, t, h, d, o, r, ls, sink, out, res, lse, stream=0)
+
+
+def test_chunk_forward_rejects_bad_arguments_on_host():
+    n0 = binding.attn_sink_launch_count()
+    p = _dense()
+    assert _chunk(p, q_pos0=(1 << 30) + 1) == INVALID
+    assert _chunk(p, q_pos0=-(1 << 30) - 1) == INVALID
+    assert _chunk(p, q=None) == INVALID
+    assert _chunk(p, lse=None) == INVALID
+    assert _chunk(p, out=FAKE_ODD) == INVALID
+    assert _chunk(p, ws=None) == 3
+    assert _chunk(_dense(head_dim=32)) == UNSUPPORTED
+    assert binding.attn_sink_fwd_chunk(None, 0, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE,
+                                       FAKE, 1 << 40, stream=0) == INVALID
+    assert _chunk(_dense(batch=0)) == OK        # nothing to compute
+    assert binding.attn_sink_launch_count() == n0
+
+
+def test_merge_rejects_bad_arguments_on_host():
+    n0 = binding.attn_sink_launch_count()
+    assert _merge(c=0) == INVALID
+    assert _merge(h=0) == INVALID
+    assert _merge(t=-1) == INVALID
+    assert _merge(d=32) == UNSUPPORTED
+    assert _merge(t=0) == OK                    # no rows: a no-op
+    for kw in (dict(o=None), dict(ls=None), dict(sink=None), dict(out=None), dict(lse=None),
+               dict(o=FAKE_ODD), dict(r=FAKE_ODD), dict(out=FAKE_ODD), dict(res=FAKE_ODD)):
+        assert _merge(**kw) == INVALID, kw
+    assert binding.attn_sink_launch_count() == n0
 
 
 def test_forward_workspace_checked_on_host():
