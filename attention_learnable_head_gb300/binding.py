@@ -5,7 +5,7 @@
 ``attn_sink_status_string``, ``attn_sink_device_error``,
 ``attn_sink_launch_count``, ``attn_sink_last_cuda_error``,
 ``attn_sink_kernel_timing``, ``attn_sink_kernel_time``, ``attn_sink_fwd_chunk``,
-``attn_sink_merge`` and ``attn_sink_fwd_noalloc`` mirror the C entry
+``attn_sink_merge``, ``attn_sink_bwd_deterministic`` and ``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -95,6 +95,8 @@ def lib():
                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     L.attn_sink_bwd.restype = c_int
+    L.attn_sink_bwd_deterministic.argtypes = L.attn_sink_bwd.argtypes
+    L.attn_sink_bwd_deterministic.restype = c_int
     L.attn_sink_status_string.argtypes = [c_int]
     L.attn_sink_status_string.restype = ctypes.c_char_p
     L.attn_sink_device_error.argtypes = [c_void_p, ctypes.POINTER(c_int)]
@@ -185,6 +187,16 @@ def attn_sink_bwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlen
                   out_residual, lse, dout, dq, dk, dv, dsink, workspace, workspace_bytes: int,
                   stream=None) -> int:
     return lib().attn_sink_bwd(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                               _ptr(out_residual), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(dsink), _ptr(workspace), int(workspace_bytes),
+                               _stream(stream))
+
+
+def attn_sink_bwd_deterministic(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out,
+                  out_residual, lse, dout, dq, dk, dv, dsink, workspace, workspace_bytes: int,
+                  stream=None) -> int:
+    return lib().attn_sink_bwd_deterministic(_pref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(sink),
                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
                                _ptr(out_residual), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                _ptr(dv), _ptr(dsink), _ptr(workspace), int(workspace_bytes),
@@ -317,8 +329,9 @@ def backward(q, k, v, sink, out, lse, dout, *, out_residual=None, causal: bool =
              window: int = 0, softmax_scale: float | None = None, cu_seqlens_q=None,
              cu_seqlens_k=None, max_seqlen_q: int | None = None,
              max_seqlen_k: int | None = None, grad_dtype: int = 0, workspace=None,
-             stream=None):
-    """dq, dk, dv (bf16, or fp32 when grad_dtype = 1) and dsink ([H_q] fp32)."""
+             deterministic: bool = False, stream=None):
+    """dq, dk, dv (bf16, or fp32 when grad_dtype = 1) and dsink ([H_q] fp32).
+    deterministic=True: bitwise reproducible (attn_sink_bwd_deterministic)."""
     num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
                     num_seqs=num_seqs, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
@@ -331,9 +344,9 @@ def backward(q, k, v, sink, out, lse, dout, *, out_residual=None, causal: bool =
     nbytes = attn_sink_bwd_workspace_size(p)
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
-    _check(attn_sink_bwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
-                         dout, dq, dk, dv, dsink, workspace, workspace.numel(), stream),
-           "attn_sink_bwd")
+    fn = attn_sink_bwd_deterministic if deterministic else attn_sink_bwd
+    _check(fn(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+              dout, dq, dk, dv, dsink, workspace, workspace.numel(), stream), fn.__name__)
     return dq, dk, dv, dsink
 
 

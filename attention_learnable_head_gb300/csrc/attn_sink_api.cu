@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "attn_sink.h"
+#include "bwd_dq_kernel.cuh"
 #include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "merge_kernel.cuh"
@@ -136,6 +137,8 @@ int device_state(int* sm_count, int** err) {
   if (!g_attr_set[dev]) {
     if (cudaFuncSetAttribute(attn_sink_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kFwdSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_sink_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kDqSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(attn_sink_bwd_main_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kBwdSmemBytes) != cudaSuccess)
@@ -468,11 +471,17 @@ size_t attn_sink_bwd_workspace_size(const attn_sink_params* params) {
   return bwd_layout(params, g, sm_count_or_default()).total;
 }
 
-int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
-                  const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                  const void* out, const void* out_residual, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, float* dsink,
-                  void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward; `deterministic` computes dQ with the query-stationary kernel
+// (fixed summation order) instead of reduce-adds from the main kernel.
+int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const void* v,
+             const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
+             const void* out, const void* out_residual, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, float* dsink, void* workspace,
+             size_t workspace_bytes, void* stream, bool deterministic) {
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -518,7 +527,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     pp.sink = sink;
     pp.LD = LD;
     pp.partials = partials;
-    pp.dq_acc = dq_acc;
+    pp.dq_acc = deterministic ? nullptr : dq_acc;
     pp.total_q = g.total_q;
     pp.heads_q = params->heads_q;
     pp.n_blocks = L.n_blocks;
@@ -578,6 +587,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
     bp.scale_log2 = scale * kLog2e;
     bp.n_ktiles = n_ktiles;
     bp.grad_fp32 = params->grad_dtype;
+    bp.skip_dq = deterministic ? 1 : 0;
     dim3 grid(params->heads_kv * L.split, g.num_seqs, n_ktiles);
     const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_BWD_MAIN, s);
     attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
@@ -592,8 +602,46 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
       if (!launched()) return ATTN_SINK_ERR_CUDA;
     }
   }
-  // 3. dq (bf16) from the fp32 accumulator
-  if (g.total_q > 0 && params->grad_dtype == 0) {
+  // 3. deterministic dQ, written directly in the requested dtype
+  if (deterministic && g.total_q > 0 && g.num_seqs > 0) {
+    const int n_qtiles = (g.max_q + kBlockM - 1) / kBlockM;
+    DqParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // An empty key tensor is never read (every tile has no key); its maps only
+    // need a valid address.
+    const void* kp = g.total_k > 0 ? (const void*)k16 : (const void*)q16;
+    const void* vp = g.total_k > 0 ? (const void*)v16 : (const void*)q16;
+    const int tk = g.total_k > 0 ? g.total_k : 1;
+    const int hk = g.total_k > 0 ? params->heads_kv : 1;
+    if ((st = encode_rows(&dp.tm_q, q16, g.total_q, params->heads_q, f16)) != ATTN_SINK_OK)
+      return st;
+    if ((st = encode_rows(&dp.tm_do, do16, g.total_q, params->heads_q, f16)) != ATTN_SINK_OK)
+      return st;
+    if ((st = encode_rows(&dp.tm_k, kp, tk, hk, f16)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&dp.tm_v, vp, tk, hk, f16)) != ATTN_SINK_OK) return st;
+    dp.cu_q = cu_seqlens_q;
+    dp.cu_k = cu_seqlens_k;
+    dp.LD = LD;
+    dp.dq = dq;
+    dp.err = err;
+    dp.seqlen_q = g.varlen ? 0 : params->seqlen_q;
+    dp.seqlen_k = g.varlen ? 0 : params->seqlen_k;
+    dp.total_q = g.total_q;
+    dp.heads_q = params->heads_q;
+    dp.group = g.group;
+    dp.causal = params->causal;
+    dp.window = params->window > 0 ? params->window : 0;
+    dp.scale = scale;
+    dp.scale_log2 = scale * kLog2e;
+    dp.n_qtiles = n_qtiles;
+    dp.grad_fp32 = params->grad_dtype;
+    attn_sink_bwd_dq_kernel<<<dim3(params->heads_q, g.num_seqs, n_qtiles), kDqThreads,
+                              kDqSmemBytes, s>>>(dp);
+    if (!launched()) return ATTN_SINK_ERR_CUDA;
+  }
+  // 3'. dq (bf16) from the fp32 accumulator
+  if (!deterministic && g.total_q > 0 && params->grad_dtype == 0) {
     const size_t n8 = (size_t)g.total_q * params->heads_q * kHeadDim / 8;
     const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)sms * 8);
     attn_sink_dq_convert_kernel<<<blocks, 256, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
@@ -608,6 +656,29 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
   if (cudaMemsetAsync(dsink, 0, sizeof(float) * params->heads_q, s) != cudaSuccess)
     return ATTN_SINK_ERR_CUDA;
   return ATTN_SINK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, const void* v,
+                  const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  const void* out, const void* out_residual, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, float* dsink,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream, false);
+}
+
+int attn_sink_bwd_deterministic(const attn_sink_params* params, const void* q, const void* k,
+                                const void* v, const float* sink, const int* cu_seqlens_q,
+                                const int* cu_seqlens_k, const void* out,
+                                const void* out_residual, const float* lse, const void* dout,
+                                void* dq, void* dk, void* dv, float* dsink, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return bwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream, true);
 }
 
 // Caller entry point that allocates nothing: the workspace of attn_sink_fwd is

@@ -1,0 +1,311 @@
+// Deterministic dQ of attention with a per-head sink, sm_103a (tcgen05 + TMA).
+//
+// The main backward adds each key tile's dQ contribution into one fp32
+// accumulator in whatever order the hardware completes the reduce-adds, so dQ
+// is not bitwise reproducible.  This kernel computes dQ query-stationary
+// instead, with a fixed summation order over the key tiles:
+//   S  = Q K^T,  P = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
+//   dP = dO V^T, dS = P o (dP - D)
+//   dQ = scale * sum_j dS_j K_j          (key tiles in increasing order)
+// (the explicit backward of the concat-sink softmax; the sink adds no key row,
+// so it enters dQ only through lse and D).  It costs two more products than
+// the fused backward (S and dP are computed again): the price of
+// reproducibility.
+//
+// One CTA per (query head h, sequence, 128-row query tile), longest first.
+// Warps 0-7 (thread = query row = TMEM lane; warps 4c..4c+3 take the key half
+// c, columns [64c, 64c+64) of a key tile) form dS from S and dP and write it
+// (fp16) over the S columns they have read; warp 8 issues TMA (Q, dO once; K/V
+// through a ring); warp 9 issues the MMAs: S and dP (M=N=128, fp16 from SMEM),
+// then dQ += dS K (M=128, N=64, K=128: dS from TMEM, K read MN-major).
+// TMEM: S 0-127, dP 128-255, dQ 256-319.
+#pragma once
+#include <cuda_bf16.h>
+#include "fwd_kernel.cuh"
+
+namespace attn_sink {
+
+constexpr int kDqThreads = 320;
+constexpr int kDqTmaWarp = 8;
+constexpr int kDqMmaWarp = 9;
+constexpr int kDqStages = 3;
+// Q, dO, kDqStages x (K, V)
+constexpr int kDqSmemBytes = 1024 + (int)kTileBytes * (2 + 2 * kDqStages);
+constexpr uint32_t kDqColS = 0, kDqColDP = 128, kDqColDQ = 256;
+
+struct DqParams {
+  CUtensorMap tm_q;    // [T_q][H_q][64] fp16 copy of q
+  CUtensorMap tm_do;   // [T_q][H_q][64] fp16 copy of dout
+  CUtensorMap tm_k;    // [T_k][H_kv][64] fp16 copy of k
+  CUtensorMap tm_v;    // fp16 copy of v
+  const int* cu_q;
+  const int* cu_k;
+  const float2* LD;    // [H_q][T_q]: (lse * log2 e, D)
+  void* dq;            // [T_q][H_q][64] bf16 (grad_fp32 = 0) or fp32
+  int* err;
+  int seqlen_q, seqlen_k;
+  int total_q;
+  int heads_q, group;
+  int causal, window;
+  float scale;         // softmax_scale
+  float scale_log2;    // softmax_scale * log2(e)
+  int n_qtiles;        // 128-row query tiles of the longest sequence
+  int grad_fp32;
+};
+
+// dS of 32 keys of one query row (thread = row), fp16-packed.
+template <bool kMask>
+__device__ __forceinline__ void dq_ds_chunk(const uint32_t* sr, const uint32_t* dr, float sl2,
+                                            float lse2, float d, int j_first, int jmin,
+                                            int jmax, uint32_t* dk) {
+  #pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float dv[2];
+    #pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -lse2));
+      if (kMask) {
+        const int j = j_first + e + u;
+        if (j < jmin || j > jmax) pe = 0.0f;
+      }
+      dv[u] = pe * (__uint_as_float(dr[e + u]) - d);
+    }
+    dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
+  }
+}
+
+__global__ void __launch_bounds__(kDqThreads, 1)
+attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t q_full, s_full, p_full, dq_done;
+  __shared__ __align__(8) uint64_t kv_full[kDqStages], kv_empty[kDqStages];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int h = blockIdx.x;
+  const int seq = blockIdx.y;
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.z;        // longest work first
+  const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
+  const int i0 = qt * kBlockM;
+  if (i0 >= sp.nq) return;                                // uniform per CTA
+  const int g = h / p.group;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int off = sp.nk - sp.nq;                          // bottom-right alignment
+  const KeyRange kr = key_tiles(i0, min(i0 + kBlockM, sp.nq) - 1, sp, off, p.causal, p.window);
+  const int num = kr.num;
+
+  if (num == 0) {
+    // No row of this tile sees a key: dQ = 0.
+    for (int t = tid; t < kBlockM * 8; t += kDqThreads) {
+      const int rr = t >> 3, c8 = t & 7;
+      if (i0 + rr < sp.nq) {
+        const size_t base = ((size_t)(sp.q0 + i0 + rr) * p.heads_q + h) * kHeadDim + 8 * c8;
+        if (p.grad_fp32) {
+          float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.dq) + base);
+          d4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          d4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + base) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    return;
+  }
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = sQ + kTileBytes;
+  uint8_t* sK = sdO + kTileBytes;                         // kDqStages tiles
+  uint8_t* sV = sK + kDqStages * kTileBytes;              // kDqStages tiles
+
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&q_full, 1);
+    mbar_init(&s_full, 1);
+    mbar_init(&p_full, 2 * kBlockM);
+    mbar_init(&dq_done, 1);
+    for (int s = 0; s < kDqStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == kDqMmaWarp) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == kDqTmaWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(&q_full, 2 * kTileBytes);
+      tma_load_3d(&p.tm_q, &q_full, sQ, 0, h, sp.q0 + i0);
+      tma_load_3d(&p.tm_do, &q_full, sdO, 0, h, sp.q0 + i0);
+      int issued = 0;
+      for (int it = 0; it < num; ++it) {
+        const int st = it % kDqStages;
+        if (it >= kDqStages &&
+            !mbar_wait(&kv_empty[st], ((it / kDqStages) & 1) ^ 1, &abort_flag)) {
+          abort_flag = 1;
+          atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 5);
+          break;
+        }
+        const int row = sp.k0 + (kr.lo + it) * kBlockN;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
+        tma_load_3d(&p.tm_k, &kv_full[st], sK + st * kTileBytes, 0, g, row);
+        tma_load_3d(&p.tm_v, &kv_full[st], sV + st * kTileBytes, 0, g, row);
+        issued = it + 1;
+      }
+      if (abort_flag) {
+        // Let the copies already in flight land before the CTA releases SMEM.
+        mbar_wait(&q_full, 0, nullptr);
+        for (int it = max(0, issued - kDqStages); it < issued; ++it)
+          mbar_wait(&kv_full[it % kDqStages], (it / kDqStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == kDqMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    // S(n+1) and dP(n+1) are issued right after dQ(n): the same thread issues
+    // them and tcgen05 MMAs execute in issue order, so dQ(n) has read dS(n)
+    // (over the S columns) before S(n+1) overwrites it; dP(n) was read by the
+    // compute warps before they arrived on p_full(n).
+    if (lane == 0) {
+      const uint32_t id_s = make_idesc(kFmtF16, kBlockM, kBlockN, false, false);
+      const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
+      const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dO0 = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
+      const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);       // K-major
+      const uint64_t dKmn = make_sdesc_sw128(smem_u32(sK), 16384, 1024);   // MN-major
+      const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16, 1024);
+      constexpr uint32_t kTileU = kTileBytes >> 4;
+      auto issue_s = [&](int n) -> bool {
+        const int st = n % kDqStages;
+        if (!mbar_wait(&kv_full[st], (n / kDqStages) & 1, &abort_flag)) return false;
+        tc_fence_after();
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_ss(tmem + kDqColS, dQ0 + 2 * k, dK0 + st * kTileU + 2 * k, id_s, k > 0);
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_ss(tmem + kDqColDP, dO0 + 2 * k, dV0 + st * kTileU + 2 * k, id_s, k > 0);
+        mma_commit(&s_full);
+        return true;
+      };
+      bool ok = mbar_wait(&q_full, 0, &abort_flag) && issue_s(0);
+      for (int n = 0; ok && n < num; ++n) {
+        const int st = n % kDqStages;
+        if (!mbar_wait(&p_full, n & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // dQ += dS K: k-step kk covers keys [16 kk, 16 kk + 16) of the tile; the
+        // key half c = kk / 4 wrote its dS over S columns [64 c, 64 c + 32).
+        #pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts(tmem + kDqColDQ, tmem + kDqColS + 64 * (kk >> 2) + 8 * (kk & 3),
+                 dKmn + st * kTileU + 128 * kk, id_dq, (n > 0 || kk > 0));
+        mma_commit(&kv_empty[st]);
+        if (n + 1 < num) ok = issue_s(n + 1);
+      }
+      if (!ok) {
+        abort_flag = 1;
+        atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 6);
+      }
+      // every MMA has finished before the epilogue reads dQ and TMEM is released
+      mma_commit(&dq_done);
+      mbar_wait(&dq_done, 0, nullptr);
+    }
+  } else {
+    // ---------------------------------------------------------------- compute warps
+    const int c = warp >> 2;                      // key half
+    const int r = tid & 127;                      // query row in tile = TMEM lane
+    const int i = i0 + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = p.scale_log2;
+    // this row's (lse log2 e, D); rows past the sequence read a valid row
+    const float2 ld = __ldg(p.LD + (size_t)h * p.total_q + sp.q0 + min(i, sp.nq - 1));
+    const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
+    const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
+    const int tile_r1 = min(i0 + kBlockM, sp.nq) - 1;
+    bool ok = true;
+    for (int it = 0; it < num; ++it) {
+      if (!mbar_wait_warp(&s_full, it & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const int j0 = (kr.lo + it) * kBlockN + 64 * c;          // first key of this half
+      const bool need_mask = (j0 + 64 > sp.nk) ||
+                             (p.causal && (j0 + 63 > i0 + off ||
+                                           (p.window > 0 && j0 <= tile_r1 + off - p.window)));
+      #pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_x32(tmem + lane_base + kDqColS + 64 * c + cc, sr);
+        tmem_ld_x32(tmem + lane_base + kDqColDP + 64 * c + cc, dr);
+        tmem_ld_wait();
+        uint32_t dk[16];
+        if (need_mask)
+          dq_ds_chunk<true>(sr, dr, sl2, ld.x, ld.y, j0 + cc, jmin, jmax, dk);
+        else
+          dq_ds_chunk<false>(sr, dr, sl2, ld.x, ld.y, j0 + cc, jmin, jmax, dk);
+        // dS over S columns this thread has already read (chunk cc -> cc / 2)
+        tmem_st_x16(tmem + lane_base + kDqColS + 64 * c + (cc >> 1), dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full);
+    }
+    // fin is warp-uniform (every wait above is), so the whole warp reaches the
+    // .sync.aligned TMEM load; only the stores depend on the row.
+    bool fin = ok && mbar_wait_warp(&dq_done, 0, &abort_flag);
+    if (!fin) {
+      abort_flag = 1;
+      atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 7);
+    } else {
+      // dQ columns [32 c, 32 c + 32) of this row, times the softmax scale
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld_x32(tmem + lane_base + kDqColDQ + 32 * c, v);
+      tmem_ld_wait();
+      if (i < sp.nq) {
+        const size_t base = ((size_t)(sp.q0 + i) * p.heads_q + h) * kHeadDim + 32 * c;
+        if (p.grad_fp32) {
+          float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(p.dq) + base);
+          #pragma unroll
+          for (int u = 0; u < 8; ++u)
+            d4[u] = make_float4(__uint_as_float(v[4 * u]) * p.scale,
+                                __uint_as_float(v[4 * u + 1]) * p.scale,
+                                __uint_as_float(v[4 * u + 2]) * p.scale,
+                                __uint_as_float(v[4 * u + 3]) * p.scale);
+        } else {
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + base);
+          #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+            #pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[8 * u + 2 * e]) * p.scale,
+                                 __uint_as_float(v[8 * u + 2 * e + 1]) * p.scale);
+            d4[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kDqMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace attn_sink

@@ -62,7 +62,7 @@ struct BwdParams {
   const int* cu_q;
   const int* cu_k;
   const float2* LD;    // [H_q][T_q]: (lse * log2 e, D) per query row
-  float* dq_acc;       // [T_q][H_q][64] fp32, pre-zeroed
+  float* dq_acc;       // [T_q][H_q][64], zeroed unless null fp32, pre-zeroed
   void* dk;            // [T_k][H_kv][64] bf16 or fp32 (split == 1)
   void* dv;
   float* dk_part;      // [split][T_k][H_kv][64] fp32 partials (split > 1)
@@ -77,6 +77,7 @@ struct BwdParams {
   float scale_log2;    // softmax_scale * log2(e)
   int n_ktiles;        // key tiles of the longest sequence
   int grad_fp32;
+  int skip_dq;         // 1: no dQ here (the deterministic dQ kernel computes it)
 };
 
 // ------------------------------------------------------------------ bwd_pre
@@ -129,9 +130,11 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
       *reinterpret_cast<uint4*>(p.do16 + base) =
           make_uint4(bf16x2_to_f16x2(g.x, &overflow), bf16x2_to_f16x2(g.y, &overflow),
                      bf16x2_to_f16x2(g.z, &overflow), bf16x2_to_f16x2(g.w, &overflow));
-      float4* z = reinterpret_cast<float4*>(p.dq_acc + base);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p.dq_acc) {
+        float4* z = reinterpret_cast<float4*>(p.dq_acc + base);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     d += __shfl_xor_sync(0xffffffffu, d, 1);
     d += __shfl_xor_sync(0xffffffffu, d, 2);
@@ -496,13 +499,15 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
             mma_ss(tmem + kColDK, dS_k + so + hh * kTileU + 2 * k, dQ_mn + ho + 128 * k,
                    id_dvdk, (m > 0 || hh > 0 || k > 0));
           if (hh == 1) {
-            if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
-            #pragma unroll
-            for (int k = 0; k < kBlockN / 16; ++k)
-              mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
-            mma_commit(&mma2_done);
+            if (!p.skip_dq) {
+              if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
+              #pragma unroll
+              for (int k = 0; k < kBlockN / 16; ++k)
+                mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
+              mma_commit(&mma2_done);
+            }
             mma_commit(&q_empty[st]);
           }
           if (more) {
@@ -625,7 +630,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const bool leader = (warp == kBwdDqWarp0 && lane == 0);
     const uint32_t stage = smem_u32(sdQ);
     bool ok = true;
-    for (int m = 0; m < num; ++m) {
+    // (with skip_dq there is no dQ here: the loop does not run)
+    for (int m = 0; m < (p.skip_dq ? 0 : num); ++m) {
       const int h = h_first + m / nqt;
       const int i0 = (qt_first + m % nqt) * kBlockM;
       const bool waited = mbar_wait_warp(&mma2_done, m & 1, &abort_flag);

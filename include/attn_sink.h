@@ -234,6 +234,26 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k,
                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
                   float* dsink, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The backward of attn_sink_bwd with bitwise reproducible results: identical
+ * inputs give identical dq, dk, dv and dsink on every call.  attn_sink_bwd
+ * sums each query row's dQ over the key tiles with reduce-adds whose order the
+ * hardware picks; here dQ comes from a separate query-stationary kernel that
+ * recomputes S and dP and sums the key tiles in increasing order (two more
+ * matrix products: about 40 % more arithmetic).  Train/inference consistency
+ * and reproducibility are the pages' central lesson (keryc.com page on GPT-OSS
+ * agentic RL fixes, section "Solutions implemented by the team"; euno.news
+ * page, section "反向传播" for the gradient itself).  Arguments, layouts,
+ * workspace (attn_sink_bwd_workspace_size covers both entry points), precision
+ * and errors as attn_sink_bwd.
+ */
+int attn_sink_bwd_deterministic(const attn_sink_params* params, const void* q, const void* k,
+                                const void* v, const float* sink, const int* cu_seqlens_q,
+                                const int* cu_seqlens_k, const void* out,
+                                const void* out_residual, const float* lse, const void* dout,
+                                void* dq, void* dk, void* dv, float* dsink, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* attn_sink_status_string(int status);
 

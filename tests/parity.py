@@ -59,7 +59,8 @@ def assert_close(name, got, ref, max_abs=TOL_MAX_ABS, rel_fro=TOL_REL_FRO):
 
 
 def run_gpu(case: Case, *, grad_dtype: int = 0, with_bwd: bool = True, dense: bool = False,
-            cu_q=None, cu_k=None, q=None, k=None, v=None, dout=None, residual: bool = True):
+            cu_q=None, cu_k=None, q=None, k=None, v=None, dout=None, residual: bool = True,
+            deterministic: bool = False):
     """Forward (+ backward) of a seeded case on cuda:0 through the C ABI."""
     dev = torch.device("cuda:0")
     w = case.workload
@@ -81,7 +82,8 @@ def run_gpu(case: Case, *, grad_dtype: int = 0, with_bwd: bool = True, dense: bo
         res = dict(out=out.view(q.shape), lse=lse)
         if with_bwd:
             dq, dk, dv, dsink = binding.backward(q4, k4, v4, sink, out, lse, do4,
-                                                 out_residual=ores, grad_dtype=grad_dtype, **kw)
+                                                 out_residual=ores, grad_dtype=grad_dtype,
+                                                 deterministic=deterministic, **kw)
             res.update(dq=dq.view(q.shape), dk=dk.view(k.shape), dv=dv.view(v.shape), dsink=dsink)
     else:
         tq = torch.tensor(cq, dtype=torch.int32, device=dev)
@@ -94,7 +96,8 @@ def run_gpu(case: Case, *, grad_dtype: int = 0, with_bwd: bool = True, dense: bo
         res = dict(out=out, lse=lse)
         if with_bwd:
             dq, dk, dv, dsink = binding.backward(q, k, v, sink, out, lse, do,
-                                                 out_residual=ores, grad_dtype=grad_dtype, **kw)
+                                                 out_residual=ores, grad_dtype=grad_dtype,
+                                                 deterministic=deterministic, **kw)
             res.update(dq=dq, dk=dk, dv=dv, dsink=dsink)
     torch.cuda.synchronize()
     st, code = binding.attn_sink_device_error()

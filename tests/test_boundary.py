@@ -24,6 +24,7 @@ def test_exports_every_declared_symbol():
                           "attn_sink_fwd_workspace_size", "attn_sink_fwd_noalloc",
                           "attn_sink_last_cuda_error", "attn_sink_kernel_timing",
                           "attn_sink_kernel_time", "attn_sink_fwd_chunk", "attn_sink_merge",
+                          "attn_sink_bwd_deterministic",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -63,14 +64,27 @@ def _fwd(p, q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, r
                                  stream=0)
 
 
-def _bwd(p, ws=FAKE, ws_bytes=1 << 40, **kw):
+def _bwd(p, ws=FAKE, ws_bytes=1 << 40, fn=None, **kw):
     args = dict(q=FAKE, k=FAKE, v=FAKE, sink=FAKE, cu_q=None, cu_k=None, out=FAKE, res=None,
                 lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, dsink=FAKE)
     args.update(kw)
-    return binding.attn_sink_bwd(p, args["q"], args["k"], args["v"], args["sink"], args["cu_q"],
-                                 args["cu_k"], args["out"], args["res"], args["lse"],
-                                 args["dout"], args["dq"], args["dk"], args["dv"], args["dsink"],
-                                 ws, ws_bytes, stream=0)
+    fn = binding.attn_sink_bwd if fn is None else fn
+    return fn(p, args["q"], args["k"], args["v"], args["sink"], args["cu_q"], args["cu_k"],
+              args["out"], args["res"], args["lse"], args["dout"], args["dq"], args["dk"],
+              args["dv"], args["dsink"], ws, ws_bytes, stream=0)
+
+
+def test_deterministic_backward_rejects_like_the_backward():
+    det = binding.attn_sink_bwd_deterministic
+    n0 = binding.attn_sink_launch_count()
+    p = _dense()
+    for kw in (dict(dsink=None), dict(dq=None), dict(dk=FAKE_ODD), dict(res=FAKE + 2),
+               dict(sink=None)):
+        assert _bwd(p, fn=det, **kw) == INVALID, kw
+    assert _bwd(None, fn=det) == INVALID
+    assert _bwd(_dense(head_dim=32), fn=det) == UNSUPPORTED
+    assert _bwd(_dense(window=4, causal=0), fn=det) == INVALID
+    assert binding.attn_sink_launch_count() == n0
 
 
 @pytest.mark.parametrize("field,value,status", [
