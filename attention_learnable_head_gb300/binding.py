@@ -5,7 +5,8 @@
 ``attn_sink_status_string``, ``attn_sink_device_error``,
 ``attn_sink_launch_count``, ``attn_sink_last_cuda_error``,
 ``attn_sink_kernel_timing``, ``attn_sink_kernel_time``, ``attn_sink_fwd_chunk``,
-``attn_sink_merge``, ``attn_sink_bwd_deterministic`` and ``attn_sink_fwd_noalloc`` mirror the C entry
+``attn_sink_merge``, ``attn_sink_bwd_deterministic``, ``attn_sink_decode``,
+``attn_sink_decode_workspace_size`` and ``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -40,6 +41,15 @@ class AttnSinkParams(ctypes.Structure):
         ("heads_q", c_int), ("heads_kv", c_int), ("head_dim", c_int),
         ("causal", c_int), ("window", c_int), ("softmax_scale", c_float),
         ("grad_dtype", c_int),
+    ]
+
+
+class AttnSinkDecodeParams(ctypes.Structure):
+    """Mirror of ``attn_sink_decode_params`` in include/attn_sink.h."""
+    _fields_ = [
+        ("batch", c_int), ("heads_q", c_int), ("heads_kv", c_int), ("head_dim", c_int),
+        ("page_size", c_int), ("num_pages", c_int), ("max_pages", c_int), ("window", c_int),
+        ("softmax_scale", c_float),
     ]
 
 
@@ -89,6 +99,13 @@ def lib():
     L.attn_sink_merge.argtypes = [c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     L.attn_sink_merge.restype = c_int
+    PD = ctypes.POINTER(AttnSinkDecodeParams)
+    L.attn_sink_decode_workspace_size.argtypes = [PD]
+    L.attn_sink_decode_workspace_size.restype = c_size_t
+    L.attn_sink_decode.argtypes = [PD, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                   c_void_p]
+    L.attn_sink_decode.restype = c_int
     L.attn_sink_bwd_workspace_size.argtypes = [P]
     L.attn_sink_bwd_workspace_size.restype = c_size_t
     L.attn_sink_bwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -159,6 +176,52 @@ def attn_sink_merge(num_chunks: int, total_q: int, heads_q: int, head_dim: int, 
                                  _ptr(o_parts), _ptr(o_residual_parts), _ptr(lse_parts),
                                  _ptr(sink), _ptr(out), _ptr(out_residual), _ptr(lse),
                                  _stream(stream))
+
+
+def attn_sink_decode_workspace_size(params: AttnSinkDecodeParams) -> int:
+    return int(lib().attn_sink_decode_workspace_size(
+        None if params is None else ctypes.byref(params)))
+
+
+def attn_sink_decode(params: AttnSinkDecodeParams, q, k_cache, v_cache, block_table, seq_lens,
+                     sink, out, out_residual, lse, workspace, workspace_bytes: int,
+                     stream=None) -> int:
+    return lib().attn_sink_decode(None if params is None else ctypes.byref(params), _ptr(q),
+                                  _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                  _ptr(seq_lens), _ptr(sink), _ptr(out), _ptr(out_residual),
+                                  _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream))
+
+
+def make_decode_params(q_shape, cache_shape, max_pages: int, *, window: int = 0,
+                       softmax_scale: float | None = None) -> AttnSinkDecodeParams:
+    """Params from q [B, H_q, d] and a cache [num_pages, page_size, H_kv, d]."""
+    p = AttnSinkDecodeParams()
+    p.batch, p.heads_q, p.head_dim = int(q_shape[0]), int(q_shape[1]), int(q_shape[2])
+    p.num_pages, p.page_size, p.heads_kv = (int(cache_shape[0]), int(cache_shape[1]),
+                                            int(cache_shape[2]))
+    p.max_pages = int(max_pages)
+    p.window = int(window)
+    p.softmax_scale = float(softmax_scale if softmax_scale is not None
+                            else 1.0 / math.sqrt(p.head_dim))
+    return p
+
+
+def decode(q, k_cache, v_cache, block_table, seq_lens, sink, *, window: int = 0,
+           softmax_scale: float | None = None, residual: bool = False, stream=None):
+    """(out, lse, out_residual) of one decode step over a paged cache
+    (attn_sink_decode): q [B, H_q, 64], caches [pages, page_size, H_kv, 64],
+    block_table [B, max_pages] int32, seq_lens [B] int32."""
+    p = make_decode_params(q.shape, k_cache.shape, block_table.shape[1], window=window,
+                           softmax_scale=softmax_scale)
+    out = torch.empty_like(q)
+    res = torch.empty_like(q) if residual else None
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    nbytes = attn_sink_decode_workspace_size(p)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(attn_sink_decode(p, q, k_cache, v_cache, block_table, seq_lens, sink, out, res, lse,
+                            ws, ws.numel(), stream), "attn_sink_decode")
+    return out, lse, res
 
 
 # Bytes of the static scratch behind attn_sink_fwd_noalloc (the header's

@@ -13,6 +13,7 @@
 #include "attn_sink.h"
 #include "bwd_dq_kernel.cuh"
 #include "bwd_kernel.cuh"
+#include "decode_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "merge_kernel.cuh"
 
@@ -446,6 +447,108 @@ int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, cons
   const int blocks = (int)std::min<size_t>((pairs + 31) / 32, (size_t)sms * 8);
   attn_sink_merge_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(mp);
   return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct DecodeLayout {
+  int splits;
+  size_t off_lo, off_lse, total;
+};
+
+// Key splits: enough (batch x kv head x split) CTAs to fill the GPU twice,
+// each split at least 256 keys of the longest possible sequence, at most 64.
+bool decode_layout(const attn_sink_decode_params* p, int sm_count, DecodeLayout* L) {
+  if (p == nullptr || p->batch < 0 || p->heads_kv < 1 || p->heads_q < 1 ||
+      p->heads_q % p->heads_kv != 0 || p->heads_q / p->heads_kv > kDecMaxGroup ||
+      p->page_size < 1 || p->num_pages < 0 || p->max_pages < 0 ||
+      !(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale))
+    return false;
+  const long long cap = (long long)p->max_pages * p->page_size;
+  if (cap > (1ll << 30)) return false;
+  const long long ctas = (long long)p->batch * p->heads_kv;
+  const long long keys = (p->window > 0) ? std::min<long long>(cap, p->window) : cap;
+  long long s = 1;
+  if (ctas > 0) s = std::max<long long>(1, (2ll * sm_count + ctas - 1) / ctas);
+  s = std::min<long long>(s, std::max<long long>(1, (keys + 255) / 256));
+  s = std::min<long long>(s, 64);
+  L->splits = (int)s;
+  const size_t o = (size_t)s * p->batch * p->heads_q * 64 * 2;   // bf16
+  L->off_lo = align256(o);
+  L->off_lse = L->off_lo + align256(o);
+  L->total = L->off_lse + align256((size_t)s * p->heads_q * p->batch * sizeof(float));
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_sink_decode_workspace_size(const attn_sink_decode_params* params) {
+  DecodeLayout L;
+  if (params == nullptr || params->head_dim != kHeadDim || params->batch == 0 ||
+      !decode_layout(params, sm_count_or_default(), &L))
+    return 0;
+  return L.total;
+}
+
+int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const void* k_cache,
+                     const void* v_cache, const int* block_table, const int* seq_lens,
+                     const float* sink, void* out, void* out_residual, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (params == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
+  if (params->head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
+  DecodeLayout L;
+  if (!decode_layout(params, sm_count_or_default(), &L)) {
+    if (params->heads_kv >= 1 && params->heads_q % params->heads_kv == 0 &&
+        params->heads_q / params->heads_kv > kDecMaxGroup)
+      return ATTN_SINK_ERR_UNSUPPORTED;
+    return ATTN_SINK_ERR_INVALID_ARG;
+  }
+  if (params->batch == 0) return ATTN_SINK_OK;
+  if (q == nullptr || sink == nullptr || out == nullptr || lse == nullptr ||
+      seq_lens == nullptr || (params->max_pages > 0 && block_table == nullptr) ||
+      (params->num_pages > 0 && (k_cache == nullptr || v_cache == nullptr)))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(out_residual))
+    return ATTN_SINK_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < L.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return ATTN_SINK_ERR_WORKSPACE;
+  int sms = 0;
+  int* err = nullptr;
+  int st;
+  if ((st = device_state(&sms, &err)) != ATTN_SINK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams dp;
+  dp.q = static_cast<const __nv_bfloat16*>(q);
+  dp.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  dp.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  dp.block_table = block_table;
+  dp.seq_lens = seq_lens;
+  dp.o_part = reinterpret_cast<__nv_bfloat16*>(ws);
+  dp.o_part_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.off_lo);
+  dp.lse_part = reinterpret_cast<float*>(ws + L.off_lse);
+  dp.err = err;
+  dp.batch = params->batch;
+  dp.heads_q = params->heads_q;
+  dp.heads_kv = params->heads_kv;
+  dp.group = params->heads_q / params->heads_kv;
+  dp.page_size = params->page_size;
+  dp.num_pages = params->num_pages;
+  dp.max_pages = params->max_pages;
+  dp.window = params->window > 0 ? params->window : 0;
+  dp.splits = L.splits;
+  dp.scale_log2 = params->softmax_scale * kLog2e;
+  attn_sink_decode_kernel<<<dim3(L.splits, params->heads_kv, params->batch), kDecThreads, 0,
+                            s>>>(dp);
+  if (!launched()) return ATTN_SINK_ERR_CUDA;
+  return attn_sink_merge(L.splits, params->batch, params->heads_q, kHeadDim, dp.o_part,
+                         dp.o_part_lo, dp.lse_part, sink, out, out_residual, lse, stream);
 }
 
 size_t attn_sink_fwd_workspace_size(const attn_sink_params* params) {

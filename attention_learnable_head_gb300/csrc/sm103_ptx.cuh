@@ -28,6 +28,7 @@ enum : int {
   DEVERR_TIMEOUT_FWD = 0x100,
   DEVERR_TIMEOUT_BWD = 0x200,
   DEVERR_FP16_RANGE = 0x400,   // an input lies outside the fp16 range of the MMA operands
+  DEVERR_DECODE_INPUT = 0x800, // decode: a block-table entry or sequence length out of range
 };
 
 // Give up on an mbarrier after this many nanoseconds.  Every legitimate wait

@@ -163,6 +163,51 @@ int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, cons
                     void* out, void* out_residual, float* lse, void* stream);
 
 /*
+ * Decode step over a paged key/value cache (one new query token per sequence):
+ * the rollout-side forward with the same sink semantics as attn_sink_fwd, so
+ * that inference and training compute the same log-probabilities (ai-engineering-
+ * academy page, sections "Desafio 2: Inconsistência Treino-Inferência" and
+ * "Desafio 3: Attention Sinks no FlashAttention"; the concat listing
+ * "带汇聚的注意力（GPT-OSS）" of the euno.news page with one query row).
+ */
+typedef struct attn_sink_decode_params {
+  int batch;          /* B >= 0 sequences */
+  int heads_q;        /* H_q, a multiple of heads_kv with H_q / H_kv <= 8 */
+  int heads_kv;       /* H_kv >= 1 */
+  int head_dim;       /* must be 64 */
+  int page_size;      /* keys per cache page, >= 1 */
+  int num_pages;      /* pages in the cache pool */
+  int max_pages;      /* columns of block_table (pages per sequence at most) */
+  int window;         /* <= 0: every cached key; W > 0: the last W keys */
+  float softmax_scale;/* multiplies q.k only; finite and > 0 */
+} attn_sink_decode_params;
+
+/*
+ * Bytes of device workspace attn_sink_decode needs (0 if the params are
+ * invalid or batch = 0): the key-split partial results.
+ */
+size_t attn_sink_decode_workspace_size(const attn_sink_decode_params* params);
+
+/*
+ * q [B, H_q, 64] bf16 (the new token of each sequence); k_cache, v_cache
+ * [num_pages, page_size, H_kv, 64] bf16; block_table [B, max_pages] int32 (the
+ * page of keys [p * page_size, (p + 1) * page_size) of sequence b);
+ * seq_lens [B] int32, the cached keys of each sequence including the new
+ * token's own (appended before the call); sink [H_q] fp32.  Writes out
+ * [B, H_q, 64] bf16, optional out_residual (as attn_sink_fwd) and lse [H_q, B]
+ * fp32; a sequence with no cached key gets out = 0, lse = sink.  The scores,
+ * softmax and P v run in fp32 (no fp16 rounding of P).  Block-table entries
+ * and lengths are checked on the device (see attn_sink_device_error).  All
+ * pointers are device pointers, 16-byte aligned where they hold bf16 rows;
+ * the workspace is 256-byte aligned and at least
+ * attn_sink_decode_workspace_size bytes.  Returns an attn_sink_status.
+ */
+int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const void* k_cache,
+                     const void* v_cache, const int* block_table, const int* seq_lens,
+                     const float* sink, void* out, void* out_residual, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace attn_sink_fwd needs (0 if the params are invalid):
  * an fp16 copy of v [T_k, H_kv, 64] for the tensor cores.  Same conventions as
  * attn_sink_bwd_workspace_size (packed fields when num_seqs > 0).  A workspace
@@ -261,7 +306,10 @@ const char* attn_sink_status_string(int status);
  * Synchronises `stream`, then reads and clears the device error word.  *code
  * receives 0 when nothing was recorded, 0x1xx / 0x2xx when a forward / backward
  * kernel gave up on a bounded wait, 0x400 when an input was outside the fp16
- * range of the tensor-core operands.  Returns ATTN_SINK_OK, or ATTN_SINK_ERR_CUDA when the
+ * range of the tensor-core operands, 0x800 when attn_sink_decode met a
+ * block-table entry outside [0, num_pages) or a sequence length outside
+ * [0, max_pages * page_size] (that key is skipped; the length is clamped).
+ * Returns ATTN_SINK_OK, or ATTN_SINK_ERR_CUDA when the
  * synchronisation itself failed.
  */
 int attn_sink_device_error(void* stream, int* code);

@@ -24,7 +24,8 @@ def test_exports_every_declared_symbol():
                           "attn_sink_fwd_workspace_size", "attn_sink_fwd_noalloc",
                           "attn_sink_last_cuda_error", "attn_sink_kernel_timing",
                           "attn_sink_kernel_time", "attn_sink_fwd_chunk", "attn_sink_merge",
-                          "attn_sink_bwd_deterministic",
+                          "attn_sink_bwd_deterministic", "attn_sink_decode",
+                          "attn_sink_decode_workspace_size",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -214,6 +215,50 @@ def test_merge_rejects_bad_arguments_on_host():
                dict(o=FAKE_ODD), dict(r=FAKE_ODD), dict(out=FAKE_ODD), dict(res=FAKE_ODD)):
         assert _merge(**kw) == INVALID, kw
     assert binding.attn_sink_launch_count() == n0
+
+
+def _dparams(**kw):
+    p = binding.AttnSinkDecodeParams()
+    p.batch, p.heads_q, p.heads_kv, p.head_dim = 4, 16, 2, 64
+    p.page_size, p.num_pages, p.max_pages, p.window, p.softmax_scale = 16, 64, 8, 0, 0.125
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _decode(p, q=FAKE, kc=FAKE, vc=FAKE, table=FAKE, lens=FAKE, sink=FAKE, out=FAKE, res=None,
+            lse=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    return binding.attn_sink_decode(p, q, kc, vc, table, lens, sink, out, res, lse, ws,
+                                    ws_bytes, stream=0)
+
+
+def test_decode_params_struct_layout():
+    assert ctypes.sizeof(binding.AttnSinkDecodeParams) == 36
+
+
+def test_decode_rejects_bad_arguments_on_host():
+    n0 = binding.attn_sink_launch_count()
+    assert _decode(None) == INVALID
+    assert _decode(_dparams(head_dim=32)) == UNSUPPORTED
+    assert _decode(_dparams(heads_q=32, heads_kv=2)) == UNSUPPORTED     # 16 heads per kv head
+    assert _decode(_dparams(heads_q=15)) == INVALID                     # not a multiple
+    assert _decode(_dparams(page_size=0)) == INVALID
+    assert _decode(_dparams(softmax_scale=0.0)) == INVALID
+    assert _decode(_dparams(softmax_scale=math.inf)) == INVALID
+    assert _decode(_dparams(max_pages=1 << 20, page_size=1 << 12)) == INVALID   # > 2^30 keys
+    assert _decode(_dparams(), q=None) == INVALID
+    assert _decode(_dparams(), table=None) == INVALID
+    assert _decode(_dparams(), lens=None) == INVALID
+    assert _decode(_dparams(), out=FAKE_ODD) == INVALID
+    assert _decode(_dparams(), ws=None) == 3
+    assert _decode(_dparams(), ws_bytes=16) == 3
+    assert _decode(_dparams(), ws=FAKE + 16) == 3
+    assert _decode(_dparams(batch=0)) == OK
+    assert binding.attn_sink_launch_count() == n0
+    assert binding.attn_sink_decode_workspace_size(_dparams()) > 0
+    assert binding.attn_sink_decode_workspace_size(_dparams(batch=0)) == 0
+    assert binding.attn_sink_decode_workspace_size(_dparams(head_dim=32)) == 0
+    assert binding.attn_sink_decode_workspace_size(None) == 0
 
 
 def test_forward_workspace_checked_on_host():
