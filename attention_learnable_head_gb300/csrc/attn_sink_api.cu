@@ -453,6 +453,9 @@ int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, cons
 
 namespace {
 
+// query heads per kv head that the decode kernel is built for
+bool decode_group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
 struct DecodeLayout {
   int splits;
   size_t off_lo, off_lse, total;
@@ -462,7 +465,7 @@ struct DecodeLayout {
 // each split at least 256 keys of the longest possible sequence, at most 64.
 bool decode_layout(const attn_sink_decode_params* p, int sm_count, DecodeLayout* L) {
   if (p == nullptr || p->batch < 0 || p->heads_kv < 1 || p->heads_q < 1 ||
-      p->heads_q % p->heads_kv != 0 || p->heads_q / p->heads_kv > kDecMaxGroup ||
+      p->heads_q % p->heads_kv != 0 || !decode_group_ok(p->heads_q / p->heads_kv) ||
       p->page_size < 1 || p->num_pages < 0 || p->max_pages < 0 ||
       !(p->softmax_scale > 0.0f) || !std::isfinite(p->softmax_scale))
     return false;
@@ -502,8 +505,9 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
   if (params->head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
   DecodeLayout L;
   if (!decode_layout(params, sm_count_or_default(), &L)) {
-    if (params->heads_kv >= 1 && params->heads_q % params->heads_kv == 0 &&
-        params->heads_q / params->heads_kv > kDecMaxGroup)
+    if (params->heads_kv >= 1 && params->heads_q >= 1 &&
+        params->heads_q % params->heads_kv == 0 &&
+        !decode_group_ok(params->heads_q / params->heads_kv))
       return ATTN_SINK_ERR_UNSUPPORTED;
     return ATTN_SINK_ERR_INVALID_ARG;
   }
@@ -537,15 +541,19 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
   dp.batch = params->batch;
   dp.heads_q = params->heads_q;
   dp.heads_kv = params->heads_kv;
-  dp.group = params->heads_q / params->heads_kv;
   dp.page_size = params->page_size;
   dp.num_pages = params->num_pages;
   dp.max_pages = params->max_pages;
   dp.window = params->window > 0 ? params->window : 0;
   dp.splits = L.splits;
   dp.scale_log2 = params->softmax_scale * kLog2e;
-  attn_sink_decode_kernel<<<dim3(L.splits, params->heads_kv, params->batch), kDecThreads, 0,
-                            s>>>(dp);
+  const dim3 grid(L.splits, params->heads_kv, params->batch);
+  switch (params->heads_q / params->heads_kv) {
+    case 1: attn_sink_decode_kernel<1><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 2: attn_sink_decode_kernel<2><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 4: attn_sink_decode_kernel<4><<<grid, kDecThreads, 0, s>>>(dp); break;
+    default: attn_sink_decode_kernel<8><<<grid, kDecThreads, 0, s>>>(dp); break;
+  }
   if (!launched()) return ATTN_SINK_ERR_CUDA;
   return attn_sink_merge(L.splits, params->batch, params->heads_q, kHeadDim, dp.o_part,
                          dp.o_part_lo, dp.lse_part, sink, out, out_residual, lse, stream);

@@ -12,7 +12,7 @@
 // query heads of g to one slice of b's keys, without the sink, and writes the
 // slice's normalised result and log-sum-exp; attn_sink_merge_kernel then adds
 // the sink once (the merge of the key-chunk forward).  The work is a skinny
-// contraction (G <= 8 rows), bound by reading the cache from HBM: it runs on the
+// contraction (G <= 8 rows) meant to be bound by reading the cache: it runs on the
 // CUDA cores in fp32.  Each key is handled by 8 lanes, each holding 8 of the 64
 // dimensions (one 16-byte load of K and of V); the lanes of a key combine the
 // G dot products with three shuffles, and every lane keeps its own online
@@ -28,6 +28,7 @@ constexpr int kDecThreads = 128;
 constexpr int kDecMaxGroup = 8;        // query heads per kv head
 constexpr int kDecStates = kDecThreads / 8;   // key groups of 8 lanes per CTA
 constexpr float kLn2Dec = 0.6931471805599453f;
+constexpr int kDecUnroll = 2;       // keys per key group whose loads are in flight together
 
 struct DecodeParams {
   const __nv_bfloat16* q;         // [B][H_q][64]
@@ -39,17 +40,20 @@ struct DecodeParams {
   __nv_bfloat16* o_part_lo;       // residuals of o_part
   float* lse_part;                // [splits][H_q][B] (natural log), -inf: no key
   int* err;
-  int batch, heads_q, heads_kv, group;
+  int batch, heads_q, heads_kv;
   int page_size, num_pages, max_pages;
   int window;
   int splits;
   float scale_log2;               // softmax_scale * log2(e)
 };
 
+// G = query heads per kv head (1, 2, 4 or 8), a compile-time constant so that
+// the G independent score / softmax chains of a key are interleaved.
+template <int G>
 __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const DecodeParams p) {
-  __shared__ float s_m[kDecStates][kDecMaxGroup];
-  __shared__ float s_l[kDecStates][kDecMaxGroup];
-  __shared__ float s_o[kDecStates][kDecMaxGroup][64];
+  __shared__ float s_m[kDecStates][G];
+  __shared__ float s_l[kDecStates][G];
+  __shared__ float s_o[kDecStates][G][64];
 
   const int split = blockIdx.x;
   const int g = blockIdx.y;
@@ -57,7 +61,6 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
   const int tid = threadIdx.x;
   const int state = tid >> 3;                  // key group of 8 lanes (0..15)
   const int ds = tid & 7;                      // dimension slice: dims [8 ds, 8 ds + 8)
-  const int G = p.group;
 
   // keys [lo, hi) of this sequence, then this split's slice of them
   int L = __ldg(p.seq_lens + b);
@@ -72,26 +75,21 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
   const int k1 = min(L, k0 + per);
 
   // the G query rows of kv head g, dims of this lane, pre-scaled to log2 units
-  float qv[kDecMaxGroup][8];
+  float qv[G][8];
   #pragma unroll
-  for (int h = 0; h < kDecMaxGroup; ++h) {
-    if (h < G) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(
-          p.q + ((size_t)b * p.heads_q + g * G + h) * 64 + 8 * ds));
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-      #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qv[h][2 * e] = bf16_lo(ww[e]) * p.scale_log2;
-        qv[h][2 * e + 1] = bf16_hi(ww[e]) * p.scale_log2;
-      }
-    } else {
-      #pragma unroll
-      for (int e = 0; e < 8; ++e) qv[h][e] = 0.0f;
+  for (int h = 0; h < G; ++h) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+        p.q + ((size_t)b * p.heads_q + g * G + h) * 64 + 8 * ds));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qv[h][2 * e] = bf16_lo(ww[e]) * p.scale_log2;
+      qv[h][2 * e + 1] = bf16_hi(ww[e]) * p.scale_log2;
     }
   }
-  float m[kDecMaxGroup], l[kDecMaxGroup], o[kDecMaxGroup][8];
+  float m[G], l[G], o[G][8];
   #pragma unroll
-  for (int h = 0; h < kDecMaxGroup; ++h) {
+  for (int h = 0; h < G; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.0f;
     #pragma unroll
@@ -99,63 +97,80 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
   }
 
   const size_t row_stride = (size_t)p.heads_kv * 64;     // one key of the cache
-  // The trip count is the same for every lane of the CTA (k0, k1 are), so the
-  // shuffles below always run with the whole warp; a lane whose key is past the
-  // slice, or whose page entry is out of range, contributes nothing.
-  for (int jb = k0; jb < k1; jb += kDecStates) {
-    const int j = jb + state;
-    bool valid = j < k1;
-    uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
-    if (valid) {
-      const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + j / p.page_size);
-      if (pg < 0 || pg >= p.num_pages) {                  // bounds check of the table
-        if (ds == 0) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
-        valid = false;
-      } else {
-        const size_t off =
-            ((size_t)pg * p.page_size + j % p.page_size) * row_stride + g * 64 + 8 * ds;
-        kw = __ldg(reinterpret_cast<const uint4*>(p.k_cache + off));
-        vw = __ldg(reinterpret_cast<const uint4*>(p.v_cache + off));
+  // Each key group takes kDecUnroll keys per step and issues their loads before
+  // using them.  The trip count is the same for every lane of the CTA (k0, k1
+  // are), so the shuffles always run with the whole warp.  The softmax update is
+  // branch-free: a lane whose key is past the slice, or whose page entry is out
+  // of range, uses a score of -inf, which changes neither m, l nor o.
+  for (int jb = k0; jb < k1; jb += kDecUnroll * kDecStates) {
+    uint4 kw[kDecUnroll], vw[kDecUnroll];
+    bool valid[kDecUnroll];
+    #pragma unroll
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int j = jb + u * kDecStates + state;
+      valid[u] = j < k1;
+      kw[u] = make_uint4(0, 0, 0, 0);
+      vw[u] = make_uint4(0, 0, 0, 0);
+      if (valid[u]) {
+        const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + j / p.page_size);
+        if (pg < 0 || pg >= p.num_pages) {                // bounds check of the table
+          if (ds == 0) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
+          valid[u] = false;
+        } else {
+          const size_t off =
+              ((size_t)pg * p.page_size + j % p.page_size) * row_stride + g * 64 + 8 * ds;
+          kw[u] = __ldg(reinterpret_cast<const uint4*>(p.k_cache + off));
+          vw[u] = __ldg(reinterpret_cast<const uint4*>(p.v_cache + off));
+        }
       }
     }
-    const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, vv[4] = {vw.x, vw.y, vw.z, vw.w};
-    float kf[8], vf[8];
     #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      kf[2 * e] = bf16_lo(kk[e]);
-      kf[2 * e + 1] = bf16_hi(kk[e]);
-      vf[2 * e] = bf16_lo(vv[e]);
-      vf[2 * e + 1] = bf16_hi(vv[e]);
-    }
-    #pragma unroll
-    for (int h = 0; h < kDecMaxGroup; ++h) {
-      if (h >= G) continue;                               // uniform: G is per launch
-      float s = 0.0f;
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const uint32_t kk[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
+      const uint32_t vv[4] = {vw[u].x, vw[u].y, vw[u].z, vw[u].w};
+      float kf[8], vf[8];
       #pragma unroll
-      for (int e = 0; e < 8; ++e) s = fmaf(qv[h][e], kf[e], s);
-      // the key's 8 lanes are consecutive: xor 1, 2, 4 stays within them
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
-      if (!valid) continue;
-      if (s > m[h]) {                                     // online softmax, log2 units
-        const float alpha = (m[h] == -INFINITY) ? 0.0f : ex2_approx(m[h] - s);
-        l[h] *= alpha;
+      for (int e = 0; e < 4; ++e) {
+        kf[2 * e] = bf16_lo(kk[e]);
+        kf[2 * e + 1] = bf16_hi(kk[e]);
+        vf[2 * e] = bf16_lo(vv[e]);
+        vf[2 * e + 1] = bf16_hi(vv[e]);
+      }
+      float sc[G];
+      #pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float s0 = qv[h][0] * kf[0], s1 = qv[h][1] * kf[1];
         #pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] *= alpha;
-        m[h] = s;
+        for (int e = 2; e < 8; e += 2) {
+          s0 = fmaf(qv[h][e], kf[e], s0);
+          s1 = fmaf(qv[h][e + 1], kf[e + 1], s1);
+        }
+        sc[h] = s0 + s1;
       }
-      const float pe = ex2_approx(s - m[h]);
-      l[h] += pe;
+      // the key's 8 lanes are consecutive: xor 1, 2, 4 stays within them
       #pragma unroll
-      for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e]);
+      for (int x = 1; x < 8; x <<= 1) {
+        #pragma unroll
+        for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], x);
+      }
+      #pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sv = valid[u] ? sc[h] : -INFINITY;
+        const float mn = fmaxf(m[h], sv);                 // online softmax, log2 units
+        const float mb = (mn == -INFINITY) ? 0.0f : mn;
+        const float alpha = ex2_approx(m[h] - mb);        // 0 while m is -inf
+        const float pe = ex2_approx(sv - mb);             // 0 for an invalid key
+        l[h] = fmaf(l[h], alpha, pe);
+        #pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * alpha);
+        m[h] = mn;
+      }
     }
   }
 
   // merge the 16 key-group states of the CTA
   #pragma unroll
-  for (int h = 0; h < kDecMaxGroup; ++h) {
-    if (h >= G) continue;
+  for (int h = 0; h < G; ++h) {
     if (ds == 0) {
       s_m[state][h] = m[h];
       s_l[state][h] = l[h];

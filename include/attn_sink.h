@@ -172,7 +172,7 @@ int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, cons
  */
 typedef struct attn_sink_decode_params {
   int batch;          /* B >= 0 sequences */
-  int heads_q;        /* H_q, a multiple of heads_kv with H_q / H_kv <= 8 */
+  int heads_q;        /* H_q = G * heads_kv with G in {1, 2, 4, 8} (else UNSUPPORTED) */
   int heads_kv;       /* H_kv >= 1 */
   int head_dim;       /* must be 64 */
   int page_size;      /* keys per cache page, >= 1 */

@@ -241,6 +241,7 @@ def test_decode_rejects_bad_arguments_on_host():
     assert _decode(None) == INVALID
     assert _decode(_dparams(head_dim=32)) == UNSUPPORTED
     assert _decode(_dparams(heads_q=32, heads_kv=2)) == UNSUPPORTED     # 16 heads per kv head
+    assert _decode(_dparams(heads_q=6)) == UNSUPPORTED                  # 3 heads per kv head
     assert _decode(_dparams(heads_q=15)) == INVALID                     # not a multiple
     assert _decode(_dparams(page_size=0)) == INVALID
     assert _decode(_dparams(softmax_scale=0.0)) == INVALID
