@@ -373,29 +373,57 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms = (float(x) for x in tt.tolist())
 
-    # end to end through the C ABI with pinned host buffers, copies inside
+    # End to end through the C ABI with pinned host buffers: every step copies
+    # its inputs in (q, k, v, dout, sink) and its results out (out, lse, dq, dk,
+    # dv, dsink) inside the timed region.  As in a training loop, one step's
+    # copies overlap its neighbours' compute: two device buffer sets, an upload,
+    # a compute and a download stream, ordered by events.
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dout))
     hs = sink.cpu().pin_memory()
-    ho, hl, hdq, hdk, hdv, hds = (torch.empty(t.shape, dtype=t.dtype).pin_memory()
-                                  for t in (out, lse, dq, dk, dv, dsink))
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                 for t in (out, lse, dq, dk, dv, dsink)] for _ in range(2)]
     # the residual of out stays on the device (it only feeds the backward)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hs))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv, hds))
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     e2e_steps = 0 if args.ncu else max(3, min(n, 20))
+    dev_in = [(q, k, v, dout, sink),
+              tuple(torch.empty_like(t) for t in (q, k, v, dout, sink))]
+    dev_out = [(out, out_res, lse, dq, dk, dv, dsink),
+               tuple(torch.empty_like(t) for t in (out, out_res, lse, dq, dk, dv, dsink))]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    cmp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        dout.copy_(hdo, non_blocking=True)
-        sink.copy_(hs, non_blocking=True)
-        fwd()
-        bwd()
-        for h, d_ in ((ho, out), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv), (hds, dsink)):
-            h.copy_(d_, non_blocking=True)
-    e1.record()
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        bsel = i & 1
+        qb, kb, vb, dob, sb = dev_in[bsel]
+        ob, orb, lb, dqb, dkb, dvb, dsb = dev_out[bsel]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(cmp_done[bsel])      # step i-2 has read these inputs
+            for d_, h in ((qb, hq), (kb, hk), (vb, hv), (dob, hdo), (sb, hs)):
+                d_.copy_(h, non_blocking=True)
+            in_ready[bsel].record(s_in)
+        s_cmp.wait_event(in_ready[bsel])
+        if i >= 2:
+            s_cmp.wait_event(out_done[bsel])         # step i-2's results are on the host
+        st = binding.attn_sink_fwd(p, qb, kb, vb, sb, cu_arg, cu_arg, ob, orb, lb, fws,
+                                   fws.numel(), s_cmp)
+        if st == 0:
+            st = binding.attn_sink_bwd(p, qb, kb, vb, sb, cu_arg, cu_arg, ob, orb, lb, dob, dqb,
+                                       dkb, dvb, dsb, workspace, workspace.numel(), s_cmp)
+        if st:
+            raise binding.AttnSinkError(st, "e2e step")
+        cmp_done[bsel].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(cmp_done[bsel])
+            for h, d_ in zip(host_out[bsel], (ob, lb, dqb, dkb, dvb, dsb)):
+                h.copy_(d_, non_blocking=True)
+            out_done[bsel].record(s_out)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / max(e2e_steps, 1)
     st, code = binding.attn_sink_device_error()
