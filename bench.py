@@ -206,6 +206,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device=None) -> list[float]:
+    """Element-wise max of a list of floats over all ranks of the default
+    process group (identity without one): a step is as long as its slowest rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_tflops(flops_per_rank: float, world_size: int, ms: float) -> float:
+    """Throughput of the whole job: every rank processes flops_per_rank (weak
+    scaling, replicas) in `ms`, the max over ranks."""
+    return world_size * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def count_launches(binding, fn) -> int:
     """Kernels libattn_sink launches during fn (the library's own launch counter)."""
     n0 = binding.attn_sink_launch_count()
@@ -368,10 +385,8 @@ def main():
     bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
     fwd_t, bwd_t = sum(fwd_ms) / n, sum(bwd_ms) / n
     step_ms = fwd_t + bwd_t
-    if ws > 1:
-        tt = torch.tensor([step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms = (float(x) for x in tt.tolist())
+    step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms = max_over_ranks(
+        [step_ms, fwd_t, bwd_t, fwd_kernel_ms, bwd_main_ms], device=dev)
 
     # End to end through the C ABI with pinned host buffers: every step copies
     # its inputs in (q, k, v, dout, sink) and its results out (out, lse, dq, dk,
@@ -425,14 +440,14 @@ def main():
             out_done[bsel].record(s_out)
     e1.record(s_out)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / max(e2e_steps, 1)
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / max(e2e_steps, 1)], device=dev)[0]
     st, code = binding.attn_sink_device_error()
     if st != 0 or code != 0:
         raise RuntimeError(f"device error word {code:#x}")
 
     alg = algorithmic(w, lengths)
     flops = alg["fwd_flops"] + alg["bwd_flops"]
-    value = ws * flops / (step_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, ws, step_ms)
     fwd_tf = alg["fwd_flops"] / (fwd_t * 1e-3) / 1e12
     bwd_tf = alg["bwd_flops"] / (bwd_t * 1e-3) / 1e12
     peaks, src = load_peaks()
@@ -469,7 +484,7 @@ def main():
                          "traffic": dram_traffic("attn_sink_fwd_kernel", w.name),
                          "hbm_gbs": alg["fwd_bytes"] / (fwd_kernel_ms * 1e-3) / 1e9},
         "e2e": None if args.ncu else {
-            "value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "value": whole_job_tflops(flops, ws, e2e_ms), "unit": "TFLOP/s",
             "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_timed,
         "gpu_launches_per_step": launches_per_step,
