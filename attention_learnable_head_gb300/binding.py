@@ -6,7 +6,8 @@
 ``attn_sink_launch_count``, ``attn_sink_last_cuda_error``,
 ``attn_sink_kernel_timing``, ``attn_sink_kernel_time``, ``attn_sink_fwd_chunk``,
 ``attn_sink_merge``, ``attn_sink_bwd_deterministic``, ``attn_sink_decode``,
-``attn_sink_decode_workspace_size`` and ``attn_sink_fwd_noalloc`` mirror the C entry
+``attn_sink_decode_workspace_size``, ``attn_sink_fwd_ex``, ``attn_sink_bwd_ex`` and
+``attn_sink_fwd_noalloc`` mirror the C entry
 points of ``include/attn_sink.h`` one to one: they only turn tensors into
 device pointers and return the library's status.  ``forward``, ``backward``
 and ``attn_sink`` (autograd) are conveniences on top that allocate outputs and
@@ -114,6 +115,10 @@ def lib():
     L.attn_sink_bwd.restype = c_int
     L.attn_sink_bwd_deterministic.argtypes = L.attn_sink_bwd.argtypes
     L.attn_sink_bwd_deterministic.restype = c_int
+    L.attn_sink_fwd_ex.argtypes = [P, c_int] + L.attn_sink_fwd.argtypes[1:]
+    L.attn_sink_fwd_ex.restype = c_int
+    L.attn_sink_bwd_ex.argtypes = [P, c_int] + L.attn_sink_bwd.argtypes[1:]
+    L.attn_sink_bwd_ex.restype = c_int
     L.attn_sink_status_string.argtypes = [c_int]
     L.attn_sink_status_string.restype = ctypes.c_char_p
     L.attn_sink_device_error.argtypes = [c_void_p, ctypes.POINTER(c_int)]
@@ -158,6 +163,30 @@ def attn_sink_fwd(params: AttnSinkParams, q, k, v, sink, cu_seqlens_q, cu_seqlen
                                _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
                                _ptr(out_residual), _ptr(lse), _ptr(workspace),
                                int(workspace_bytes), _stream(stream))
+
+
+ATTN_SINK_FLAG_SINK_BF16 = 1
+ATTN_SINK_FLAG_ACCUMULATE_DSINK = 2
+ATTN_SINK_FLAG_DETERMINISTIC = 4
+
+
+def attn_sink_fwd_ex(params: AttnSinkParams, flags: int, q, k, v, sink, cu_seqlens_q,
+                     cu_seqlens_k, out, out_residual, lse, workspace, workspace_bytes: int,
+                     stream=None) -> int:
+    return lib().attn_sink_fwd_ex(_pref(params), int(flags), _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(sink), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                                  _ptr(out_residual), _ptr(lse), _ptr(workspace),
+                                  int(workspace_bytes), _stream(stream))
+
+
+def attn_sink_bwd_ex(params: AttnSinkParams, flags: int, q, k, v, sink, cu_seqlens_q,
+                     cu_seqlens_k, out, out_residual, lse, dout, dq, dk, dv, dsink, workspace,
+                     workspace_bytes: int, stream=None) -> int:
+    return lib().attn_sink_bwd_ex(_pref(params), int(flags), _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(sink), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(out),
+                                  _ptr(out_residual), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(dsink), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream))
 
 
 def attn_sink_fwd_chunk(params: AttnSinkParams, q_pos0: int, q, k, v, cu_seqlens_q,
@@ -349,8 +378,13 @@ def forward(q, k, v, sink, *, causal: bool = True, window: int = 0,
     lse = torch.empty((q.shape[-2], _lse_len(q)), dtype=torch.float32, device=q.device)
     nbytes = attn_sink_fwd_workspace_size(p)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
-    _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, res, lse, ws,
-                         ws.numel(), stream), "attn_sink_fwd")
+    if sink.dtype == torch.bfloat16:      # a bf16 sink parameter, read exactly
+        _check(attn_sink_fwd_ex(p, ATTN_SINK_FLAG_SINK_BF16, q, k, v, sink, cu_seqlens_q,
+                                cu_seqlens_k, out, res, lse, ws, ws.numel(), stream),
+               "attn_sink_fwd_ex")
+    else:
+        _check(attn_sink_fwd(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, res, lse, ws,
+                             ws.numel(), stream), "attn_sink_fwd")
     return out, lse, res
 
 
@@ -392,9 +426,12 @@ def backward(q, k, v, sink, out, lse, dout, *, out_residual=None, causal: bool =
              window: int = 0, softmax_scale: float | None = None, cu_seqlens_q=None,
              cu_seqlens_k=None, max_seqlen_q: int | None = None,
              max_seqlen_k: int | None = None, grad_dtype: int = 0, workspace=None,
-             deterministic: bool = False, stream=None):
-    """dq, dk, dv (bf16, or fp32 when grad_dtype = 1) and dsink ([H_q] fp32).
-    deterministic=True: bitwise reproducible (attn_sink_bwd_deterministic)."""
+             deterministic: bool = False, dsink=None, accumulate_dsink: bool = False,
+             stream=None):
+    """dq, dk, dv (bf16, or fp32 when grad_dtype = 1) and dsink ([H_q], the
+    sink's dtype: fp32, or bf16 for a bf16 sink).
+    deterministic=True: bitwise reproducible (attn_sink_bwd_deterministic);
+    accumulate_dsink=True: the gradient is added into the given `dsink`."""
     num_seqs = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_params(q.shape, k.shape, causal=causal, window=window, softmax_scale=softmax_scale,
                     num_seqs=num_seqs, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
@@ -403,13 +440,24 @@ def backward(q, k, v, sink, out, lse, dout, *, out_residual=None, causal: bool =
     dq = torch.empty(q.shape, dtype=gd, device=q.device)
     dk = torch.empty(k.shape, dtype=gd, device=q.device)
     dv = torch.empty(v.shape, dtype=gd, device=q.device)
-    dsink = torch.empty_like(sink)
+    if accumulate_dsink and dsink is None:
+        raise ValueError("accumulate_dsink needs the dsink tensor to add into")
+    if dsink is None:
+        dsink = torch.empty_like(sink)
     nbytes = attn_sink_bwd_workspace_size(p)
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
-    fn = attn_sink_bwd_deterministic if deterministic else attn_sink_bwd
-    _check(fn(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
-              dout, dq, dk, dv, dsink, workspace, workspace.numel(), stream), fn.__name__)
+    flags = ((ATTN_SINK_FLAG_SINK_BF16 if sink.dtype == torch.bfloat16 else 0)
+             | (ATTN_SINK_FLAG_ACCUMULATE_DSINK if accumulate_dsink else 0)
+             | (ATTN_SINK_FLAG_DETERMINISTIC if deterministic else 0))
+    if flags & (ATTN_SINK_FLAG_SINK_BF16 | ATTN_SINK_FLAG_ACCUMULATE_DSINK):
+        _check(attn_sink_bwd_ex(p, flags, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out,
+                                out_residual, lse, dout, dq, dk, dv, dsink, workspace,
+                                workspace.numel(), stream), "attn_sink_bwd_ex")
+    else:
+        fn = attn_sink_bwd_deterministic if deterministic else attn_sink_bwd
+        _check(fn(p, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  dout, dq, dk, dv, dsink, workspace, workspace.numel(), stream), fn.__name__)
     return dq, dk, dv, dsink
 
 

@@ -327,9 +327,9 @@ namespace {
 // The forward, with or without the sink; `chunk` selects key-chunk mode (no
 // sink, query row i at key position i + q_pos0 in every sequence).
 int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const void* v,
-             const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k, void* out,
+             const void* sink, const int* cu_seqlens_q, const int* cu_seqlens_k, void* out,
              void* out_residual, float* lse, void* workspace, size_t workspace_bytes,
-             void* stream, bool chunk, int q_pos0) {
+             void* stream, bool chunk, int q_pos0, bool sink_bf16) {
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -371,7 +371,8 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   }
   fp.cu_q = cu_seqlens_q;
   fp.cu_k = cu_seqlens_k;
-  fp.sink = sink;
+  fp.sink = sink_bf16 ? nullptr : static_cast<const float*>(sink);
+  fp.sink_bf16 = sink_bf16 ? static_cast<const __nv_bfloat16*>(sink) : nullptr;
   fp.out = static_cast<__nv_bfloat16*>(out);
   fp.out_lo = static_cast<__nv_bfloat16*>(out_residual);
   fp.lse = lse;
@@ -405,7 +406,17 @@ int attn_sink_fwd(const attn_sink_params* params, const void* q, const void* k, 
                   void* out, void* out_residual, float* lse, void* workspace,
                   size_t workspace_bytes, void* stream) {
   return fwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
-                  workspace, workspace_bytes, stream, false, 0);
+                  workspace, workspace_bytes, stream, false, 0, false);
+}
+
+int attn_sink_fwd_ex(const attn_sink_params* params, int flags, const void* q, const void* k,
+                     const void* v, const void* sink, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if ((flags & ~ATTN_SINK_FLAG_SINK_BF16) != 0) return ATTN_SINK_ERR_INVALID_ARG;
+  return fwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  workspace, workspace_bytes, stream, false, 0,
+                  (flags & ATTN_SINK_FLAG_SINK_BF16) != 0);
 }
 
 int attn_sink_fwd_chunk(const attn_sink_params* params, int q_pos0, const void* q,
@@ -413,7 +424,7 @@ int attn_sink_fwd_chunk(const attn_sink_params* params, int q_pos0, const void* 
                         const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
   return fwd_impl(params, q, k, v, nullptr, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
-                  workspace, workspace_bytes, stream, true, q_pos0);
+                  workspace, workspace_bytes, stream, true, q_pos0, false);
 }
 
 int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, const void* o_parts,
@@ -589,10 +600,13 @@ namespace {
 // The backward; `deterministic` computes dQ with the query-stationary kernel
 // (fixed summation order) instead of reduce-adds from the main kernel.
 int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const void* v,
-             const float* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
+             const void* sink, const int* cu_seqlens_q, const int* cu_seqlens_k,
              const void* out, const void* out_residual, const float* lse, const void* dout,
-             void* dq, void* dk, void* dv, float* dsink, void* workspace,
-             size_t workspace_bytes, void* stream, bool deterministic) {
+             void* dq, void* dk, void* dv, void* dsink, void* workspace,
+             size_t workspace_bytes, void* stream, int flags) {
+  const bool deterministic = (flags & ATTN_SINK_FLAG_DETERMINISTIC) != 0;
+  const bool sink_bf16 = (flags & ATTN_SINK_FLAG_SINK_BF16) != 0;
+  const bool accumulate = (flags & ATTN_SINK_FLAG_ACCUMULATE_DSINK) != 0;
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -635,7 +649,8 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
     pp.out = static_cast<const __nv_bfloat16*>(out);
     pp.dout = static_cast<const __nv_bfloat16*>(dout);
     pp.lse = lse;
-    pp.sink = sink;
+    pp.sink = sink_bf16 ? nullptr : static_cast<const float*>(sink);
+    pp.sink_bf16 = sink_bf16 ? static_cast<const __nv_bfloat16*>(sink) : nullptr;
     pp.LD = LD;
     pp.partials = partials;
     pp.dq_acc = deterministic ? nullptr : dq_acc;
@@ -761,10 +776,13 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   }
   // 4. dsink
   if (g.total_q > 0) {
-    attn_sink_dsink_reduce_kernel<<<params->heads_q, 256, 0, s>>>(partials, L.n_blocks, dsink);
+    attn_sink_dsink_reduce_kernel<<<params->heads_q, 256, 0, s>>>(
+        partials, L.n_blocks, dsink, sink_bf16 ? 1 : 0, accumulate ? 1 : 0);
     return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
   }
-  if (cudaMemsetAsync(dsink, 0, sizeof(float) * params->heads_q, s) != cudaSuccess)
+  // no query row: the gradient is zero (nothing to add when accumulating)
+  if (!accumulate && cudaMemsetAsync(dsink, 0, (sink_bf16 ? 2 : 4) * (size_t)params->heads_q,
+                                     s) != cudaSuccess)
     return ATTN_SINK_ERR_CUDA;
   return ATTN_SINK_OK;
 }
@@ -779,7 +797,7 @@ int attn_sink_bwd(const attn_sink_params* params, const void* q, const void* k, 
                   const void* dout, void* dq, void* dk, void* dv, float* dsink,
                   void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
-                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream, false);
+                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream, 0);
 }
 
 int attn_sink_bwd_deterministic(const attn_sink_params* params, const void* q, const void* k,
@@ -789,7 +807,20 @@ int attn_sink_bwd_deterministic(const attn_sink_params* params, const void* q, c
                                 void* dq, void* dk, void* dv, float* dsink, void* workspace,
                                 size_t workspace_bytes, void* stream) {
   return bwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
-                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream, true);
+                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream,
+                  ATTN_SINK_FLAG_DETERMINISTIC);
+}
+
+int attn_sink_bwd_ex(const attn_sink_params* params, int flags, const void* q, const void* k,
+                     const void* v, const void* sink, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, const void* out, const void* out_residual,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     void* dsink, void* workspace, size_t workspace_bytes, void* stream) {
+  if ((flags & ~(ATTN_SINK_FLAG_SINK_BF16 | ATTN_SINK_FLAG_ACCUMULATE_DSINK |
+                 ATTN_SINK_FLAG_DETERMINISTIC)) != 0)
+    return ATTN_SINK_ERR_INVALID_ARG;
+  return bwd_impl(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
+                  dout, dq, dk, dv, dsink, workspace, workspace_bytes, stream, flags);
 }
 
 // Caller entry point that allocates nothing: the workspace of attn_sink_fwd is

@@ -88,6 +88,7 @@ struct PreParams {
   const __nv_bfloat16* dout;
   const float* lse;
   const float* sink;
+  const __nv_bfloat16* sink_bf16;   // bf16 sink when non-null
   float2* LD;          // [H_q][T_q]: (lse * log2 e, D)
   float* partials;     // [H_q][n_blocks]
   float* dq_acc;       // [T_q][H_q][64]
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
   const int tid = threadIdx.x;
   const int sub = tid & 7;          // 16-byte slice of the 128-byte row
   const int rloc = tid >> 3;        // 0..31
-  const float sink_h = p.sink[h];
+  const float sink_h = p.sink_bf16 ? __bfloat162float(p.sink_bf16[h]) : p.sink[h];
   float acc = 0.0f;                 // dsink contribution of this thread's rows
   bool overflow = false;
   #pragma unroll 1
@@ -199,9 +200,12 @@ __global__ void __launch_bounds__(256) attn_sink_kv_convert_kernel(
 }
 
 // ------------------------------------------------------------------ dsink_reduce
+// dsink[h] (fp32, or bf16 with dsink_bf16) = the sum of the partials, or
+// += it with accumulate.
 __global__ void __launch_bounds__(256) attn_sink_dsink_reduce_kernel(const float* partials,
-                                                                     int n_blocks,
-                                                                     float* dsink) {
+                                                                     int n_blocks, void* dsink,
+                                                                     int dsink_bf16,
+                                                                     int accumulate) {
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
   float s = 0.0f;
@@ -215,7 +219,13 @@ __global__ void __launch_bounds__(256) attn_sink_dsink_reduce_kernel(const float
     float t = 0.0f;
     #pragma unroll
     for (int w = 0; w < 8; ++w) t += wsum[w];
-    dsink[h] = t;
+    if (dsink_bf16) {
+      __nv_bfloat16* d = static_cast<__nv_bfloat16*>(dsink) + h;
+      *d = __float2bfloat16_rn(accumulate ? __bfloat162float(*d) + t : t);
+    } else {
+      float* d = static_cast<float*>(dsink) + h;
+      *d = accumulate ? *d + t : t;
+    }
   }
 }
 

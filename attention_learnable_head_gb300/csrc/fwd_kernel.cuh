@@ -68,7 +68,8 @@ struct FwdParams {
   CUtensorMap tm_v;
   const int* cu_q;    // null for a dense batch
   const int* cu_k;
-  const float* sink;  // [H_q]
+  const float* sink;  // [H_q] fp32, or
+  const __nv_bfloat16* sink_bf16;   // [H_q] bf16 when non-null
   __nv_bfloat16* out; // [T_q][H_q][64]
   __nv_bfloat16* out_lo; // [T_q][H_q][64] residual O/l - out, or null
   float* lse;         // [H_q][T_q]
@@ -167,7 +168,9 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   }
   const int num = (kr_a.num > 0 || kr_b.num > 0) ? hi - lo : 0;
   // chunk mode: no sink (its logit is -inf, i.e. absent from the normaliser)
-  const float sink_h = p.chunk ? -INFINITY : __ldg(p.sink + h);
+  const float sink_h = p.chunk       ? -INFINITY
+                      : p.sink_bf16 ? __bfloat162float(p.sink_bf16[h])
+                                    : __ldg(p.sink + h);
 
   if (num == 0) {
     // No row of this block sees a key: out = 0, lse = sink (the sink alone).

@@ -208,6 +208,41 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Flags of attn_sink_fwd_ex / attn_sink_bwd_ex, for a sink held as a bf16
+ * training parameter whose gradient accumulates over micro-batches (direct use
+ * under sharded data-parallel training; the pages train GPT-OSS with FSDP:
+ * ai-engineering-academy page, section "Desafio 2: Inconsistência
+ * Treino-Inferência").
+ */
+#define ATTN_SINK_FLAG_SINK_BF16 1        /* sink and dsink are bf16 [H_q] */
+#define ATTN_SINK_FLAG_ACCUMULATE_DSINK 2 /* bwd: dsink += gradient (else =) */
+#define ATTN_SINK_FLAG_DETERMINISTIC 4    /* bwd: as attn_sink_bwd_deterministic */
+
+/*
+ * attn_sink_fwd with flags (only ATTN_SINK_FLAG_SINK_BF16; any other bit
+ * returns ATTN_SINK_ERR_INVALID_ARG).  With it, sink points to bf16 [H_q],
+ * read exactly (bf16 -> fp32).  Everything else as attn_sink_fwd.
+ */
+int attn_sink_fwd_ex(const attn_sink_params* params, int flags, const void* q, const void* k,
+                     const void* v, const void* sink, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, void* out, void* out_residual, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_sink_bwd with flags.  ATTN_SINK_FLAG_SINK_BF16: sink and dsink are bf16
+ * [H_q] (dsink rounded to nearest from the fp32 sum);
+ * ATTN_SINK_FLAG_ACCUMULATE_DSINK: dsink += the gradient (in fp32 for an fp32
+ * dsink, in bf16 after the fp32 sum otherwise) instead of dsink = gradient;
+ * ATTN_SINK_FLAG_DETERMINISTIC: the bitwise-reproducible backward.  Unknown
+ * bits return ATTN_SINK_ERR_INVALID_ARG.  Everything else as attn_sink_bwd.
+ */
+int attn_sink_bwd_ex(const attn_sink_params* params, int flags, const void* q, const void* k,
+                     const void* v, const void* sink, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, const void* out, const void* out_residual,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     void* dsink, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace attn_sink_fwd needs (0 if the params are invalid):
  * an fp16 copy of v [T_k, H_kv, 64] for the tensor cores.  Same conventions as
  * attn_sink_bwd_workspace_size (packed fields when num_seqs > 0).  A workspace

@@ -25,7 +25,8 @@ def test_exports_every_declared_symbol():
                           "attn_sink_last_cuda_error", "attn_sink_kernel_timing",
                           "attn_sink_kernel_time", "attn_sink_fwd_chunk", "attn_sink_merge",
                           "attn_sink_bwd_deterministic", "attn_sink_decode",
-                          "attn_sink_decode_workspace_size",
+                          "attn_sink_decode_workspace_size", "attn_sink_fwd_ex",
+                          "attn_sink_bwd_ex",
                           "attn_sink_status_string", "attn_sink_device_error",
                           "attn_sink_launch_count"}
     lib = binding.lib()
@@ -260,6 +261,23 @@ def test_decode_rejects_bad_arguments_on_host():
     assert binding.attn_sink_decode_workspace_size(_dparams(batch=0)) == 0
     assert binding.attn_sink_decode_workspace_size(_dparams(head_dim=32)) == 0
     assert binding.attn_sink_decode_workspace_size(None) == 0
+
+
+def test_ex_entry_points_reject_unknown_flags_on_host():
+    n0 = binding.attn_sink_launch_count()
+    p = _dense()
+    args = (FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE, FAKE, 1 << 40)
+    for bad in (2, 4, 8, -1):                       # forward knows only SINK_BF16
+        assert binding.attn_sink_fwd_ex(p, bad, *args, stream=0) == INVALID, bad
+    bargs = (FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+             FAKE, 1 << 40)
+    for bad in (8, 16, -1):
+        assert binding.attn_sink_bwd_ex(p, bad, *bargs, stream=0) == INVALID, bad
+    assert binding.attn_sink_fwd_ex(None, 1, *args, stream=0) == INVALID
+    assert binding.attn_sink_bwd_ex(None, 7, *bargs, stream=0) == INVALID
+    assert binding.attn_sink_fwd_ex(_dense(head_dim=32), 1, *args, stream=0) == UNSUPPORTED
+    assert binding.attn_sink_bwd_ex(_dense(head_dim=32), 3, *bargs, stream=0) == UNSUPPORTED
+    assert binding.attn_sink_launch_count() == n0
 
 
 def test_forward_workspace_checked_on_host():
