@@ -332,7 +332,7 @@ __device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, dq_free, drained;
+  __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2];
   __shared__ float2 s_LD[kBwdStages][kBlockM];    // (lse * log2 e, D) of the step's rows
@@ -390,7 +390,6 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     mbar_init(&kv_full, 1);
     mbar_init(&kv_tmem, 2 * kBlockN);
     mbar_init(&mma2_done, 1);
-    mbar_init(&dq_free, kBlockM);
     mbar_init(&drained, 1);
     for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 lanes' cp.async (lse / D)
@@ -398,7 +397,9 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     }
     for (int hh = 0; hh < 2; ++hh) {
       mbar_init(&s_full[hh], 1);
-      mbar_init(&p_full[hh], kBlockN);
+      // half 1 also waits for the dQ warps to have read the previous dQ out of
+      // TMEM (they arrive on it), so the MMA thread needs no separate wait
+      mbar_init(&p_full[hh], kBlockN + (hh == 1 && !p.skip_dq ? kBlockM : 0));
     }
     fence_mbarrier_init();
   }
@@ -510,8 +511,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
                    id_dvdk, (m > 0 || hh > 0 || k > 0));
           if (hh == 1) {
             if (!p.skip_dq) {
-              if (m > 0 && !mbar_wait(&dq_free, (m - 1) & 1, &abort_flag)) { ok = false; break; }
-              tc_fence_after();
+              // p_full[1](m) included the dQ warps' arrival: dQ(m - 1) is read
               // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
               #pragma unroll
               for (int k = 0; k < kBlockN / 16; ++k)
@@ -641,6 +641,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const uint32_t stage = smem_u32(sdQ);
     bool ok = true;
     // (with skip_dq there is no dQ here: the loop does not run)
+    // The dQ TMEM columns are free for step 0.
+    if (!p.skip_dq && num > 0) mbar_arrive(&p_full[1]);
     for (int m = 0; m < (p.skip_dq ? 0 : num); ++m) {
       const int h = h_first + m / nqt;
       const int i0 = (qt_first + m % nqt) * kBlockM;
@@ -655,7 +657,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tmem_ld_x32(tmem + lane_base + kColDQ + 32, v + 32);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&dq_free);
+      // dQ TMEM is free for the next step: arrive on its half-1 P barrier
+      if (m + 1 < num) mbar_arrive(&p_full[1]);
       #pragma unroll
       for (int half = 0; half < 2; ++half) {
         #pragma unroll
