@@ -387,9 +387,9 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   fp.scale_log2 = params->softmax_scale * kLog2e;
   fp.chunk = chunk ? 1 : 0;
   fp.q_pos0 = chunk ? q_pos0 : 0;
-  fp.n_qblocks = (g.max_q + kFwdRowsPerCta - 1) / kFwdRowsPerCta;
-  if (fp.n_qblocks == 0) return ATTN_SINK_OK;
-  dim3 grid(params->heads_q, g.num_seqs, fp.n_qblocks);
+  fp.n_qtiles = (g.max_q + kBlockM - 1) / kBlockM;
+  if (fp.n_qtiles == 0) return ATTN_SINK_OK;
+  dim3 grid(params->heads_q, g.num_seqs, fp.n_qtiles);
   const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_FWD, static_cast<cudaStream_t>(stream));
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
   const bool ok = launched();

@@ -1,9 +1,13 @@
 // Forward kernel: attention with a per-head sink, sm_103a (tcgen05 + TMA).
 //
-// One CTA per (query head h, sequence, 256-row query block).  The block is two
-// 128-row tiles, A and B, that share every K/V tile and run in ping-pong: while
-// one tile's softmax turns its S tile into P, the tensor cores run the other
-// tile's MMAs.  Per tile and key tile:
+// One CTA per (query head h, sequence, 128-row query tile); two CTAs share an
+// SM (320 threads x 96 registers, 86 KB of SMEM and 256 TMEM columns each), so
+// while one CTA's softmax turns its S tile into P the tensor cores run the
+// other CTA's MMAs, and one CTA's set-up, Q load and epilogue overlap the
+// other's loop.  Two CTAs with one MMA issuer each keep the tensor pipe busier
+// than one CTA whose single issuer alternates between two tiles: every pause
+// of an issuer (an mbarrier wait costs ~200 cycles) idles the pipe only for
+// its own CTA.  Per key tile:
 //   S = Q K^T (tcgen05, bf16 operands from SMEM, fp32 accumulators in TMEM),
 //   online softmax whose running max and sum start from the sink logit
 //   (m0 = sink[h] * log2 e, l0 = 1 in the exp2 domain),
@@ -30,16 +34,16 @@
 // stays below 2^threshold, and out/lse are exact because l_c and O_c use the
 // same max.
 //
-// Warp roles (576 threads):
-//   warps 0-3   softmax of tile A, key half 0 (thread t owns row t = TMEM lane t)
-//   warps 4-7   tile A, key half 1;   warps 8-11 / 12-15: tile B, halves 0 / 1
-//   warp 16     TMA producer: Q_A, Q_B once, then K/V tiles through a ring
-//   warp 17     MMA issuer (one lane) and TMEM owner
-// TMEM columns: S_A 0, S_B 128 (128 fp32 each; P_xc, 64 fp16 two per column, is
-// written over the first 32 columns of half c of S_x once read), O_A0 256,
-// O_A1 320, O_B0 384, O_B1 448 (64 fp32 each).
-// P_xc overwrites S_x safely: PV_x(n) is issued before S_x(n+1) by the same
-// thread, and tcgen05 MMAs from one thread execute in issue order.
+// Warp roles (320 threads):
+//   warps 0-3   softmax of key half 0 (thread t owns row t = TMEM lane t)
+//   warps 4-7   softmax of key half 1
+//   warp 8      TMA producer: Q once, then K/V tiles through a two-stage ring
+//   warp 9      MMA issuer (one lane) and TMEM owner
+// TMEM columns (256 allocated): S 0-127 (fp32; P_c, 64 fp16 two per column, is
+// written over the first 32 columns of half c of S once read), O_0 128-191,
+// O_1 192-255 (fp32).
+// P_c overwrites S safely: PV(n) is issued before S(n+1) by the same thread,
+// and tcgen05 MMAs from one thread execute in issue order.
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -49,15 +53,16 @@ namespace attn_sink {
 constexpr int kBlockM = 128;   // query rows per tile
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kHeadDim = 64;
-constexpr int kFwdTiles = 2;   // query tiles per CTA
-constexpr int kFwdStages = 4;
-constexpr int kFwdThreads = 576;    // 16 softmax warps, TMA warp, MMA warp
-constexpr int kFwdTmaWarp = 16;
-constexpr int kFwdMmaWarp = 17;
-constexpr int kFwdRowsPerCta = kFwdTiles * kBlockM;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
 constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
-constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (kFwdTiles + 2 * kFwdStages);
+
+constexpr int kFwdStages = 2;       // K/V ring depth
+constexpr int kFwdThreads = 320;    // 8 softmax warps, TMA warp, MMA warp
+constexpr int kFwdTmaWarp = 8;
+constexpr int kFwdMmaWarp = 9;
+constexpr uint32_t kFwdTmemCols = 256;
+constexpr uint32_t kFwdColO = 128;  // first O column
+constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (1 + 2 * kFwdStages);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -79,7 +84,7 @@ struct FwdParams {
   int heads_q, group;
   int causal, window;
   float scale_log2;   // softmax_scale * log2(e)
-  int n_qblocks;      // 256-row query blocks of the longest sequence
+  int n_qtiles;       // 128-row query tiles of the longest sequence
   // Key-chunk mode: no sink term, and query row i of every sequence sits at key
   // position i + q_pos0 (the default is bottom-right: q_pos0 = N_k - N_q).
   int chunk;
@@ -127,54 +132,41 @@ __device__ __forceinline__ KeyRange key_tiles(int r0, int r1, const SeqSpan& sp,
   return kr;
 }
 
-// Registers are split per SM sub-partition (16384 each); with 18 warps one of the
-// four hosts 5 warps, so a thread may use at most 102: 96 is used.
+// Registers are split per SM sub-partition (16384 each); two CTAs of 10 warps
+// place 5 warps on each, so a thread may use at most 102: 96 is used.
 __global__ void __maxnreg__(96)
 attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, mma_drained;
   __shared__ __align__(8) uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
-  __shared__ __align__(8) uint64_t s_full[kFwdTiles], p_full[kFwdTiles], pv_done[kFwdTiles][2];
+  __shared__ __align__(8) uint64_t s_full, p_full, pv_done[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ float s_red_m[kFwdTiles][2][kBlockM];   // [tile][half][row], epilogue only
-  __shared__ float s_red_l[kFwdTiles][2][kBlockM];
+  __shared__ float s_red_m[2][kBlockM];   // [half][row], epilogue only
+  __shared__ float s_red_l[2][kBlockM];
 
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
-  const int qblock = p.n_qblocks - 1 - (int)blockIdx.z;   // longest work first
+  const int qtile = p.n_qtiles - 1 - (int)blockIdx.z;    // longest work first
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
-  const int i0 = qblock * (kFwdTiles * kBlockM);
+  const int i0 = qtile * kBlockM;
   if (i0 >= sp.nq) return;                                // uniform per CTA
   const int g = h / p.group;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const bool has_b = i0 + kBlockM < sp.nq;
+  const int tile_r1 = min(i0 + kBlockM, sp.nq) - 1;       // last row of the tile
   // key position of query row 0 (bottom-right alignment unless chunk mode sets it)
   const int off = p.chunk ? p.q_pos0 : sp.nk - sp.nq;
-  const KeyRange kr_a = key_tiles(i0, min(i0 + kBlockM, sp.nq) - 1, sp, off, p.causal, p.window);
-  const KeyRange kr_b = has_b ? key_tiles(i0 + kBlockM, min(i0 + 2 * kBlockM, sp.nq) - 1, sp,
-                                          off, p.causal, p.window)
-                              : KeyRange{0, 0};
-  // union of the two tiles' key ranges
-  int lo, hi;
-  if (kr_a.num > 0 && kr_b.num > 0) {
-    lo = min(kr_a.lo, kr_b.lo);
-    hi = max(kr_a.lo + kr_a.num, kr_b.lo + kr_b.num);
-  } else if (kr_a.num > 0) {
-    lo = kr_a.lo; hi = kr_a.lo + kr_a.num;
-  } else {
-    lo = kr_b.lo; hi = kr_b.lo + kr_b.num;
-  }
-  const int num = (kr_a.num > 0 || kr_b.num > 0) ? hi - lo : 0;
+  const KeyRange kr = key_tiles(i0, tile_r1, sp, off, p.causal, p.window);
+  const int lo = kr.lo, num = kr.num;
   // chunk mode: no sink (its logit is -inf, i.e. absent from the normaliser)
   const float sink_h = p.chunk       ? -INFINITY
                       : p.sink_bf16 ? __bfloat162float(p.sink_bf16[h])
                                     : __ldg(p.sink + h);
 
   if (num == 0) {
-    // No row of this block sees a key: out = 0, lse = sink (the sink alone).
-    for (int t = tid; t < kFwdTiles * kBlockM; t += kFwdThreads) {
+    // No row of this tile sees a key: out = 0, lse = sink (the sink alone).
+    for (int t = tid; t < kBlockM; t += kFwdThreads) {
       if (i0 + t < sp.nq) {
         const size_t row = (size_t)(sp.q0 + i0 + t);
         uint4* o = reinterpret_cast<uint4*>(p.out + (row * p.heads_q + h) * kHeadDim);
@@ -193,8 +185,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;                                   // kFwdTiles tiles
-  uint8_t* sK = sQ + kFwdTiles * kTileBytes;
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kTileBytes;
   uint8_t* sV = sK + kFwdStages * kTileBytes;
 
   if (tid == 0) {
@@ -205,15 +197,13 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int x = 0; x < kFwdTiles; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 2 * kBlockM);
-      for (int c = 0; c < 2; ++c) mbar_init(&pv_done[x][c], 1);
-    }
+    mbar_init(&s_full, 1);
+    mbar_init(&p_full, 2 * kBlockM);
+    for (int c = 0; c < 2; ++c) mbar_init(&pv_done[c], 1);
     fence_mbarrier_init();
   }
   if (warp == kFwdMmaWarp) {
-    tmem_alloc(&tmem_base_sh, 512);
+    tmem_alloc(&tmem_base_sh, kFwdTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -228,9 +218,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       const uint64_t keep = l2_policy_evict_last();
-      mbar_arrive_expect_tx(&q_full, (has_b ? 2 : 1) * kTileBytes);
+      mbar_arrive_expect_tx(&q_full, kTileBytes);
       tma_load_3d(&p.tm_q, &q_full, sQ, 0, h, sp.q0 + i0);
-      if (has_b) tma_load_3d(&p.tm_q, &q_full, sQ + kTileBytes, 0, h, sp.q0 + i0 + kBlockM);
       int issued = 0;
       for (int it = 0; it < num; ++it) {
         const int st = it % kFwdStages;
@@ -257,93 +246,61 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else if (warp == kFwdMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    // Per tile x and key tile n: S_x = Q_x K_n^T (M=N=128) into TMEM; the softmax
-    // of key half c (S_x columns [64c, 64c+64)) writes P_xc (fp16) over the first
-    // 32 of its columns, and O_xc += P_xc V_n[64c, 64c+64) (M=128, N=64, K=64, A
-    // from TMEM).  S_x(n+1) is issued right after PV_x0(n) and PV_x1(n): the same
-    // thread issues them and tcgen05 MMAs execute in issue order, so both P_xc are
-    // read before S_x(n+1) overwrites them.
-    // The tensor pipe holds little more than the MMA being executed, so every
-    // pause of this thread between MMAs (an mbarrier wait costs ~200 cycles even
-    // when the phase has already completed) leaves it idle: the thread waits once
-    // per key tile for K/V and once per tile for P, and issues 12 MMAs in a row.
+    // Per key tile n: S = Q K_n^T (M=N=128) into TMEM; the softmax of key half c
+    // (S columns [64c, 64c+64)) writes P_c (fp16) over the first 32 of its
+    // columns, and O_c += P_c V_n[64c, 64c+64) (M=128, N=64, K=64, A from TMEM).
+    // S(n+1) is issued right after PV_0(n) and PV_1(n): the same thread issues
+    // them and tcgen05 MMAs execute in issue order, so both P_c are read before
+    // S(n+1) overwrites them.  The thread waits once per key tile for K/V and
+    // once for P, and issues 12 MMAs in a row.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
       const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
-      const KeyRange kr[kFwdTiles] = {kr_a, kr_b};
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
       // Shared-memory descriptors, built once; an operand at byte offset o from a
       // base is the base's descriptor plus o / 16 (the start-address field).
-      const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16384, 1024);   // MN-major
       constexpr uint32_t kTileU = kTileBytes >> 4;
       constexpr uint32_t kHalfU = (64 * kHeadDim * 2) >> 4;   // 64 rows of V
-      // K/V of union key tiles [0, kv_seen] have landed (waited in order).
-      int kv_seen = -1;
       auto kv_ready = [&](int n) -> bool {
-        for (int a = kv_seen + 1; a <= n; ++a) {
-          if (!mbar_wait(&kv_full[a % kFwdStages], (a / kFwdStages) & 1, &abort_flag))
-            return false;
-          kv_seen = a;
-        }
+        if (!mbar_wait(&kv_full[n % kFwdStages], (n / kFwdStages) & 1, &abort_flag))
+          return false;
         tc_fence_after();
         return true;
       };
-      auto issue_s = [&](int x, int n) {
+      auto issue_s = [&](int n) {
         const int st = n % kFwdStages;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + x * 128, dQ0 + x * kTileU + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s,
-                 k > 0);
-        mma_commit(&s_full[x]);
+          mma_ss(tmem, dQ + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s, k > 0);
+        mma_commit(&s_full);
       };
-      auto in_range = [&](int x, int n) {
-        const int a = lo + n;
-        return kr[x].num > 0 && a >= kr[x].lo && a < kr[x].lo + kr[x].num;
-      };
-      // First S of every tile whose first key tile is within the ring's reach; a
-      // tile that starts later gets it at the top of its first step.
-      bool started[kFwdTiles];
-      #pragma unroll
-      for (int x = 0; x < kFwdTiles; ++x) {
-        started[x] = false;
-        if (ok && kr[x].num > 0 && kr[x].lo - lo < kFwdStages) {
-          ok = kv_ready(kr[x].lo - lo);
-          if (ok) issue_s(x, kr[x].lo - lo);
-          started[x] = true;
-        }
-      }
+      if (ok) ok = kv_ready(0);
+      if (ok) issue_s(0);
       for (int n = 0; ok && n < num; ++n) {
         const int st = n % kFwdStages;
         // K/V of the next key tile (for S(n+1)); V(n) was waited with K(n).
         if (n + 1 < num && !kv_ready(n + 1)) { ok = false; break; }
+        if (!mbar_wait(&p_full, n & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
         #pragma unroll
-        for (int x = 0; x < kFwdTiles; ++x) {
-          if (!in_range(x, n)) continue;
-          const int local = lo + n - kr[x].lo;
-          if (!started[x]) {
-            issue_s(x, n);
-            started[x] = true;
-          }
-          if (!mbar_wait(&p_full[x], local & 1, &abort_flag)) { ok = false; break; }
-          tc_fence_after();
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t tP = tmem + 64 * c;   // P_c over S
+          const uint32_t tO = tmem + kFwdColO + 64 * c;
           #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t tP = tmem + x * 128 + 64 * c;   // P_xc over S_x
-            const uint32_t tO = tmem + 256 + x * 128 + 64 * c;
-            #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ts(tO, tP + 8 * k, dV0 + st * kTileU + c * kHalfU + 128 * k, idesc_o,
-                     (local > 0 || k > 0));
-          }
-          if (local == kr[x].num - 1) {
-            mma_commit(&pv_done[x][0]);
-            mma_commit(&pv_done[x][1]);
-          }
-          if (in_range(x, n + 1)) issue_s(x, n + 1);
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tO, tP + 8 * k, dV0 + st * kTileU + c * kHalfU + 128 * k, idesc_o,
+                   (n > 0 || k > 0));
         }
-        if (ok) mma_commit(&kv_empty[st]);
+        if (n == num - 1) {
+          mma_commit(&pv_done[0]);
+          mma_commit(&pv_done[1]);
+        } else {
+          issue_s(n + 1);
+        }
+        mma_commit(&kv_empty[st]);
       }
       if (!ok) {
         abort_flag = 1;
@@ -355,24 +312,19 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else {
     // ---------------------------------------------------------------- softmax warps
-    // Tile x = warp / 8, key half c = (warp / 4) & 1: S_x columns [64c, 64c+64).
-    // Thread = row = TMEM lane.  Each half keeps its own running max m, sum l and
-    // accumulator O_xc over the keys of its half, so the halves never wait for
-    // each other inside the loop; a row's two halves are merged once, in the
-    // epilogue (the same merge as two key blocks of a split softmax).
-    const int x = warp >> 3;
-    const int c = (warp >> 2) & 1;
+    // Key half c = warp / 4: S columns [64c, 64c+64).  Thread = row = TMEM lane.
+    // Each half keeps its own running max m, sum l and accumulator O_c over the
+    // keys of its half, so the halves never wait for each other inside the loop;
+    // a row's two halves are merged once, in the epilogue (the same merge as two
+    // key blocks of a split softmax).
+    const int c = warp >> 2;
     const int r = tid & 127;
-    const int i = i0 + x * kBlockM + r;      // row within the sequence
-    const KeyRange kx = x == 0 ? kr_a : kr_b;
+    const int i = i0 + r;                    // row within the sequence
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + 64 * c + lane_base;
-    const uint32_t tP = tS;                                     // P over S_xc
-    const uint32_t tOx = tmem + 256 + x * 128 + lane_base;      // O_x0; O_x1 at +64
-    const uint32_t tO = tOx + 64 * c;
-    const uint32_t bar_id = 1 + x;
-    const int tile_r0 = i0 + x * kBlockM;
-    const int tile_r1 = min(tile_r0 + kBlockM, sp.nq) - 1;
+    const uint32_t tS = tmem + 64 * c + lane_base;
+    const uint32_t tP = tS;                                     // P over S_c
+    const uint32_t tO0 = tmem + kFwdColO + lane_base;           // O_0; O_1 at +64
+    const uint32_t tO = tO0 + 64 * c;
     const bool sink_finite = sink_h > -INFINITY;
     // running max (log2 domain) starts at the sink logit in both halves; the
     // sink's term of the sum (1 at m = sink log2 e) is counted in half 0 only
@@ -382,12 +334,12 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
     bool ok = true;
-    for (int it = 0; it < kx.num; ++it) {
-      if (!mbar_wait_warp(&s_full[x], it & 1, &abort_flag)) { ok = false; break; }
+    for (int it = 0; it < num; ++it) {
+      if (!mbar_wait_warp(&s_full, it & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const int j0 = (kx.lo + it) * kBlockN + 64 * c;          // first key of this half
+      const int j0 = (lo + it) * kBlockN + 64 * c;              // first key of this half
       const bool need_mask = (j0 + 64 > sp.nk) ||
-                             (p.causal && (j0 + 63 > tile_r0 + off ||
+                             (p.causal && (j0 + 63 > i0 + off ||
                                            (p.window > 0 && j0 <= tile_r1 + off - p.window)));
       // S of this half, read from TMEM once (each tcgen05.ld competes with the
       // MMAs for TMEM, so S is not read a second time for the exponentials).
@@ -419,8 +371,8 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         alpha = ex2_approx(m - mx);
         m = mx;
       }
-      // S_x(it) completing implies PV_xc(it - 1) completed (issued before it by
-      // the same thread): O_xc may be rescaled and P_xc overwritten.
+      // S(it) completing implies PV_c(it - 1) completed (issued before it by the
+      // same thread): O_c may be rescaled and P_c overwritten.
       if (it > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         #pragma unroll
         for (int q = 0; q < 64; q += 16) {
@@ -433,7 +385,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       }
       // P = exp2(S * scale * log2 e - m), fp16, over the first 32 columns of this
-      // half of S_x (already read into registers).
+      // half of S (already read into registers).
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       float rs0 = 0.0f, rs1 = 0.0f;
       #pragma unroll
@@ -452,40 +404,36 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       l = l * alpha + (rs0 + rs1);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[x]);
+      mbar_arrive(&p_full);
     }
-    // Both halves' last PV have landed in O_x0 / O_x1.
+    // Both halves' last PV have landed in O_0 / O_1.
     bool fin = ok;
-    if (fin && kx.num > 0)
-      fin = mbar_wait_warp(&pv_done[x][0], 0, &abort_flag) &&
-            mbar_wait_warp(&pv_done[x][1], 0, &abort_flag);
-    s_red_m[x][c][r] = m;
-    s_red_l[x][c][r] = l;
-    fin = named_barrier_and(bar_id, 2 * kBlockM, fin);
+    if (fin)
+      fin = mbar_wait_warp(&pv_done[0], 0, &abort_flag) &&
+            mbar_wait_warp(&pv_done[1], 0, &abort_flag);
+    s_red_m[c][r] = m;
+    s_red_l[c][r] = l;
+    fin = named_barrier_and(1, 2 * kBlockM, fin);
     if (!fin) {
       abort_flag = 1;
       atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 3);
     } else {
       tc_fence_after();
       // merge the halves: m_t = max(m_0, m_1), weights 2^(m_c - m_t)
-      const float m0 = s_red_m[x][0][r], m1 = s_red_m[x][1][r];
+      const float m0 = s_red_m[0][r], m1 = s_red_m[1][r];
       const float mt = fmaxf(m0, m1);
       const float w0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - mt);
       const float w1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - mt);
-      const float lt = s_red_l[x][0][r] * w0 + s_red_l[x][1][r] * w1;
+      const float lt = s_red_l[0][r] * w0 + s_red_l[1][r] * w1;
       const float inv_l = (lt > 0.0f) ? 1.0f / lt : 0.0f;
       const bool valid = i < sp.nq;
       const size_t row = (size_t)(sp.q0 + i);
-      // this half writes output columns [32c, 32c + 32)
+      // this half writes output columns [32c, 32c + 32); the loads run with the
+      // whole warp (rows past the tail included), only the stores are guarded
       uint32_t o0[32], o1[32];
-      if (kx.num > 0) {
-        tmem_ld_x32(tOx + 32 * c, o0);
-        tmem_ld_x32(tOx + 64 + 32 * c, o1);
-        tmem_ld_wait();
-      } else {
-        #pragma unroll
-        for (int e = 0; e < 32; ++e) { o0[e] = 0u; o1[e] = 0u; }
-      }
+      tmem_ld_x32(tO0 + 32 * c, o0);
+      tmem_ld_x32(tO0 + 64 + 32 * c, o1);
+      tmem_ld_wait();
       if (valid) {
         const float s0 = w0 * inv_l, s1 = w1 * inv_l;
         const size_t base = (row * p.heads_q + h) * kHeadDim + 32 * c;
@@ -494,17 +442,17 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float f[8];
-          uint32_t hi[4], lo[4];
+          uint32_t hi[4], lo2[4];
           #pragma unroll
           for (int e = 0; e < 8; ++e)
             f[e] = __uint_as_float(o0[8 * u + e]) * s0 + __uint_as_float(o1[8 * u + e]) * s1;
           #pragma unroll
           for (int e = 0; e < 4; ++e) {
             hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-            lo[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
+            lo2[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
           }
           dst[u] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          if (dlo) dlo[u] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          if (dlo) dlo[u] = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
         }
         if (c == 0)
           p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (mt + __log2f(lt)) * kLn2 : -INFINITY;
@@ -516,7 +464,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   __syncthreads();
   if (warp == kFwdMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kFwdTmemCols);
   }
 }
 

@@ -36,6 +36,10 @@ SMALL = [
     ("g1_window1", 2, 2, [300, 3], True, 1),
     ("g2_window128", 4, 2, [385], True, 128),
     ("g2_window129", 4, 2, [385, 130], True, 129),
+    # windows that give a 128-row tile three key tiles, so the forward's
+    # two-stage K/V ring wraps (256: the tiles just fit; 257: one more key)
+    ("g4_window256", 8, 2, [700, 129], True, 256),
+    ("g2_window257", 4, 2, [700], True, 257),
     ("noncausal", 2, 2, [129, 64, 1], False, 0),
     ("g8_long", 16, 2, [700], True, 0),
 ]
@@ -55,16 +59,18 @@ def test_dense_batch_layout():
     check_against(run_gpu(c, dense=True), _ref(c))
 
 
-@pytest.mark.parametrize("causal", [True, False])
-def test_different_query_and_key_lengths(causal):
+@pytest.mark.parametrize("causal,window", [(True, 0), (False, 0), (True, 100)])
+def test_different_query_and_key_lengths(causal, window):
     """N_q != N_k per sequence (bottom-right causal), including a sequence whose
-    first query rows see no key (N_q > N_k) and an empty query sequence."""
+    first query rows see no key (N_q > N_k) and an empty query sequence; with
+    and without a window."""
     lq, lk = [100, 64, 0, 130], [150, 10, 40, 130]
     cq, ck = [0], [0]
     for a, b in zip(lq, lk):
         cq.append(cq[-1] + a)
         ck.append(ck[-1] + b)
-    w = small_workload("qk", 421 + causal, 4, 2, [sum(lq)], causal=causal)
+    w = small_workload("qk", 421 + causal + 2 * (window > 0), 4, 2, [sum(lq)], causal=causal,
+                       window=window)
     c = make_case(w)
     g = torch.Generator().manual_seed(4242)
     k = torch.randn((sum(lk), 2, 64), generator=g).to(torch.bfloat16)
