@@ -18,7 +18,9 @@
 //                 dQ   = dS K         (A = dS^T read MN-major, once per step)
 //               Two compute warpgroups own one query half each, so the tensor
 //               cores run one half's products while the other half's exponentials
-//               are computed.  dK and dV stay in TMEM for the whole loop; a
+//               are computed; two threads issue the MMAs (S^T, dP^T, dV / dK, dQ)
+//               so that one's waits do not idle the tensor pipe.  dK and dV stay
+//               in TMEM for the whole loop; a
 //               dedicated warpgroup moves each step's dQ from TMEM into a
 //               swizzled shared-memory tile that a TMA reduce-add sums into
 //               the fp32 accumulator.
@@ -32,11 +34,13 @@
 namespace attn_sink {
 
 constexpr int kBwdStages = 2;
-// warps 0-3 compute queries 0-63 of a step, 4-7 queries 64-127, 8 TMA, 9 MMA, 10-13 dQ
-constexpr int kBwdThreads = 448;
+// warps 0-3 compute queries 0-63 of a step, 4-7 queries 64-127, 8 TMA, 9 MMA issuer A
+// (S^T, dP^T, dV), 10-13 dQ, 14 MMA issuer B (dK, dQ)
+constexpr int kBwdThreads = 480;
 constexpr int kBwdProducerWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdDqWarp0 = 10;
+constexpr int kBwdMma2Warp = 14;
 constexpr int kPreRows = 128;      // rows per bwd_pre CTA
 constexpr uint32_t kDqStageBytes = kBlockM * kHeadDim * 4;   // 32 KB fp32 dQ tile
 // K, V, kBwdStages x (Q, dO), 2 x dS^T, the dQ staging tile
@@ -334,7 +338,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
-  __shared__ __align__(8) uint64_t s_full[2], p_full[2];
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2], ds_free[2];
   __shared__ float2 s_LD[kBwdStages][kBlockM];    // (lse * log2 e, D) of the step's rows
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -390,11 +394,12 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     mbar_init(&kv_full, 1);
     mbar_init(&kv_tmem, 2 * kBlockN);
     mbar_init(&mma2_done, 1);
-    mbar_init(&drained, 1);
+    mbar_init(&drained, 2);               // one commit from each MMA issuer
     for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 lanes' cp.async (lse / D)
-      mbar_init(&q_empty[s], 1);
+      mbar_init(&q_empty[s], 2);          // read by both issuers' MMAs
     }
+    for (int b = 0; b < 2; ++b) mbar_init(&ds_free[b], 1);   // dS^T buffer b read
     for (int hh = 0; hh < 2; ++hh) {
       mbar_init(&s_full[hh], 1);
       // half 1 also waits for the dQ warps to have read the previous dQ out of
@@ -457,9 +462,18 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       for (int m = max(0, issued - kBwdStages); m < issued; ++m)
         mbar_wait(&q_full[m % kBwdStages], (m / kBwdStages) & 1, nullptr);
     }
-  } else if (warp == kBwdMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == kBwdMmaWarp || warp == kBwdMma2Warp) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Two issuing threads, so that one issuer's mbarrier waits (each leaves the
+    // tensor pipe idle for ~200 cycles) are covered by the other's MMAs.  Each
+    // accumulator has one issuer, whose MMAs run in issue order:
+    //   A (warp 9):  S^T / dP^T of every half, dV += P^T dO
+    //   B (warp 14): dK += dS^T Q, dQ = dS K
+    // A reads only TMEM-resident P^T and the Q / dO stage; B reads the dS^T SMEM
+    // buffer and the Q stage.  A stage is refilled once both issuers' commits on
+    // q_empty have landed; B's commit on ds_free[b] releases dS^T buffer b.
     if (lane == 0) {
+      const bool issuer_a = warp == kBwdMmaWarp;
       const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM / 2, false, false);
       const uint32_t id_dvdk = make_idesc(kFmtF16, kBlockN, kHeadDim, false, true);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
@@ -484,49 +498,62 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           mma_ts(tmem + kColDPT + 64 * hh, tmem + kColV + 8 * k, dO_k + qo + 2 * k, id_s, k > 0);
         mma_commit(&s_full[hh]);
       };
-      // kv_tmem: K and V are in TMEM (the compute warps copied them from SMEM)
-      bool ok = mbar_wait(&kv_tmem, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(0, 1);
+      bool ok = true;
+      if (issuer_a) {
+        // kv_tmem: K and V are in TMEM (the compute warps copied them from SMEM)
+        ok = mbar_wait(&kv_tmem, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          issue_s(0, 1);
+        }
       }
       for (int m = 0; ok && m < num; ++m) {
         const int st = m % kBwdStages;
         const uint32_t so = (m & 1) * kPTileU;            // dS^T buffer of this step
         const bool more = m + 1 < num;
         for (int hh = 0; hh < 2; ++hh) {
+          // p_full[hh]: this half's P^T is in TMEM and its dS^T in SMEM (for half
+          // 1 also: the dQ warps have read the previous dQ out of TMEM)
           if (!mbar_wait(&p_full[hh], m & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
-          // dV += P^T dO and dK += dS^T Q over this half's 64 queries (K = 64);
-          // B operands step 16 query rows (2048 bytes) per k.
+          // B operands step 16 query rows (2048 bytes) per k (K = 64 queries)
           const uint32_t ho = st * kTileU + hh * (kTileU / 2);
-          #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kColDV, tmem + kColST + 64 * hh + 8 * k, dO_mn + ho + 128 * k,
-                   id_dvdk, (m > 0 || hh > 0 || k > 0));
-          #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + kColDK, dS_k + so + hh * kTileU + 2 * k, dQ_mn + ho + 128 * k,
-                   id_dvdk, (m > 0 || hh > 0 || k > 0));
-          if (hh == 1) {
-            if (!p.skip_dq) {
-              // p_full[1](m) included the dQ warps' arrival: dQ(m - 1) is read
-              // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
-              #pragma unroll
-              for (int k = 0; k < kBlockN / 16; ++k)
-                mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
-              mma_commit(&mma2_done);
+          if (issuer_a) {
+            // dV += P^T dO over this half's 64 queries
+            #pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(tmem + kColDV, tmem + kColST + 64 * hh + 8 * k, dO_mn + ho + 128 * k,
+                     id_dvdk, (m > 0 || hh > 0 || k > 0));
+            if (hh == 1) mma_commit(&q_empty[st]);
+            if (more) {
+              // next step's half hh: its S^T / dP^T columns were read by this half
+              // (Q / dO of the next step are waited for once, before its half 0)
+              if (hh == 0 && !mbar_wait(&q_full[(m + 1) % kBwdStages],
+                                        ((m + 1) / kBwdStages) & 1, &abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(m + 1, hh);
             }
-            mma_commit(&q_empty[st]);
-          }
-          if (more) {
-            // next step's half hh: its S^T / dP^T columns were read by this half
-            // (Q / dO of the next step are waited for once, before its half 0)
-            if (hh == 0 && !mbar_wait(&q_full[(m + 1) % kBwdStages], ((m + 1) / kBwdStages) & 1,
-                                      &abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(m + 1, hh);
+          } else {
+            // dK += dS^T Q over this half's 64 queries
+            #pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + kColDK, dS_k + so + hh * kTileU + 2 * k, dQ_mn + ho + 128 * k,
+                     id_dvdk, (m > 0 || hh > 0 || k > 0));
+            if (hh == 1) {
+              if (!p.skip_dq) {
+                // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
+                #pragma unroll
+                for (int k = 0; k < kBlockN / 16; ++k)
+                  mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
+                mma_commit(&mma2_done);
+              }
+              mma_commit(&ds_free[m & 1]);
+              mma_commit(&q_empty[st]);
+            }
           }
         }
       }
@@ -534,6 +561,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         abort_flag = 1;
         atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 2);
       }
+      // both issuers commit once; `drained` completes when all their MMAs have
       mma_commit(&drained);
       mbar_wait(&drained, 0, nullptr);
     }
@@ -571,10 +599,16 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const int st = m % kBwdStages;
       const int i0 = (qt_first + m % nqt) * kBlockM + 64 * hh;   // first query of this half
       // q_full: the producer's lse / D rows of this step are in SMEM.
-      // s_full: this half's S^T / dP^T, and every earlier MMA (the readers of
-      // the P^T half and of this step's dS^T buffer) has completed.
+      // s_full: this half's S^T / dP^T, and every earlier MMA of issuer A (dV,
+      // the reader of the P^T half) has completed.
+      // ds_free: issuer B's MMAs of step m - 2 (the last readers of this step's
+      // dS^T buffer) have completed; buffer m & 1 is released once per two steps.
       if (!mbar_wait_warp(&q_full[st], (m / kBwdStages) & 1, &abort_flag) ||
-          !mbar_wait_warp(&s_full[hh], m & 1, &abort_flag)) { ok = false; break; }
+          !mbar_wait_warp(&s_full[hh], m & 1, &abort_flag) ||
+          (m >= 2 && !mbar_wait_warp(&ds_free[m & 1], ((m >> 1) - 1) & 1, &abort_flag))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const bool need_mask = (j0 + kBlockN > sp.nk) || (i0 + 64 > sp.nq) ||
                              (p.causal && (j0 + kBlockN - 1 > i0 + off ||
@@ -628,7 +662,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         store_kv_grad_row(p, part, (size_t)(sp.k0 + j), g, which, v,
                           which == 0 ? p.scale : 1.0f);
     }
-  } else if (warp >= kBwdDqWarp0) {
+  } else if (warp >= kBwdDqWarp0 && warp < kBwdDqWarp0 + 4) {
     // ---------------------------------------------------------------- dQ warps
     // Each step's dQ tile (128 queries x 64, fp32, times the softmax scale) is
     // staged in SMEM (two 128-byte-swizzled halves of 32 columns) and added to the
