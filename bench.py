@@ -66,9 +66,11 @@ def algorithmic(w, lengths):
                  bwd_bytes=bwd_bytes)
 
 
+# the kernel's own code and the host code that picks its launch shape (grid,
+# GQA split), both of which decide its DRAM traffic
 KERNEL_SOURCES = {
-    "attn_sink_fwd_kernel": ("fwd_kernel.cuh", "sm103_ptx.cuh"),
-    "attn_sink_bwd_main_kernel": ("bwd_kernel.cuh", "sm103_ptx.cuh"),
+    "attn_sink_fwd_kernel": ("fwd_kernel.cuh", "sm103_ptx.cuh", "attn_sink_api.cu"),
+    "attn_sink_bwd_main_kernel": ("bwd_kernel.cuh", "sm103_ptx.cuh", "attn_sink_api.cu"),
 }
 
 
