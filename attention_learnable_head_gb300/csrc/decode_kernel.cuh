@@ -11,13 +11,20 @@
 // Split-KV: CTA (split, kv head g, sequence b) attends the G = H_q / H_kv
 // query heads of g to one slice of b's keys, without the sink, and writes the
 // slice's normalised result and log-sum-exp; attn_sink_merge_kernel then adds
-// the sink once (the merge of the key-chunk forward).  The work is a skinny
-// contraction (G <= 8 rows) meant to be bound by reading the cache: it runs on the
-// CUDA cores in fp32.  Each key is handled by 8 lanes, each holding 8 of the 64
-// dimensions (one 16-byte load of K and of V); the lanes of a key combine the
-// G dot products with three shuffles, and every lane keeps its own online
-// softmax state for its keys.  The 16 states of a CTA (4 warps x 4 keys in
-// flight) are merged through shared memory at the end.
+// the sink once (the merge of the key-chunk forward).
+//
+// The G query heads are the rows of a skinny product (G <= 8, padded to the 16
+// rows of a warp-level mma.sync m16n8k16; a tcgen05 MMA needs 64 or more rows).
+// Blocks of 64 keys of K and V are copied into swizzled shared memory with
+// cp.async (two stages, page by page through the block table, rows past the
+// slice or behind a bad table entry zero-filled and masked); each of the 4
+// warps takes 16 keys of a block:
+//   S = Q K^T   (bf16 operands: exact products, fp32 accumulators; K read with
+//                ldmatrix as the column-major B operand)
+//   online softmax per head row in fp32 (exp2 domain)
+//   O += P V    (P and V as fp16, like the prefill forward's P V product; V
+//                read with a transposing ldmatrix and converted from bf16)
+// The 4 warps' (m, l, O) states are merged through shared memory at the end.
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -25,10 +32,11 @@
 namespace attn_sink {
 
 constexpr int kDecThreads = 128;
+constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kDecMaxGroup = 8;        // query heads per kv head
-constexpr int kDecStates = kDecThreads / 8;   // key groups of 8 lanes per CTA
+constexpr int kDecKeys = 64;           // keys per stage: 16 per warp
+constexpr int kDecStages = 2;
 constexpr float kLn2Dec = 0.6931471805599453f;
-constexpr int kDecUnroll = 2;       // keys per key group whose loads are in flight together
 
 struct DecodeParams {
   const __nv_bfloat16* q;         // [B][H_q][64]
@@ -47,20 +55,22 @@ struct DecodeParams {
   float scale_log2;               // softmax_scale * log2(e)
 };
 
-// G = query heads per kv head (1, 2, 4 or 8), a compile-time constant so that
-// the G independent score / softmax chains of a key are interleaved.
+// G = query heads per kv head (1, 2, 4 or 8).
 template <int G>
 __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const DecodeParams p) {
-  __shared__ float s_m[kDecStates][G];
-  __shared__ float s_l[kDecStates][G];
-  __shared__ float s_o[kDecStates][G][64];
+  __shared__ __align__(128) uint8_t s_kv[kDecStages][2][kDecKeys * 128];   // K, V blocks
+  __shared__ uint8_t s_valid[kDecStages][kDecKeys];    // key inside the slice, page in range
+  __shared__ float s_m[kDecWarps][kDecMaxGroup];
+  __shared__ float s_l[kDecWarps][kDecMaxGroup];
+  __shared__ float s_o[kDecWarps][kDecMaxGroup][64];
 
   const int split = blockIdx.x;
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int tid = threadIdx.x;
-  const int state = tid >> 3;                  // key group of 8 lanes (0..15)
-  const int ds = tid & 7;                      // dimension slice: dims [8 ds, 8 ds + 8)
+  const int warp = tid >> 5, lane = tid & 31;
+  const int gr = lane >> 2;          // fragment row = query head of the group
+  const int t4 = lane & 3;           // fragment column pair
 
   // keys [lo, hi) of this sequence, then this split's slice of them
   int L = __ldg(p.seq_lens + b);
@@ -73,110 +83,165 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
   const int per = (L - lo + p.splits - 1) / p.splits;
   const int k0 = lo + split * per;
   const int k1 = min(L, k0 + per);
-
-  // the G query rows of kv head g, dims of this lane, pre-scaled to log2 units
-  float qv[G][8];
-  #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(
-        p.q + ((size_t)b * p.heads_q + g * G + h) * 64 + 8 * ds));
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      qv[h][2 * e] = bf16_lo(ww[e]) * p.scale_log2;
-      qv[h][2 * e + 1] = bf16_hi(ww[e]) * p.scale_log2;
-    }
-  }
-  float m[G], l[G], o[G][8];
-  #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
-    #pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] = 0.0f;
-  }
-
+  const int nblk = k1 > k0 ? (k1 - k0 + kDecKeys - 1) / kDecKeys : 0;
   const size_t row_stride = (size_t)p.heads_kv * 64;     // one key of the cache
-  // Each key group takes kDecUnroll keys per step and issues their loads before
-  // using them.  The trip count is the same for every lane of the CTA (k0, k1
-  // are), so the shuffles always run with the whole warp.  The softmax update is
-  // branch-free: a lane whose key is past the slice, or whose page entry is out
-  // of range, uses a score of -inf, which changes neither m, l nor o.
-  for (int jb = k0; jb < k1; jb += kDecUnroll * kDecStates) {
-    uint4 kw[kDecUnroll], vw[kDecUnroll];
-    bool valid[kDecUnroll];
-    #pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const int j = jb + u * kDecStates + state;
-      valid[u] = j < k1;
-      kw[u] = make_uint4(0, 0, 0, 0);
-      vw[u] = make_uint4(0, 0, 0, 0);
-      if (valid[u]) {
-        const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + j / p.page_size);
-        if (pg < 0 || pg >= p.num_pages) {                // bounds check of the table
-          if (ds == 0) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
-          valid[u] = false;
-        } else {
-          const size_t off =
-              ((size_t)pg * p.page_size + j % p.page_size) * row_stride + g * 64 + 8 * ds;
-          kw[u] = __ldg(reinterpret_cast<const uint4*>(p.k_cache + off));
-          vw[u] = __ldg(reinterpret_cast<const uint4*>(p.v_cache + off));
-        }
-      }
-    }
-    #pragma unroll
-    for (int u = 0; u < kDecUnroll; ++u) {
-      const uint32_t kk[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
-      const uint32_t vv[4] = {vw[u].x, vw[u].y, vw[u].z, vw[u].w};
-      float kf[8], vf[8];
-      #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[2 * e] = bf16_lo(kk[e]);
-        kf[2 * e + 1] = bf16_hi(kk[e]);
-        vf[2 * e] = bf16_lo(vv[e]);
-        vf[2 * e + 1] = bf16_hi(vv[e]);
-      }
-      float sc[G];
-      #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float s0 = qv[h][0] * kf[0], s1 = qv[h][1] * kf[1];
-        #pragma unroll
-        for (int e = 2; e < 8; e += 2) {
-          s0 = fmaf(qv[h][e], kf[e], s0);
-          s1 = fmaf(qv[h][e + 1], kf[e + 1], s1);
-        }
-        sc[h] = s0 + s1;
-      }
-      // the key's 8 lanes are consecutive: xor 1, 2, 4 stays within them
-      #pragma unroll
-      for (int x = 1; x < 8; x <<= 1) {
-        #pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], x);
-      }
-      #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float sv = valid[u] ? sc[h] : -INFINITY;
-        const float mn = fmaxf(m[h], sv);                 // online softmax, log2 units
-        const float mb = (mn == -INFINITY) ? 0.0f : mn;
-        const float alpha = ex2_approx(m[h] - mb);        // 0 while m is -inf
-        const float pe = ex2_approx(sv - mb);             // 0 for an invalid key
-        l[h] = fmaf(l[h], alpha, pe);
-        #pragma unroll
-        for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * alpha);
-        m[h] = mn;
-      }
+
+  // Q as the A operand (rows >= G are zero): a0 = dims 16 kk + 2 t4 .. + 1,
+  // a2 = the same + 8, of head row gr; a1 = a3 = 0 (rows 8..15).
+  uint32_t qa0[4], qa2[4];
+  #pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    qa0[kk] = 0u;
+    qa2[kk] = 0u;
+    if (gr < G) {
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+          p.q + ((size_t)b * p.heads_q + g * G + gr) * 64 + 16 * kk + 2 * t4);
+      qa0[kk] = __ldg(qp);
+      qa2[kk] = __ldg(qp + 4);
     }
   }
 
-  // merge the 16 key-group states of the CTA
+  // Block `blk` of the slice into stage `st`: 64 keys x (K, V) x 8 chunks of 16
+  // bytes, 8 per thread.  A key past the slice, or whose table entry is out of
+  // range (reported, nothing read), is zero-filled and marked invalid.
+  auto load_block = [&](int blk, int st) {
+    const int base = k0 + blk * kDecKeys;
+    #pragma unroll
+    for (int i = 0; i < (2 * kDecKeys * 8) / kDecThreads; ++i) {
+      const int q = tid + kDecThreads * i;
+      const int kv = q / (kDecKeys * 8);
+      const int key = (q >> 3) & (kDecKeys - 1);
+      const int c = q & 7;
+      const int j = base + key;
+      const __nv_bfloat16* cache = kv ? p.v_cache : p.k_cache;
+      const __nv_bfloat16* src = p.q;        // read by no copy (0 bytes): any valid address
+      uint32_t bytes = 0;
+      bool valid = false;
+      if (j < k1) {
+        const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + j / p.page_size);
+        valid = pg >= 0 && pg < p.num_pages;
+        if (valid) {
+          src = cache + ((size_t)pg * p.page_size + j % p.page_size) * row_stride + g * 64 + 8 * c;
+          bytes = 16;
+        } else if (kv == 0 && c == 0) {
+          atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
+        }
+      }
+      if (kv == 0 && c == 0) s_valid[st][key] = valid ? 1 : 0;
+      cp_async_16_zfill(smem_u32(&s_kv[st][kv][0]) + sw128_offset(key, c), src, bytes);
+    }
+    cp_async_commit();
+  };
+
+  float m_r = -INFINITY;   // running max of head row gr (log2 units)
+  float l_r = 0.0f;        // this thread's share of the row sum
+  float oacc[8][4];        // O: n-tile nd = dims 8 nd .. 8 nd + 7 (c0, c1: row gr)
   #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    if (ds == 0) {
-      s_m[state][h] = m[h];
-      s_l[state][h] = l[h];
+  for (int nd = 0; nd < 8; ++nd) {
+    #pragma unroll
+    for (int e = 0; e < 4; ++e) oacc[nd][e] = 0.0f;
+  }
+  bool overflow = false;
+  const int mi = lane >> 3, ri = lane & 7;   // ldmatrix: matrix and row this lane addresses
+  const int kb = 16 * warp;                  // this warp's keys within a block
+
+  if (nblk > 0) load_block(0, 0);
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int st = blk & 1;
+    if (blk + 1 < nblk) {
+      load_block(blk + 1, st ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t kt = smem_u32(&s_kv[st][0][0]);
+    const uint32_t vt = smem_u32(&s_kv[st][1][0]);
+
+    // S = Q K^T for keys kb .. kb + 15 (n-tiles of 8 keys); matrices of the x4
+    // load: (keys +0, dims 16 kk), (keys +0, dims +8), (keys +8, ...), (keys +8, +8)
+    float sc[2][4];
+    #pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      #pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = 0.0f;
     }
     #pragma unroll
-    for (int e = 0; e < 8; ++e) s_o[state][h][8 * ds + e] = o[h][e];
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t b00, b01, b10, b11;
+      ldmatrix_x4(kt + sw128_offset(kb + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10,
+                  b11);
+      mma_16816_bf16(sc[0], qa0[kk], 0u, qa2[kk], 0u, b00, b01);
+      mma_16816_bf16(sc[1], qa0[kk], 0u, qa2[kk], 0u, b10, b11);
+    }
+
+    // online softmax of row gr over keys kb + 8 nt + 2 t4 + e (log2 units)
+    float x[2][2];
+    float mx = -INFINITY;
+    #pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      #pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool valid = s_valid[st][kb + 8 * nt + 2 * t4 + e] != 0;
+        x[nt][e] = valid ? sc[nt][e] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[nt][e]);
+      }
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m_r, mx);
+    const float mb = (mn == -INFINITY) ? 0.0f : mn;
+    const float alpha = ex2_approx(m_r - mb);            // 0 while m is -inf
+    float pv[2][2];
+    float rs = 0.0f;
+    #pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      #pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        pv[nt][e] = ex2_approx(x[nt][e] - mb);           // 0 for an invalid key
+        rs += pv[nt][e];
+      }
+    }
+    l_r = fmaf(l_r, alpha, rs);
+    m_r = mn;
+    #pragma unroll
+    for (int nd = 0; nd < 8; ++nd) {
+      oacc[nd][0] *= alpha;
+      oacc[nd][1] *= alpha;
+    }
+    // P as the A operand: a0 = keys 2 t4 .. + 1, a2 = keys 8 + 2 t4 .. + 1
+    const uint32_t pa0 = pack_f16x2(pv[0][0], pv[0][1]);
+    const uint32_t pa2 = pack_f16x2(pv[1][0], pv[1][1]);
+
+    // O += P V; transposed x4 load matrices: (keys +0, dims 16 u), (keys +8,
+    // dims 16 u), (keys +0, dims +8), (keys +8, dims +8)
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint32_t v0, v1, v2, v3;
+      ldmatrix_x4_trans(vt + sw128_offset(kb + (mi & 1) * 8 + ri, 2 * u + (mi >> 1)), v0, v1,
+                        v2, v3);
+      mma_16816_f16(oacc[2 * u], pa0, 0u, pa2, 0u, bf16x2_to_f16x2(v0, &overflow),
+                    bf16x2_to_f16x2(v1, &overflow));
+      mma_16816_f16(oacc[2 * u + 1], pa0, 0u, pa2, 0u, bf16x2_to_f16x2(v2, &overflow),
+                    bf16x2_to_f16x2(v3, &overflow));
+    }
+    __syncthreads();   // every warp is done with stage st before it is refilled
+  }
+  if (overflow) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
+
+  // the row sum over the 4 lanes of row gr, then the 4 warps' states merged
+  l_r += __shfl_xor_sync(0xffffffffu, l_r, 1);
+  l_r += __shfl_xor_sync(0xffffffffu, l_r, 2);
+  if (gr < G) {
+    if (t4 == 0) {
+      s_m[warp][gr] = m_r;
+      s_l[warp][gr] = l_r;
+    }
+    #pragma unroll
+    for (int nd = 0; nd < 8; ++nd) {
+      s_o[warp][gr][8 * nd + 2 * t4] = oacc[nd][0];
+      s_o[warp][gr][8 * nd + 2 * t4 + 1] = oacc[nd][1];
+    }
   }
   __syncthreads();
   // thread t: head t / 16, dims 4 (t % 16) .. + 4
@@ -184,15 +249,15 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
   const int d0 = 4 * (tid & 15);
   if (h < G) {
     float mm = -INFINITY;
-    for (int st = 0; st < kDecStates; ++st) mm = fmaxf(mm, s_m[st][h]);
+    for (int w = 0; w < kDecWarps; ++w) mm = fmaxf(mm, s_m[w][h]);
     float ll = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (mm > -INFINITY) {
-      for (int st = 0; st < kDecStates; ++st) {
-        if (s_m[st][h] == -INFINITY) continue;
-        const float w = ex2_approx(s_m[st][h] - mm);
-        ll = fmaf(w, s_l[st][h], ll);
+      for (int w = 0; w < kDecWarps; ++w) {
+        if (s_m[w][h] == -INFINITY) continue;
+        const float wt = ex2_approx(s_m[w][h] - mm);
+        ll = fmaf(wt, s_l[w][h], ll);
         #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = fmaf(w, s_o[st][h][d0 + e], acc[e]);
+        for (int e = 0; e < 4; ++e) acc[e] = fmaf(wt, s_o[w][h][d0 + e], acc[e]);
       }
     }
     const float inv = (ll > 0.0f) ? 1.0f / ll : 0.0f;

@@ -195,8 +195,10 @@ size_t attn_sink_decode_workspace_size(const attn_sink_decode_params* params);
  * seq_lens [B] int32, the cached keys of each sequence including the new
  * token's own (appended before the call); sink [H_q] fp32.  Writes out
  * [B, H_q, 64] bf16, optional out_residual (as attn_sink_fwd) and lse [H_q, B]
- * fp32; a sequence with no cached key gets out = 0, lse = sink.  The scores,
- * softmax and P v run in fp32 (no fp16 rounding of P).  Block-table entries
+ * fp32; a sequence with no cached key gets out = 0, lse = sink.  The scores
+ * multiply the bf16 inputs exactly with fp32 accumulation and the softmax runs
+ * in fp32; P and v enter the P v product as fp16, as in attn_sink_fwd (v values
+ * outside the fp16 range are reported as 0x400).  Block-table entries
  * and lengths are checked on the device (see attn_sink_device_error).  All
  * pointers are device pointers, 16-byte aligned where they hold bf16 rows;
  * the workspace is 256-byte aligned and at least
