@@ -476,8 +476,11 @@ struct DecodeLayout {
   size_t off_lo, off_lse, total;
 };
 
-// Key splits: enough (batch x kv head x split) CTAs to fill the GPU twice,
-// each split at least 256 keys of the longest possible sequence, at most 64.
+// Key splits: enough (batch x kv head x split) CTAs for about eight waves of
+// the five decode CTAs an SM holds at once (fewer waves leave a part-filled
+// last wave and too few copies in flight: measured, 40 x SMs beat 2, 8 and 20
+// x SMs), each split at least 256 keys of the longest possible sequence, at
+// most 64.
 bool decode_layout(const attn_sink_decode_params* p, int sm_count, DecodeLayout* L) {
   if (p == nullptr || p->batch < 0 || p->heads_kv < 1 || p->heads_q < 1 ||
       p->heads_q % p->heads_kv != 0 || !decode_group_ok(p->heads_q / p->heads_kv) ||
@@ -489,7 +492,7 @@ bool decode_layout(const attn_sink_decode_params* p, int sm_count, DecodeLayout*
   const long long ctas = (long long)p->batch * p->heads_kv;
   const long long keys = (p->window > 0) ? std::min<long long>(cap, p->window) : cap;
   long long s = 1;
-  if (ctas > 0) s = std::max<long long>(1, (2ll * sm_count + ctas - 1) / ctas);
+  if (ctas > 0) s = std::max<long long>(1, (40ll * sm_count + ctas - 1) / ctas);
   s = std::min<long long>(s, std::max<long long>(1, (keys + 255) / 256));
   s = std::min<long long>(s, 64);
   L->splits = (int)s;
