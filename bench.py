@@ -6,6 +6,7 @@ H_q=64, H_kv=8, d=64, N=4096, causal).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU float64 oracle, on host cores
+  python bench.py --decode [--steps K] [--warmup W]   # the paged decode step
 
 Timing: CUDA events on the launching stream around the fwd and bwd calls of
 each step, and (recorded by the library on the same stream) around each launch
@@ -261,6 +262,97 @@ def run_reference(args, w, case):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- decode
+DECODE_METRIC = "paged decode: KV-cache GB/s read on 1 GB300; % of measured HBM copy bandwidth"
+
+
+def decode_case(batch: int, cached: int, heads_q: int, heads_kv: int, page: int, seed: int):
+    """Seeded serving-shaped decode inputs on the host: every sequence holds
+    `cached` keys in pages of `page` keys, the pool's pages handed out in a
+    random order (as an allocator that has been running a while would)."""
+    g = torch.Generator().manual_seed(seed)
+    per_seq = (cached + page - 1) // page
+    n_pages = batch * per_seq
+    kc = torch.randn(n_pages, page, heads_kv, 64, generator=g).to(torch.bfloat16)
+    vc = torch.randn(n_pages, page, heads_kv, 64, generator=g).to(torch.bfloat16)
+    table = torch.randperm(n_pages, generator=g).to(torch.int32).view(batch, per_seq)
+    lens = torch.full((batch,), cached, dtype=torch.int32)
+    q = torch.randn(batch, heads_q, 64, generator=g).to(torch.bfloat16)
+    sink = torch.randn(heads_q, generator=g)
+    return q, kc, vc, table, lens, sink
+
+
+def run_decode(args):
+    """One step = attn_sink_decode (the split kernel and the sink merge) for a
+    batch of 128 sequences with 8192 cached keys each, H 64/8, page 16.  The
+    cache (2.1 GB) is larger than L2, so no flush is needed between steps."""
+    from attention_learnable_head_gb300 import binding
+    from attention_learnable_head_gb300.build import build
+    B, L, HQ, HKV, PAGE, SCALE = 128, 8192, 64, 8, 16, 0.125
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    host = decode_case(B, L, HQ, HKV, PAGE, seed=4242)
+    q, kc, vc, table, lens, sink = (t.to(dev) for t in host)
+    cache_bytes = 2 * B * L * HKV * 64 * 2
+    alg_bytes = cache_bytes + table.numel() * 4 + q.numel() * 2 * 2 + HQ * B * 4
+    step = lambda: binding.decode(q, kc, vc, table, lens, sink, softmax_scale=SCALE)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches = count_launches(binding, step)
+    clocks = ClockSampler(0)
+    clocks.start()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    clock = clocks.stop()
+    st, code = binding.attn_sink_device_error()
+    if st != 0 or code != 0:
+        raise RuntimeError(f"device error word {code:#x} after the decode steps")
+    ms = statistics.median(times)
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    line = {
+        "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "decode_serving", "batch": B, "cached_keys": L, "heads_q": HQ,
+                   "heads_kv": HKV, "head_dim": 64, "page_size": PAGE, "window": 0,
+                   "l2": "inputs larger than L2 (2.1 GB of cache), no flush"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_note": f"{src} copy bandwidth; achieved = algorithmic bytes "
+                                  f"(cache {cache_bytes} + q, out, lse, block table) / step time"},
+        "gpu_launches": launches * args.steps, "gpu_launches_per_step": launches,
+        "clocks": clock,
+    }
+    if not args.no_cpu_baseline:
+        from oracle.decode import oracle_decode  # test infrastructure: only this leg runs it
+        torch.set_num_threads(os.cpu_count() or 1)
+        hq, hkc, hvc, htable, hlens, hsink = host
+        done, t0 = 0, time.perf_counter()
+        while done < B:
+            idx = torch.tensor([done])
+            oracle_decode(hq[idx], hkc, hvc, htable[idx], hlens[idx], hsink, scale=SCALE)
+            done += 1
+            if time.perf_counter() - t0 >= args.cpu_budget:
+                break
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": done * (cache_bytes / B) / dt / 1e9, "unit": "GB/s",
+            "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"decode_serving: sequences 0..{done - 1} of {B}, float64"}
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -277,9 +369,14 @@ def main():
     ap.add_argument("--ncu", action="store_true",
                     help="minimal run for a profiler: no e2e leg, no CPU baseline, no clock "
                          "sampling, no launch count")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the paged decode step instead (one JSON line of its own)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode:
+        run_decode(args)
+        return
 
     w = WORKLOADS[args.workload]
     case = make_case(w)
