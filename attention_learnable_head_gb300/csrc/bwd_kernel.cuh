@@ -403,7 +403,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     for (int hh = 0; hh < 2; ++hh) {
       mbar_init(&s_full[hh], 1);
       // half 1 also waits for the dQ warps to have read the previous dQ out of
-      // TMEM (they arrive on it), so the MMA thread needs no separate wait
+      // TMEM (they arrive on it), so the MMA issuers need no separate wait
       mbar_init(&p_full[hh], kBlockN + (hh == 1 && !p.skip_dq ? kBlockM : 0));
     }
     fence_mbarrier_init();
@@ -469,9 +469,9 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     // accumulator has one issuer, whose MMAs run in issue order:
     //   A (warp 9):  S^T / dP^T of every half, dV += P^T dO
     //   B (warp 14): dK += dS^T Q, dQ = dS K
-    // A reads only TMEM-resident P^T and the Q / dO stage; B reads the dS^T SMEM
-    // buffer and the Q stage.  A stage is refilled once both issuers' commits on
-    // q_empty have landed; B's commit on ds_free[b] releases dS^T buffer b.
+    // A reads K, V and P^T from TMEM and the Q / dO stage; B reads the dS^T SMEM
+    // buffer, the Q stage and K.  A stage is refilled once both issuers' commits
+    // on q_empty have landed; B's commit on ds_free[b] releases dS^T buffer b.
     if (lane == 0) {
       const bool issuer_a = warp == kBwdMmaWarp;
       const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM / 2, false, false);
