@@ -510,6 +510,7 @@ extern "C" {
 size_t attn_sink_decode_workspace_size(const attn_sink_decode_params* params) {
   DecodeLayout L;
   if (params == nullptr || params->head_dim != kHeadDim || params->batch == 0 ||
+      params->batch > 65535 || params->heads_kv > 65535 ||
       !decode_layout(params, sm_count_or_default(), &L))
     return 0;
   return L.total;
@@ -521,6 +522,8 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
                      void* workspace, size_t workspace_bytes, void* stream) {
   if (params == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
   if (params->head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
+  // launch-grid limits: kv heads in grid.y, sequences in grid.z
+  if (params->batch > 65535 || params->heads_kv > 65535) return ATTN_SINK_ERR_UNSUPPORTED;
   DecodeLayout L;
   if (!decode_layout(params, sm_count_or_default(), &L)) {
     if (params->heads_kv >= 1 && params->heads_q >= 1 &&
@@ -916,7 +919,10 @@ int attn_sink_device_error(void* stream, int* code) {
       return ATTN_SINK_ERR_CUDA;
   }
   *code = v;
-  return ATTN_SINK_OK;
+  // a kernel that gave up on a bounded wait (0x1xx forward, 0x2xx backward)
+  const int kind = v & 0xF00;
+  return (kind == DEVERR_TIMEOUT_FWD || kind == DEVERR_TIMEOUT_BWD) ? ATTN_SINK_ERR_TIMEOUT
+                                                                   : ATTN_SINK_OK;
 }
 
 }  // extern "C"

@@ -436,25 +436,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, for x <= 8 (the softmax exponents; anything below
-// -125, including -inf, returns 0).  Cody-Waite split
-// x = n + f with n = round(x) (the 1.5 * 2^23 add puts n in t's low mantissa
-// bits) and f in [-1/2, 1/2]; 2^f by a degree-3 polynomial whose coefficients
-// minimise the maximum relative error on [-1/2, 1/2] (fit_exp2.py: 7.5e-5,
-// below the fp16 rounding of P); 2^n is added into the exponent field.
-constexpr float kExp2C0 = 0.99992806f, kExp2C1 = 0.69326097f, kExp2C2 = 0.24261113f,
-                kExp2C3 = 0.05517167f;
-
-__device__ __forceinline__ float exp2_poly(float x) {
-  const float xc = fmaxf(x, -125.0f);
-  const float t = xc + 12582912.0f;
-  const float n = t - 12582912.0f;
-  const float f = xc - n;
-  const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, kExp2C0);
-  const float r = __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-  return x < -125.0f ? 0.0f : r;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.

@@ -17,6 +17,7 @@ large ones):
                    sink[h] drawn from {-30, -2, 0, 2, 8}
   5 long_full      B=4, H 64/8, N=16384, causal, q scaled by 3, sink ~ N(0, 2^2)
   5 long_window    same inputs, window 128
+  long_full_1seq / long_window_1seq: their first sequence alone (profiling)
 """
 from __future__ import annotations
 
@@ -65,6 +66,12 @@ WORKLOADS = {
                           sink_sigma=2.0),
     "long_window": Workload("long_window", 5, 64, 8, batch=4, seqlen=16384, window=128,
                             q_mult=3.0, sink_sigma=2.0),
+    # the first sequence of long_full alone (the same seeds, so the same first
+    # 16384 tokens): a profiler capture of one sequence stays a few GB
+    "long_full_1seq": Workload("long_full_1seq", 5, 64, 8, batch=1, seqlen=16384, q_mult=3.0,
+                               sink_sigma=2.0),
+    "long_window_1seq": Workload("long_window_1seq", 5, 64, 8, batch=1, seqlen=16384,
+                                 window=128, q_mult=3.0, sink_sigma=2.0),
 }
 
 

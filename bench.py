@@ -1,12 +1,15 @@
 """Throughput of attention with a learnable per-head sink, forward + backward.
 
 One step = attn_sink_fwd + attn_sink_bwd (through the C ABI) over one batch of
-the workload (default: the GPT-OSS-20B-shaped full-attention layer, B=1,
-H_q=64, H_kv=8, d=64, N=4096, causal).  Prints one JSON line.
+the workload (default: the long batch, B=4, N=16384, H_q=64, H_kv=8, d=64,
+causal, q scaled by 3, the largest single-GPU configuration).  Prints one
+JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU float64 oracle, on host cores
   python bench.py --decode [--steps K] [--warmup W]   # the paged decode step
+  python bench.py --record-traffic CSV --workload NAME [--traffic-scale X]
+      # store the DRAM bytes of an ncu capture in profiles/dram_traffic.json
 
 Timing: CUDA events on the launching stream around the fwd and bwd calls of
 each step, and (recorded by the library on the same stream) around each launch
@@ -91,23 +94,69 @@ def kernel_sources_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
 def dram_traffic(kernel: str, workload: str):
     """DRAM bytes (read + write) per launch of `kernel` on `workload` from the ncu
-    counters summarised in profiles/dram_traffic.md, or None when none were taken
-    or the kernel's sources changed since (the table row carries their hash)."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
+    counters stored in profiles/dram_traffic.json (written by --record-traffic),
+    or None when none were taken or the kernel's sources changed since (each
+    entry carries their hash)."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
+    with open(TRAFFIC_JSON) as f:
+        entries = json.load(f).get("entries", [])
     want = kernel_sources_hash(kernel)
-    for line in open(path):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 5 and cells[0] == kernel and cells[1] == workload:
-            try:
-                rd, wr = float(cells[2]), float(cells[3])
-            except ValueError:
-                continue
-            return rd + wr if cells[4] == want else None
+    for e in entries:
+        if e["kernel"] == kernel and e["workload"] == workload:
+            if e["sources_sha256"] != want:
+                return None
+            return float(e["dram_bytes_read"]) + float(e["dram_bytes_write"])
     return None
+
+
+def record_traffic(csv_path: str, workload: str, scale: float, command: str):
+    """Parse an ncu CSV (--csv, one row per launch and metric) and store, per
+    kernel of KERNEL_SOURCES, the mean DRAM bytes read / written per launch,
+    times `scale` (for a capture on a smaller case whose traffic grows in
+    proportion to the work), with the kernel's current source hash."""
+    import csv
+    per = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if r]
+    head = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    cols = rows[head]
+    ki, mi, vi, ui = (cols.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
+                                               "Metric Unit"))
+    idi = cols.index("ID")
+    mult = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    for r in rows[head + 1:]:
+        name = r[ki].split("(")[0].split("::")[-1].strip()
+        if name not in KERNEL_SOURCES or r[mi] not in ("dram__bytes_read.sum",
+                                                       "dram__bytes_write.sum"):
+            continue
+        val = float(r[vi].replace(",", "")) * mult.get(r[ui], 1.0)
+        per.setdefault(name, {}).setdefault(r[idi], {})[r[mi]] = val
+    data = {"entries": []}
+    if os.path.exists(TRAFFIC_JSON):
+        with open(TRAFFIC_JSON) as f:
+            data = json.load(f)
+    for name, launches in per.items():
+        rd = [m["dram__bytes_read.sum"] for m in launches.values()]
+        wr = [m["dram__bytes_write.sum"] for m in launches.values()]
+        entry = {"kernel": name, "workload": workload,
+                 "dram_bytes_read": scale * sum(rd) / len(rd),
+                 "dram_bytes_write": scale * sum(wr) / len(wr),
+                 "launches": len(rd), "scale": scale, "command": command,
+                 "sources_sha256": kernel_sources_hash(name)}
+        data["entries"] = [e for e in data["entries"]
+                           if not (e["kernel"] == name and e["workload"] == workload)]
+        data["entries"].append(entry)
+        print(json.dumps(entry))
+    data["entries"].sort(key=lambda e: (e["workload"], e["kernel"]))
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(data, f, indent=1)
+        f.write("\n")
 
 
 def load_peaks():
@@ -177,28 +226,71 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def cpu_oracle_rate(w, case, budget_s: float):
-    """Time the CPU float64 oracle (fwd + bwd) on whole query heads of the
-    workload until ``budget_s`` is spent (at least one GQA group)."""
-    from oracle import oracle_bwd  # test infrastructure: only this leg runs it
-    torch.set_num_threads(os.cpu_count() or 1)
-    group = w.heads_q // w.heads_kv
+def cpu_oracle_rates(w, case, budget_s: float, threads: int | None = None):
+    """Time the CPU float64 oracle on whole query heads of the workload (all
+    rows of every sequence): the forward (oracle_fwd) for about a third of
+    ``budget_s`` and forward + backward (oracle_bwd, which recomputes the
+    forward) for the rest, at least one head each.  Rates use the same
+    algorithmic flops as the GPU line (fwd 4 d, bwd 10 d per visible pair)."""
+    from oracle import oracle_bwd, oracle_fwd  # test infrastructure: only this leg runs it
+    torch.set_num_threads(threads or os.cpu_count() or 1)
     cu = case.cu_seqlens
     pairs = visible_pairs(case.lengths, w.causal, w.window)
-    done_heads, t0 = 0, time.perf_counter()
-    while done_heads < w.heads_q:
-        heads = list(range(done_heads, done_heads + group))
-        oracle_bwd(case.q, case.k, case.v, case.sink, case.dout, scale=w.scale, causal=w.causal,
-                   window=w.window, cu_seqlens_q=cu, cu_seqlens_k=cu, heads=heads)
-        done_heads += group
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    flops = 14.0 * w.head_dim * pairs * done_heads
-    return dict(value=flops / dt / 1e12, unit="TFLOP/s", cores=torch.get_num_threads(),
-                kind="oracle", seconds=dt,
-                sample=f"{w.name}: query heads 0..{done_heads - 1} of {w.heads_q}, all rows, "
-                       f"fwd+bwd in float64")
+    kw = dict(scale=w.scale, causal=w.causal, window=w.window, cu_seqlens_q=cu,
+              cu_seqlens_k=cu)
+
+    def timed(fn, budget):
+        fn(heads=[0])                      # warm-up call (thread pool, allocator), untimed
+        done, t0 = 0, time.perf_counter()
+        while done < w.heads_q:
+            fn(heads=[done])
+            done += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        return done, time.perf_counter() - t0
+
+    nf, tf = timed(lambda heads: oracle_fwd(case.q, case.k, case.v, case.sink, heads=heads,
+                                            **kw), budget_s / 3)
+    nb, tb = timed(lambda heads: oracle_bwd(case.q, case.k, case.v, case.sink, case.dout,
+                                            heads=heads, **kw), budget_s * 2 / 3)
+    d = w.head_dim
+    t_fwd_head, t_both_head = tf / nf, tb / nb
+    t_bwd_head = t_both_head - t_fwd_head
+    return dict(
+        value=14.0 * d * pairs / t_both_head / 1e12, unit="TFLOP/s",
+        fwd_value=4.0 * d * pairs / t_fwd_head / 1e12,
+        # the backward's own share, where it stands clear of the timing noise
+        bwd_value=(10.0 * d * pairs / t_bwd_head / 1e12
+                   if t_bwd_head > 0.1 * t_both_head else None),
+        cores=torch.get_num_threads(), kind="oracle", seconds=tf + tb,
+        sample=(f"{w.name}: forward of query heads 0..{nf - 1} and forward+backward of query "
+                f"heads 0..{nb - 1} of {w.heads_q}, all rows of every sequence, float64; "
+                f"value = fwd+bwd, bwd_value = (fwd+bwd time - fwd time) per head"))
+
+
+def cpu_baseline_line(w, case, budget_s: float):
+    """The cpu_baseline object: the workload on every host core, plus the tiny
+    workload on one thread."""
+    res = cpu_oracle_rates(w, case, budget_s)
+    res.pop("seconds", None)
+    tw = WORKLOADS["tiny"]
+    tiny = cpu_oracle_rates(tw, make_case(tw), 0.5, threads=1)
+    tiny.pop("seconds", None)
+    res["tiny_1_thread"] = tiny
+    torch.set_num_threads(os.cpu_count() or 1)
+    return res
+
+
+def config_dict(w, lengths, ws: int) -> dict:
+    """The `config` object of both arms' lines (identical for one workload)."""
+    packed = w.is_varlen
+    return {"workload": w.name, "batch": None if packed else len(lengths),
+            "lengths": lengths if packed else None,
+            "seq_len": None if packed else lengths[0], "heads_q": w.heads_q,
+            "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal,
+            "window": w.window, "q_scale": w.q_mult, "parallelism": f"replicas x{ws}",
+            "l2": "GPU arm: flushed between steps (256 MiB write outside the timed events); "
+                  "inputs on the CPU arm live in host memory"}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -241,7 +333,7 @@ def run_reference(args, w, case):
     rates = []
     res = None
     for i in range(args.warmup + args.steps):
-        res = cpu_oracle_rate(w, case, budget_s=args.ref_budget)
+        res = cpu_oracle_rates(w, case, budget_s=args.ref_budget)
         if i >= args.warmup:
             steps.append(res["seconds"])
             rates.append(res["value"])
@@ -251,11 +343,10 @@ def run_reference(args, w, case):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "lengths": case.lengths, "heads_q": w.heads_q,
-                   "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal,
-                   "window": w.window},
+        "config": config_dict(w, case.lengths, ws),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"],
-                         "kind": "oracle", "sample": res["sample"]},
+                         "kind": "oracle", "sample": res["sample"],
+                         "fwd_value": res["fwd_value"], "bwd_value": res["bwd_value"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -357,9 +448,9 @@ def run_decode(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gptoss_full", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="long_full", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of CPU oracle work for the cpu_baseline leg")
@@ -371,7 +462,20 @@ def main():
                          "sampling, no launch count")
     ap.add_argument("--decode", action="store_true",
                     help="time the paged decode step instead (one JSON line of its own)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="store the DRAM bytes per launch of an ncu capture (--csv with "
+                         "dram__bytes_read.sum and dram__bytes_write.sum) of the workload "
+                         "named by --workload in profiles/dram_traffic.json, and exit")
+    ap.add_argument("--traffic-scale", type=float, default=1.0,
+                    help="with --record-traffic: multiply the captured bytes (a capture of "
+                         "a smaller case whose traffic grows in proportion)")
+    ap.add_argument("--traffic-command", default="",
+                    help="with --record-traffic: the ncu command line, stored with the entry")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic, args.workload, args.traffic_scale,
+                       args.traffic_command)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.decode:
@@ -551,37 +655,61 @@ def main():
     bwd_tf = alg["bwd_flops"] / (bwd_t * 1e-3) / 1e12
     peaks, src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    # the dominant kernel is the backward main kernel (all five backward
-    # products); its achieved rate is the backward's algorithmic flops over its
-    # own launch time, the forward kernel's likewise
+    hbm = float(peaks["hbm_gbs"])
+    # the dominant kernel is the longer of the forward kernel and the backward
+    # main kernel (all five backward products); its achieved rate is its pass's
+    # algorithmic flops (or minimum bytes) over its own launch time
     bwd_main_tf = alg["bwd_flops"] / (bwd_main_ms * 1e-3) / 1e12
     fwd_kernel_tf = alg["fwd_flops"] / (fwd_kernel_ms * 1e-3) / 1e12
-    if bwd_main_ms >= fwd_kernel_ms:
-        dom, dom_tf, dom_ms = "attn_sink_bwd_main_kernel", bwd_main_tf, bwd_main_ms
-    else:
-        dom, dom_tf, dom_ms = "attn_sink_fwd_kernel", fwd_kernel_tf, fwd_kernel_ms
+    bwd_main_gbs = alg["bwd_bytes"] / (bwd_main_ms * 1e-3) / 1e9
+    fwd_kernel_gbs = alg["fwd_bytes"] / (fwd_kernel_ms * 1e-3) / 1e9
+    # which ceiling binds: the tensor cores, or HBM at the pass's arithmetic
+    # intensity (the windowed layers)
+    hbm_bound = (alg["bwd_flops"] / alg["bwd_bytes"]) * hbm / 1e3 < peak
+
+    def roofline(kernel, tf, gbs, ms, bytes_alg, flops_alg):
+        if hbm_bound:
+            r = {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                 "frac": gbs / hbm, "tflops": tf, "tflops_frac_of_bf16_peak": tf / peak,
+                 "peak_note": f"{src} copy bandwidth; achieved = the pass's minimum bytes "
+                              f"({bytes_alg:.4g}) / kernel time"}
+        else:
+            r = {"kernel": kernel, "bound": "tensor", "achieved": tf, "peak": peak,
+                 "unit": "TFLOP/s", "frac": tf / peak,
+                 "frac_of_sustained": tf / float(peaks.get("bf16_tflops_sustained", peak)),
+                 "hbm_gbs": gbs,
+                 "peak_note": f"{src} dense bf16 burst; achieved = the pass's algorithmic "
+                              f"flops ({flops_alg:.4g}) / kernel time"}
+        r.update(kernel_ms=ms, traffic=dram_traffic(kernel, w.name),
+                 algorithmic_bytes=bytes_alg)
+        return r
+
+    rl_bwd = roofline("attn_sink_bwd_main_kernel", bwd_main_tf, bwd_main_gbs, bwd_main_ms,
+                      alg["bwd_bytes"], alg["bwd_flops"])
+    rl_fwd = roofline("attn_sink_fwd_kernel", fwd_kernel_tf, fwd_kernel_gbs, fwd_kernel_ms,
+                      alg["fwd_bytes"], alg["fwd_flops"])
+    dom, other = (rl_bwd, rl_fwd) if bwd_main_ms >= fwd_kernel_ms else (rl_fwd, rl_bwd)
+    # Exponential-unit ceiling: one exp per visible pair and head in each pass,
+    # ex2.approx.f32 at 32 results per SM clock (measured with a single-SM
+    # probe), at the median SM clock sampled during the timed region.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    ex2_per_s = 32.0 * sms * mhz * 1e6
+    sfu = {"ex2_per_sm_clock": 32, "sms": sms, "sm_mhz": mhz, "exp_per_s": ex2_per_s,
+           "fwd_ceiling_tflops": ex2_per_s * 4 * w.head_dim / 1e12,
+           "bwd_ceiling_tflops": ex2_per_s * 10 * w.head_dim / 1e12,
+           "note": "fwd 4 d and bwd 10 d algorithmic flops per exponential"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": n, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "batch": len(lengths) if not packed else None,
-                   "lengths": lengths if packed else None,
-                   "seq_len": None if packed else lengths[0], "heads_q": w.heads_q,
-                   "heads_kv": w.heads_kv, "head_dim": w.head_dim, "causal": w.causal,
-                   "window": w.window, "parallelism": f"replicas x{ws}",
-                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+        "config": config_dict(w, lengths, ws),
         "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf, "fwd_ms": fwd_t, "bwd_ms": bwd_t,
         "frac_of_peak": value / peak, "fwd_frac_of_peak": fwd_tf / peak,
         "bwd_frac_of_peak": bwd_tf / peak, "peak_source": src,
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_tf, "peak": peak,
-                     "unit": "TFLOP/s", "frac": dom_tf / peak,
-                     "traffic": dram_traffic(dom, w.name), "kernel_ms": dom_ms,
-                     "peak_note": f"{src} dense bf16 burst (each kernel runs under 1 ms)"},
-        "roofline_fwd": {"kernel": "attn_sink_fwd_kernel", "bound": "tensor",
-                         "achieved": fwd_kernel_tf, "peak": peak, "unit": "TFLOP/s",
-                         "frac": fwd_kernel_tf / peak, "kernel_ms": fwd_kernel_ms,
-                         "traffic": dram_traffic("attn_sink_fwd_kernel", w.name),
-                         "hbm_gbs": alg["fwd_bytes"] / (fwd_kernel_ms * 1e-3) / 1e9},
+        "roofline": dom,
+        "roofline_other": other,
+        "sfu_ceiling": sfu,
         "e2e": None if args.ncu else {
             "value": whole_job_tflops(flops, ws, e2e_ms), "unit": "TFLOP/s",
             "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -591,8 +719,7 @@ def main():
         "wall_s_timed_region": wall,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.ncu:
-        line["cpu_baseline"] = cpu_oracle_rate(w, case, budget_s=args.cpu_budget)
-        line["cpu_baseline"].pop("seconds", None)
+        line["cpu_baseline"] = cpu_baseline_line(w, case, args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -202,7 +202,9 @@ size_t attn_sink_decode_workspace_size(const attn_sink_decode_params* params);
  * and lengths are checked on the device (see attn_sink_device_error).  All
  * pointers are device pointers, 16-byte aligned where they hold bf16 rows;
  * the workspace is 256-byte aligned and at least
- * attn_sink_decode_workspace_size bytes.  Returns an attn_sink_status.
+ * attn_sink_decode_workspace_size bytes.  batch and heads_kv above 65535
+ * (launch-grid limits) return ATTN_SINK_ERR_UNSUPPORTED.  Returns an
+ * attn_sink_status.
  */
 int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const void* k_cache,
                      const void* v_cache, const int* block_table, const int* seq_lens,
@@ -275,7 +277,9 @@ size_t attn_sink_fwd_workspace_size(const attn_sink_params* params);
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
- * capture.  Every call on a device shares the one array: calls that overlap on
+ * capture.  The cached address belongs to the device's primary context:
+ * resetting that context (cudaDeviceReset) after the first call is not
+ * supported, since later calls would pass the old address.  Every call on a device shares the one array: calls that overlap on
  * the GPU (different streams, no ordering between them) race on it and must
  * be serialised by the caller.  Nothing in the array needs to start at zero:
  * each call overwrites the part it reads.
@@ -346,8 +350,16 @@ const char* attn_sink_status_string(int status);
  * range of the tensor-core operands, 0x800 when attn_sink_decode met a
  * block-table entry outside [0, num_pages) or a sequence length outside
  * [0, max_pages * page_size] (that key is skipped; the length is clamped).
- * Returns ATTN_SINK_OK, or ATTN_SINK_ERR_CUDA when the
- * synchronisation itself failed.
+ * Only the first code recorded since the last read is kept.
+ * The word is one per device, shared by every stream and every caller of the
+ * library on that device: it is not tied to `stream`, so a code may come from
+ * a launch on another stream, and a read clears it for every caller.  Callers
+ * that run the library on several streams at once should read it after
+ * synchronising all of them.
+ * Returns ATTN_SINK_ERR_TIMEOUT when *code is a bounded-wait code (0x1xx or
+ * 0x2xx), ATTN_SINK_ERR_CUDA when the synchronisation or the read itself
+ * failed, ATTN_SINK_OK otherwise (including the input codes 0x400 / 0x800,
+ * which *code reports).
  */
 int attn_sink_device_error(void* stream, int* code);
 

@@ -256,6 +256,10 @@ def test_decode_rejects_bad_arguments_on_host():
     assert _decode(_dparams(), ws_bytes=16) == 3
     assert _decode(_dparams(), ws=FAKE + 16) == 3
     assert _decode(_dparams(batch=0)) == OK
+    # launch-grid limits (sequences in grid.z, kv heads in grid.y)
+    assert _decode(_dparams(batch=65536)) == UNSUPPORTED
+    assert _decode(_dparams(heads_q=65536, heads_kv=65536)) == UNSUPPORTED
+    assert binding.attn_sink_decode_workspace_size(_dparams(batch=65536)) == 0
     assert binding.attn_sink_launch_count() == n0
     assert binding.attn_sink_decode_workspace_size(_dparams()) > 0
     assert binding.attn_sink_decode_workspace_size(_dparams(batch=0)) == 0

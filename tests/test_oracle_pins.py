@@ -86,28 +86,36 @@ CASES = [
 ]
 
 
+# Row blocks of the oracle: the default (one block per short sequence) and
+# blocks of 3 rows, so that every block after the first takes its key range
+# from the causal / window bounds of a later first row (r0 > 0).
+BLOCKS = [256, 3]
+
+
+@pytest.mark.parametrize("block", BLOCKS)
 @pytest.mark.parametrize("lq,lk,hq,hkv,d,causal,window", CASES)
-def test_neginf_sink_is_standard_attention(lq, lk, hq, hkv, d, causal, window):
+def test_neginf_sink_is_standard_attention(lq, lk, hq, hkv, d, causal, window, block):
     """sink = -inf removes the sink column: torch's SDPA (float64) must agree."""
     q, k, v, do, sink, cq, ck = _problem(lq, lk, hq, hkv, d, 11)
     sink = torch.full((hq,), -math.inf, dtype=F64)
     scale = 0.37
     out, lse = oracle_fwd(q, k, v, sink, scale=scale, causal=causal, window=window,
-                          cu_seqlens_q=cq, cu_seqlens_k=ck)
+                          cu_seqlens_q=cq, cu_seqlens_k=ck, block=block)
     ref, ref_lse = _sdpa_per_sequence(q, k, v, cq, ck, scale, causal, window)
     torch.testing.assert_close(out, ref, rtol=1e-12, atol=1e-12)
     torch.testing.assert_close(lse, ref_lse, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("block", BLOCKS)
 @pytest.mark.parametrize("lq,lk,hq,hkv,d,causal,window", CASES)
-def test_finite_sink_gates_standard_attention(lq, lk, hq, hkv, d, causal, window):
+def test_finite_sink_gates_standard_attention(lq, lk, hq, hkv, d, causal, window, block):
     """With a finite sink, P_ih = sigmoid(sink - LSE_std), so the output is the
     standard output times (1 - P_ih) and LSE = logaddexp(LSE_std, sink).
     The scale is not 1, so a sink that were (wrongly) scaled would fail."""
     q, k, v, do, sink, cq, ck = _problem(lq, lk, hq, hkv, d, 23, sink_scale=2.0)
     scale = 0.29
     out, lse = oracle_fwd(q, k, v, sink, scale=scale, causal=causal, window=window,
-                          cu_seqlens_q=cq, cu_seqlens_k=ck)
+                          cu_seqlens_q=cq, cu_seqlens_k=ck, block=block)
     ref, ref_lse = _sdpa_per_sequence(q, k, v, cq, ck, scale, causal, window)
     gate = torch.sigmoid(ref_lse - sink.unsqueeze(1))          # [H, T] = 1 - P_ih
     torch.testing.assert_close(out, ref * gate.T.unsqueeze(-1), rtol=1e-11, atol=1e-12)
@@ -128,12 +136,13 @@ def _gated_autograd(q, k, v, sink, do, cq, ck, scale, causal, window):
     return q.grad, k.grad, v.grad, sink.grad
 
 
+@pytest.mark.parametrize("block", BLOCKS)
 @pytest.mark.parametrize("lq,lk,hq,hkv,d,causal,window", CASES)
-def test_backward_matches_autograd_of_gated_form(lq, lk, hq, hkv, d, causal, window):
+def test_backward_matches_autograd_of_gated_form(lq, lk, hq, hkv, d, causal, window, block):
     q, k, v, do, sink, cq, ck = _problem(lq, lk, hq, hkv, d, 31, sink_scale=1.5)
     scale = 0.41
     g = oracle_bwd(q, k, v, sink, do, scale=scale, causal=causal, window=window,
-                   cu_seqlens_q=cq, cu_seqlens_k=ck)
+                   cu_seqlens_q=cq, cu_seqlens_k=ck, block=block)
     dq, dk, dv, dsink = _gated_autograd(q, k, v, sink, do, cq, ck, scale, causal, window)
     torch.testing.assert_close(g["dq"], dq, rtol=1e-10, atol=1e-11)
     torch.testing.assert_close(g["dk"], dk, rtol=1e-10, atol=1e-11)
@@ -214,20 +223,32 @@ def test_hand_worked_example():
                                    rtol=1e-14, atol=1e-14)
 
 
-def _loss(q, k, v, sink, do, cq, ck, scale, causal, window):
+def _loss(q, k, v, sink, do, cq, ck, scale, causal, window, block=256):
     out, _ = oracle_fwd(q, k, v, sink, scale=scale, causal=causal, window=window,
-                        cu_seqlens_q=cq, cu_seqlens_k=ck)
+                        cu_seqlens_q=cq, cu_seqlens_k=ck, block=block)
     return float((out * do).sum())
 
 
-@pytest.mark.parametrize("causal,window", [(True, 0), (True, 3), (False, 0)])
-def test_finite_differences(causal, window):
+FD_CASES = [
+    # lengths_q, lengths_k, causal, window, block
+    ([3, 5], [3, 5], True, 0, 256),
+    ([3, 5], [3, 5], True, 3, 256),
+    ([3, 5], [3, 5], False, 0, 256),
+    # blocks of 2 rows: windowed key ranges of later blocks, N_q != N_k
+    ([3, 7], [3, 7], True, 3, 2),
+    ([5, 4], [7, 9], True, 2, 2),
+    ([6], [4], True, 0, 2),
+]
+
+
+@pytest.mark.parametrize("lq,lk,causal,window,block", FD_CASES)
+def test_finite_differences(lq, lk, causal, window, block):
     """Central differences of L = <O, dO> for every element of q, k, v, sink:
-    two packed sequences (3, 5), H_q = 4, H_kv = 2, d = 8."""
-    q, k, v, do, sink, cq, ck = _problem([3, 5], [3, 5], 4, 2, 8, 57)
+    small packed sequences, H_q = 4, H_kv = 2, d = 8."""
+    q, k, v, do, sink, cq, ck = _problem(lq, lk, 4, 2, 8, 57)
     scale, eps = 0.45, 1e-6
     g = oracle_bwd(q, k, v, sink, do, scale=scale, causal=causal, window=window,
-                   cu_seqlens_q=cq, cu_seqlens_k=ck)
+                   cu_seqlens_q=cq, cu_seqlens_k=ck, block=block)
     args = dict(q=q, k=k, v=v, sink=sink)
     for name in ("q", "k", "v", "sink"):
         base = args[name]
@@ -236,9 +257,9 @@ def test_finite_differences(causal, window):
         for idx in range(flat.numel()):
             old = float(flat[idx])
             flat[idx] = old + eps
-            lp = _loss(q, k, v, sink, do, cq, ck, scale, causal, window)
+            lp = _loss(q, k, v, sink, do, cq, ck, scale, causal, window, block)
             flat[idx] = old - eps
-            lm = _loss(q, k, v, sink, do, cq, ck, scale, causal, window)
+            lm = _loss(q, k, v, sink, do, cq, ck, scale, causal, window, block)
             flat[idx] = old
             fd.view(-1)[idx] = (lp - lm) / (2 * eps)
         an = g["d" + name]
