@@ -40,7 +40,7 @@ struct DqParams {
   CUtensorMap tm_v;    // fp16 copy of v
   const int* cu_q;
   const int* cu_k;
-  const float2* LD;    // [H_q][T_q]: (lse * log2 e, D)
+  const float2* LD;    // [H_q][T_q]: (-lse * log2 e, D)
   void* dq;            // [T_q][H_q][64] bf16 (grad_fp32 = 0) or fp32
   int* err;
   int seqlen_q, seqlen_k;
@@ -55,22 +55,23 @@ struct DqParams {
 
 // dS of 32 keys of one query row (thread = row), fp16-packed.
 template <bool kMask>
-__device__ __forceinline__ void dq_ds_chunk(const uint32_t* sr, const uint32_t* dr, float sl2,
-                                            float lse2, float d, int j_first, int jmin,
-                                            int jmax, uint32_t* dk) {
+__device__ __forceinline__ void dq_ds_chunk(const uint32_t* sr, const uint32_t* dr,
+                                            uint64_t sl2x2, uint64_t nlse2x2, uint64_t d2,
+                                            int j_first, int jmin, int jmax, uint32_t* dk) {
   #pragma unroll
   for (int e = 0; e < 32; e += 2) {
-    float dv[2];
-    #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -lse2));
-      if (kMask) {
-        const int j = j_first + e + u;
-        if (j < jmin || j > jmax) pe = 0.0f;
-      }
-      dv[u] = pe * (__uint_as_float(dr[e + u]) - d);
+    const uint64_t x =
+        ffma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, nlse2x2);
+    float p0 = ex2_approx(f2_lo(x));
+    float p1 = ex2_approx(f2_hi(x));
+    if (kMask) {
+      const int j = j_first + e;
+      if (j < jmin || j > jmax) p0 = 0.0f;
+      if (j + 1 < jmin || j + 1 > jmax) p1 = 0.0f;
     }
-    dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
+    const uint64_t ds =
+        fmul2(f2(p0, p1), fsub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), d2));
+    dk[e >> 1] = pack_f16x2(f2_lo(ds), f2_hi(ds));
   }
 }
 
@@ -233,6 +234,7 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     const float sl2 = p.scale_log2;
     // this row's (lse log2 e, D); rows past the sequence read a valid row
     const float2 ld = __ldg(p.LD + (size_t)h * p.total_q + sp.q0 + min(i, sp.nq - 1));
+    const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(ld.x, ld.x), d2 = f2(ld.y, ld.y);
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
     const int tile_r1 = min(i0 + kBlockM, sp.nq) - 1;
@@ -252,9 +254,9 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         tmem_ld_wait();
         uint32_t dk[16];
         if (need_mask)
-          dq_ds_chunk<true>(sr, dr, sl2, ld.x, ld.y, j0 + cc, jmin, jmax, dk);
+          dq_ds_chunk<true>(sr, dr, sl2x2, nlse2x2, d2, j0 + cc, jmin, jmax, dk);
         else
-          dq_ds_chunk<false>(sr, dr, sl2, ld.x, ld.y, j0 + cc, jmin, jmax, dk);
+          dq_ds_chunk<false>(sr, dr, sl2x2, nlse2x2, d2, j0 + cc, jmin, jmax, dk);
         // dS over S columns this thread has already read (chunk cc -> cc / 2)
         tmem_st_x16(tmem + lane_base + kDqColS + 64 * c + (cc >> 1), dk);
       }

@@ -65,7 +65,7 @@ struct BwdParams {
   CUtensorMap tm_dq;   // [T_q][H_q][64] fp32 dq accumulator, box 32 x 1 x 128, 128B swizzle
   const int* cu_q;
   const int* cu_k;
-  const float2* LD;    // [H_q][T_q]: (lse * log2 e, D) per query row
+  const float2* LD;    // [H_q][T_q]: (-lse * log2 e, D) per query row
   float* dq_acc;       // [T_q][H_q][64], zeroed unless null fp32, pre-zeroed
   void* dk;            // [T_k][H_kv][64] bf16 or fp32 (split == 1)
   void* dv;
@@ -93,7 +93,7 @@ struct PreParams {
   const float* lse;
   const float* sink;
   const __nv_bfloat16* sink_bf16;   // bf16 sink when non-null
-  float2* LD;          // [H_q][T_q]: (lse * log2 e, D)
+  float2* LD;          // [H_q][T_q]: (-lse * log2 e, D)
   float* partials;     // [H_q][n_blocks]
   float* dq_acc;       // [T_q][H_q][64]
   uint16_t* q16;       // [T_q][H_q][64] fp16 copy of q
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(256) attn_sink_bwd_pre_kernel(const PreParams 
     d += __shfl_xor_sync(0xffffffffu, d, 4);
     if (sub == 0 && t < p.total_q) {
       const float lse = p.lse[(size_t)h * p.total_q + t];
-      p.LD[(size_t)h * p.total_q + t] = make_float2(lse * kLog2e, d);
+      p.LD[(size_t)h * p.total_q + t] = make_float2(-lse * kLog2e, d);
       // P_ih = exp(sink - lse); zero when the sink is -inf.
       if (sink_h > -INFINITY && lse > -INFINITY)
         acc -= ex2_approx((sink_h - lse) * kLog2e) * d;
@@ -306,30 +306,34 @@ __device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, 
 // P^T and dS^T of 32 queries of one key row (thread = key), fp16-packed:
 //   P  = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
 //   dS = P (dP - D)
-// ld_row holds (lse * log2 e, D) of the 32 queries.
+// nl_row / d_row hold -lse * log2 e and D of the 32 queries.  Pairs of
+// queries go through the packed fp32 pair instructions (scale-and-subtract,
+// dP - D, the product with P); the exponentials stay per element.
 // With kMask, entries whose (query, key) pair is not visible, or whose row or
 // key lies past the sequence, are exact zeros.
 template <bool kMask>
 __device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t* dr,
-                                              const float2* ld_row,
-                                              float sl2, int i_first, int imin, int imax,
+                                              const float* nl_row, const float* d_row,
+                                              uint64_t sl2x2, int i_first, int imin, int imax,
                                               int nq, bool key_ok, uint32_t* pk, uint32_t* dk) {
   #pragma unroll
   for (int e = 0; e < 32; e += 2) {
-    float pv[2], dv[2];
-    #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const float2 ld = ld_row[e + u];
-      float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -ld.x));
-      if (kMask) {
-        const int i = i_first + e + u;
-        if (!key_ok || i < imin || i > imax || i >= nq) pe = 0.0f;
-      }
-      pv[u] = pe;
-      dv[u] = pe * (__uint_as_float(dr[e + u]) - ld.y);
+    const float2 nl = *reinterpret_cast<const float2*>(nl_row + e);
+    const float2 dd = *reinterpret_cast<const float2*>(d_row + e);
+    const uint64_t x =
+        ffma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, f2(nl.x, nl.y));
+    float p0 = ex2_approx(f2_lo(x));
+    float p1 = ex2_approx(f2_hi(x));
+    if (kMask) {
+      const int i = i_first + e;
+      if (!key_ok || i < imin || i > imax || i >= nq) p0 = 0.0f;
+      if (!key_ok || i + 1 < imin || i + 1 > imax || i + 1 >= nq) p1 = 0.0f;
     }
-    pk[e >> 1] = pack_f16x2(pv[0], pv[1]);
-    dk[e >> 1] = pack_f16x2(dv[0], dv[1]);
+    const uint64_t ds =
+        fmul2(f2(p0, p1), fsub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                f2(dd.x, dd.y)));
+    pk[e >> 1] = pack_f16x2(p0, p1);
+    dk[e >> 1] = pack_f16x2(f2_lo(ds), f2_hi(ds));
   }
 }
 
@@ -339,7 +343,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
   __shared__ __align__(8) uint64_t s_full[2], p_full[2], ds_free[2];
-  __shared__ float2 s_LD[kBwdStages][kBlockM];    // (lse * log2 e, D) of the step's rows
+  __shared__ __align__(16) float s_nL[kBwdStages][kBlockM];   // -lse * log2 e of the step's rows
+  __shared__ __align__(16) float s_D[kBwdStages][kBlockM];    // D of the step's rows
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -446,13 +451,16 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tma_load_3d(&p.tm_q, &q_full[st], sQ + st * kTileBytes, 0, h, sp.q0 + i0);
         tma_load_3d(&p.tm_do, &q_full[st], sdO + st * kTileBytes, 0, h, sp.q0 + i0);
       }
-      // (lse log2 e, D) of the step's 128 query rows, copied asynchronously; rows
-      // past the sequence read a valid row and are masked by the compute warps.
+      // (-lse log2 e, D) of the step's 128 query rows, copied asynchronously into
+      // two planes (so that pairs of rows load as one 8-byte word); rows past the
+      // sequence read a valid row and are masked by the compute warps.
       #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = lane + 32 * u;
         const size_t idx = (size_t)h * p.total_q + sp.q0 + min(i0 + t, sp.nq - 1);
-        cp_async_8(smem_u32(&s_LD[st][t]), p.LD + idx);
+        const float* src = reinterpret_cast<const float*>(p.LD + idx);
+        cp_async_4(smem_u32(&s_nL[st][t]), src);
+        cp_async_4(smem_u32(&s_D[st][t]), src + 1);
       }
       cp_async_mbar_arrive_noinc(&q_full[st]);
       issued = m + 1;
@@ -572,7 +580,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const int r = tid & 127;                        // key row in tile = TMEM lane
     const int j = j0 + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2(p.scale_log2, p.scale_log2);
     const int imin = p.causal ? j - off : 0;
     const int imax = (p.causal && p.window > 0) ? j - off + p.window - 1 : sp.nq - 1;
     const bool key_ok = j < sp.nk;
@@ -623,12 +631,14 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         uint32_t pk[16], dk[16];
         // The mask test is hoisted out of the element loop (a branch per element
         // keeps the compiler from interleaving the elements' exponentials).
+        const float* nl_row = &s_nL[st][64 * hh + c];
+        const float* d_row = &s_D[st][64 * hh + c];
         if (need_mask)
-          bwd_pds_chunk<true>(sr, dr, &s_LD[st][64 * hh + c], sl2,
-                              i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
+          bwd_pds_chunk<true>(sr, dr, nl_row, d_row, sl2x2, i0 + c, imin, imax, sp.nq, key_ok,
+                              pk, dk);
         else
-          bwd_pds_chunk<false>(sr, dr, &s_LD[st][64 * hh + c], sl2,
-                               i0 + c, imin, imax, sp.nq, key_ok, pk, dk);
+          bwd_pds_chunk<false>(sr, dr, nl_row, d_row, sl2x2, i0 + c, imin, imax, sp.nq, key_ok,
+                               pk, dk);
         // P^T over S^T columns this thread has already read (chunk c -> c / 2)
         tmem_st_x16(tmem + lane_base + kColST + 64 * hh + (c >> 1), pk);
         // dS^T row r, queries c..c+31 of this half: 4 chunks of 16 bytes

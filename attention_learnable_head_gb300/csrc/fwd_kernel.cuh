@@ -385,23 +385,27 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       }
       // P = exp2(S * scale * log2 e - m), fp16, over the first 32 columns of this
-      // half of S (already read into registers).
+      // half of S (already read into registers).  The scale-and-subtract and the
+      // row sum run on pairs of columns (packed fp32 pair instructions), two
+      // running pair sums in turn.
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      float rs0 = 0.0f, rs1 = 0.0f;
+      const uint64_t sl2x2 = f2(sl2, sl2), negm2 = f2(-m_use, -m_use);
+      uint64_t rs = f2(0.0f, 0.0f);
       #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t pk[16];
         #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(a[cc + e]), sl2, -m_use));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(a[cc + e + 1]), sl2, -m_use));
-          rs0 += e0;
-          rs1 += e1;
+          const uint64_t x = ffma2(f2(__uint_as_float(a[cc + e]), __uint_as_float(a[cc + e + 1])),
+                                   sl2x2, negm2);
+          const float e0 = ex2_approx(f2_lo(x));
+          const float e1 = ex2_approx(f2_hi(x));
+          rs = fadd2(rs, f2(e0, e1));
           pk[e >> 1] = pack_f16x2(e0, e1);
         }
         tmem_st_x16(tP + (cc >> 1), pk);
       }
-      l = l * alpha + (rs0 + rs1);
+      l = l * alpha + (f2_lo(rs) + f2_hi(rs));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full);
