@@ -1,18 +1,14 @@
 // Forward kernel: attention with a per-head sink, sm_103a (tcgen05 + TMA).
 //
 // One CTA per (query head h, sequence, 128-row query tile); two CTAs share an
-// SM (320 threads x 96 registers, 86 KB of SMEM and 256 TMEM columns each), so
-// while one CTA's softmax turns its S tile into P the tensor cores run the
-// other CTA's MMAs, and one CTA's set-up, Q load and epilogue overlap the
-// other's loop.  Two CTAs with one MMA issuer each keep the tensor pipe busier
-// than one CTA whose single issuer alternates between two tiles: every pause
-// of an issuer (an mbarrier wait costs ~200 cycles) idles the pipe only for
-// its own CTA.  Per key tile:
-//   S = Q K^T (tcgen05, bf16 operands from SMEM, fp32 accumulators in TMEM),
+// SM (320 threads x 96 registers, ~100 KB of SMEM and 256 TMEM columns each).
+// Per key tile n:
+//   S(n) = Q K_n^T (tcgen05, bf16 operands from SMEM, fp32 accumulators in TMEM),
 //   online softmax whose running max and sum start from the sink logit
 //   (m0 = sink[h] * log2 e, l0 = 1 in the exp2 domain),
-//   P (fp16) written to TMEM and consumed there by O += P V (tcgen05, A from
-//   TMEM; V read as fp16 from SMEM, converted into the workspace before launch),
+//   P(n) (fp16) written to TMEM and consumed there by O += P(n) V_n (tcgen05, A
+//   from TMEM; V read as fp16 from SMEM, converted into the workspace before
+//   launch),
 // then out = O / l (bf16, plus optionally the bf16 residual O/l - out) and
 // lse = ln 2 * (m + log2 l), which includes the sink.  S = Q K^T multiplies the
 // bf16 inputs exactly; P and V go to the tensor cores as fp16 (11-bit
@@ -22,28 +18,29 @@
 // concat listing "带汇聚的注意力（GPT-OSS）" on the euno.news page, and the
 // P_ij / P_ih equations of its section "数学公式".
 //
-// Each key tile's 128 columns are two halves of 64 (c = 0, 1) with their own
-// softmax warps, running max m_c, sum l_c and accumulator O_c = sum P V over
-// the half's keys, so the halves never wait for each other inside the loop.  A
-// row's halves are merged once, at the end, like two key blocks of a split
-// softmax: m = max(m_0, m_1), l = sum l_c 2^(m_c - m), O = sum O_c 2^(m_c - m).
-// The sink's term (1 at m = sink log2 e) is counted in half 0.
+// Pipelining.  P has TMEM columns of its own, so S(n+1) is issued as soon as
+// the softmax warps have read S(n) out of TMEM, before PV(n): the tensor cores
+// compute the next scores while this tile's exponentials run, and the softmax
+// warps find S(n+1) ready when they finish P(n).  Before writing P(n+1) they
+// wait for PV(n) (which reads the P columns and updates O).  K and V come
+// through separate rings (K: 3 stages, released by S; V: 2 stages, released by
+// PV), because K(n+2) is needed before V(n+1).
 //
-// Rescaling of O_c is lazy: the running max used for the exponentials only
-// moves when a row's max grows by more than kRescaleThreshold (log2 units); P
-// stays below 2^threshold, and out/lse are exact because l_c and O_c use the
-// same max.
+// Each key tile's 128 columns are two halves of 64 (c = 0, 1), one softmax
+// warpgroup each (thread = query row = TMEM lane).  The halves of a row
+// exchange their maxima through SMEM once per tile and share one running max
+// and one O; each keeps its part of the row sum (the sink's term in half 0).
+// Rescaling of O is lazy: the running max only moves when a row's max grows by
+// more than kRescaleThreshold (log2 units); P stays below 2^threshold, and
+// out/lse are exact because l and O use the same max.
 //
 // Warp roles (320 threads):
-//   warps 0-3   softmax of key half 0 (thread t owns row t = TMEM lane t)
+//   warps 0-3   softmax of key half 0
 //   warps 4-7   softmax of key half 1
-//   warp 8      TMA producer: Q once, then K/V tiles through a two-stage ring
+//   warp 8      TMA producer: Q once, then K and V tiles through their rings
 //   warp 9      MMA issuer (one lane) and TMEM owner
-// TMEM columns (256 allocated): S 0-127 (fp32; P_c, 64 fp16 two per column, is
-// written over the first 32 columns of half c of S once read), O_0 128-191,
-// O_1 192-255 (fp32).
-// P_c overwrites S safely: PV(n) is issued before S(n+1) by the same thread,
-// and tcgen05 MMAs from one thread execute in issue order.
+// TMEM columns (256 allocated): S 0-127 (fp32), P 128-191 (128 keys as fp16
+// pairs), O 192-255 (fp32).
 #pragma once
 #include <cuda_bf16.h>
 #include "sm103_ptx.cuh"
@@ -56,13 +53,16 @@ constexpr int kHeadDim = 64;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
 constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
 
-constexpr int kFwdStages = 2;       // K/V ring depth
+constexpr int kFwdKStages = 3;      // K ring depth
+constexpr int kFwdVStages = 2;      // V ring depth
 constexpr int kFwdThreads = 320;    // 8 softmax warps, TMA warp, MMA warp
 constexpr int kFwdTmaWarp = 8;
 constexpr int kFwdMmaWarp = 9;
 constexpr uint32_t kFwdTmemCols = 256;
-constexpr uint32_t kFwdColO = 128;  // first O column
-constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (1 + 2 * kFwdStages);
+constexpr uint32_t kFwdColS = 0;    // S: 128 fp32 columns
+constexpr uint32_t kFwdColP = 128;  // P: 128 keys as fp16 pairs, 64 columns
+constexpr uint32_t kFwdColO = 192;  // O: 64 fp32 columns
+constexpr int kFwdSmemBytes = 1024 + (int)kTileBytes * (1 + kFwdKStages + kFwdVStages);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -138,12 +138,13 @@ __global__ void __maxnreg__(96)
 attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, mma_drained;
-  __shared__ __align__(8) uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
-  __shared__ __align__(8) uint64_t s_full, p_full, pv_done[2];
+  __shared__ __align__(8) uint64_t k_full[kFwdKStages], k_empty[kFwdKStages];
+  __shared__ __align__(8) uint64_t v_full[kFwdVStages], v_empty[kFwdVStages];
+  __shared__ __align__(8) uint64_t s_full, s_free, p_full, pv_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ float s_red_m[2][kBlockM];   // [half][row], epilogue only
-  __shared__ float s_red_l[2][kBlockM];
+  __shared__ float s_mx[2][2][kBlockM];   // [tile parity][half][row]: the halves' row maxima
+  __shared__ float s_red_l[2][kBlockM];   // [half][row], epilogue only
 
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
@@ -187,19 +188,24 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + kTileBytes;
-  uint8_t* sV = sK + kFwdStages * kTileBytes;
+  uint8_t* sV = sK + kFwdKStages * kTileBytes;
 
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&q_full, 1);
     mbar_init(&mma_drained, 1);
-    for (int s = 0; s < kFwdStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < kFwdKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kFwdVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(&s_full, 1);
+    mbar_init(&s_free, 2 * kBlockM);
     mbar_init(&p_full, 2 * kBlockM);
-    for (int c = 0; c < 2; ++c) mbar_init(&pv_done[c], 1);
+    mbar_init(&pv_done, 1);
     fence_mbarrier_init();
   }
   if (warp == kFwdMmaWarp) {
@@ -213,6 +219,11 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
 
   if (warp == kFwdTmaWarp) {
     // ---------------------------------------------------------------- TMA producer
+    // Two rings filled in the order the MMA thread consumes them: K(n) is read
+    // by S(n) only (3 stages, released when S(n) completes), V(n) by PV(n) only
+    // (2 stages, released when PV(n) completes).  One thread polls both rings'
+    // release barriers and issues whichever copy is free, so K runs up to three
+    // tiles ahead regardless of when the V stages come back.
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
@@ -220,87 +231,101 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       const uint64_t keep = l2_policy_evict_last();
       mbar_arrive_expect_tx(&q_full, kTileBytes);
       tma_load_3d(&p.tm_q, &q_full, sQ, 0, h, sp.q0 + i0);
-      int issued = 0;
-      for (int it = 0; it < num; ++it) {
-        const int st = it % kFwdStages;
-        if (it >= kFwdStages &&
-            !mbar_wait(&kv_empty[st], ((it / kFwdStages) & 1) ^ 1, &abort_flag)) {
-          abort_flag = 1;
-          atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 1);
-          break;
+      int nk = 0, nv = 0;                    // copies issued so far
+      unsigned long long t_last = global_timer_ns();
+      bool ok = true;
+      while (nk < num || nv < num) {
+        bool progress = false;
+        // K(nk): its stage was last read by S(nk - 3)
+        if (nk < num && (nk < kFwdKStages ||
+                         mbar_test_wait(smem_u32(&k_empty[nk % kFwdKStages]),
+                                        ((nk / kFwdKStages) & 1) ^ 1))) {
+          const int st = nk % kFwdKStages;
+          mbar_arrive_expect_tx(&k_full[st], kTileBytes);
+          tma_load_3d_hint(&p.tm_k, &k_full[st], sK + st * kTileBytes, 0, g,
+                           sp.k0 + (lo + nk) * kBlockN, keep);
+          ++nk;
+          progress = true;
         }
-        const int row = sp.k0 + (lo + it) * kBlockN;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
-        tma_load_3d_hint(&p.tm_k, &kv_full[st], sK + st * kTileBytes, 0, g, row, keep);
-        tma_load_3d_hint(&p.tm_v, &kv_full[st], sV + st * kTileBytes, 0, g, row, keep);
-        issued = it + 1;
+        // V(nv): its stage was last read by PV(nv - 2); V never runs ahead of K
+        if (nv < nk && (nv < kFwdVStages ||
+                        mbar_test_wait(smem_u32(&v_empty[nv % kFwdVStages]),
+                                       ((nv / kFwdVStages) & 1) ^ 1))) {
+          const int st = nv % kFwdVStages;
+          mbar_arrive_expect_tx(&v_full[st], kTileBytes);
+          tma_load_3d_hint(&p.tm_v, &v_full[st], sV + st * kTileBytes, 0, g,
+                           sp.k0 + (lo + nv) * kBlockN, keep);
+          ++nv;
+          progress = true;
+        }
+        if (progress) {
+          t_last = global_timer_ns();
+        } else if (abort_flag || global_timer_ns() - t_last > kWaitLimitNs) {
+          ok = false;
+          break;
+        } else {
+          __nanosleep(32);
+        }
       }
-      if (abort_flag) {
+      if (!ok) {
+        abort_flag = 1;
+        atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 1);
         // Let the copies already in flight land before the CTA releases SMEM.
         mbar_wait(&q_full, 0, nullptr);
-        for (int it = max(0, issued - kFwdStages); it < issued; ++it) {
-          const int st = it % kFwdStages;
-          mbar_wait(&kv_full[st], (it / kFwdStages) & 1, nullptr);
-        }
+        for (int it = max(0, nk - kFwdKStages); it < nk; ++it)
+          mbar_wait(&k_full[it % kFwdKStages], (it / kFwdKStages) & 1, nullptr);
+        for (int it = max(0, nv - kFwdVStages); it < nv; ++it)
+          mbar_wait(&v_full[it % kFwdVStages], (it / kFwdVStages) & 1, nullptr);
       }
     }
   } else if (warp == kFwdMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    // Per key tile n: S = Q K_n^T (M=N=128) into TMEM; the softmax of key half c
-    // (S columns [64c, 64c+64)) writes P_c (fp16) over the first 32 of its
-    // columns, and O_c += P_c V_n[64c, 64c+64) (M=128, N=64, K=64, A from TMEM).
-    // S(n+1) is issued right after PV_0(n) and PV_1(n): the same thread issues
-    // them and tcgen05 MMAs execute in issue order, so both P_c are read before
-    // S(n+1) overwrites them.  The thread waits once per key tile for K/V and
-    // once for P, and issues 12 MMAs in a row.
+    // Per key tile n: S(n) = Q K_n^T (M=N=128, bf16) into the S columns; the
+    // softmax writes P(n) (fp16, 128 keys in 64 columns) into the P columns and
+    // O += P(n) V_n (M=128, N=64, K=128, A from TMEM) accumulates in the O
+    // columns.  S(n+1) is issued as soon as the softmax warps have read S(n)
+    // (s_free), before PV(n): the tensor cores compute the next scores while
+    // the current tile's exponentials run.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, kBlockN, false, false);
       const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
-      bool ok = mbar_wait(&q_full, 0, &abort_flag);
       // Shared-memory descriptors, built once; an operand at byte offset o from a
       // base is the base's descriptor plus o / 16 (the start-address field).
       const uint64_t dQ = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16384, 1024);   // MN-major
       constexpr uint32_t kTileU = kTileBytes >> 4;
-      constexpr uint32_t kHalfU = (64 * kHeadDim * 2) >> 4;   // 64 rows of V
-      auto kv_ready = [&](int n) -> bool {
-        if (!mbar_wait(&kv_full[n % kFwdStages], (n / kFwdStages) & 1, &abort_flag))
-          return false;
+      auto issue_s = [&](int n) -> bool {
+        const int st = n % kFwdKStages;
+        if (!mbar_wait(&k_full[st], (n / kFwdKStages) & 1, &abort_flag)) return false;
         tc_fence_after();
-        return true;
-      };
-      auto issue_s = [&](int n) {
-        const int st = n % kFwdStages;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem, dQ + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s, k > 0);
+          mma_ss(tmem + kFwdColS, dQ + 2 * k, dK0 + st * kTileU + 2 * k, idesc_s, k > 0);
         mma_commit(&s_full);
+        mma_commit(&k_empty[st]);
+        return true;
       };
-      if (ok) ok = kv_ready(0);
-      if (ok) issue_s(0);
+      bool ok = mbar_wait(&q_full, 0, &abort_flag) && issue_s(0);
       for (int n = 0; ok && n < num; ++n) {
-        const int st = n % kFwdStages;
-        // K/V of the next key tile (for S(n+1)); V(n) was waited with K(n).
-        if (n + 1 < num && !kv_ready(n + 1)) { ok = false; break; }
-        if (!mbar_wait(&p_full, n & 1, &abort_flag)) { ok = false; break; }
+        // S(n+1) once S(n) has been read out of TMEM
+        if (n + 1 < num) {
+          if (!mbar_wait(&s_free, n & 1, &abort_flag) || !issue_s(n + 1)) { ok = false; break; }
+        }
+        // PV(n) once P(n) is in TMEM (and O rescaled) and V(n) has landed
+        const int sv = n % kFwdVStages;
+        if (!mbar_wait(&v_full[sv], (n / kFwdVStages) & 1, &abort_flag) ||
+            !mbar_wait(&p_full, n & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t tP = tmem + 64 * c;   // P_c over S
-          const uint32_t tO = tmem + kFwdColO + 64 * c;
-          #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tO, tP + 8 * k, dV0 + st * kTileU + c * kHalfU + 128 * k, idesc_o,
-                   (n > 0 || k > 0));
-        }
-        if (n == num - 1) {
-          mma_commit(&pv_done[0]);
-          mma_commit(&pv_done[1]);
-        } else {
-          issue_s(n + 1);
-        }
-        mma_commit(&kv_empty[st]);
+        for (int k = 0; k < kBlockN / 16; ++k)
+          mma_ts(tmem + kFwdColO, tmem + kFwdColP + 8 * k, dV0 + sv * kTileU + 128 * k, idesc_o,
+                 (n > 0 || k > 0));
+        mma_commit(&pv_done);
+        mma_commit(&v_empty[sv]);
       }
       if (!ok) {
         abort_flag = 1;
@@ -313,109 +338,122 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   } else {
     // ---------------------------------------------------------------- softmax warps
     // Key half c = warp / 4: S columns [64c, 64c+64).  Thread = row = TMEM lane.
-    // Each half keeps its own running max m, sum l and accumulator O_c over the
-    // keys of its half, so the halves never wait for each other inside the loop;
-    // a row's two halves are merged once, in the epilogue (the same merge as two
-    // key blocks of a split softmax).
+    // The two halves of a row share one running max (exchanged through SMEM once
+    // per tile) and one O; each half keeps its own part of the row sum.
     const int c = warp >> 2;
     const int r = tid & 127;
     const int i = i0 + r;                    // row within the sequence
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + 64 * c + lane_base;
-    const uint32_t tP = tS;                                     // P over S_c
-    const uint32_t tO0 = tmem + kFwdColO + lane_base;           // O_0; O_1 at +64
-    const uint32_t tO = tO0 + 64 * c;
+    const uint32_t tS = tmem + kFwdColS + 64 * c + lane_base;
+    const uint32_t tP = tmem + kFwdColP + 32 * c + lane_base;  // P of keys [64c, 64c+64)
+    const uint32_t tO = tmem + kFwdColO + 32 * c + lane_base;  // O columns [32c, 32c+32)
     const bool sink_finite = sink_h > -INFINITY;
-    // running max (log2 domain) starts at the sink logit in both halves; the
-    // sink's term of the sum (1 at m = sink log2 e) is counted in half 0 only
+    // running max (log2 domain) starts at the sink logit; the sink's term of the
+    // sum (1 at m = sink log2 e) is counted in half 0 only
     float m = sink_finite ? sink_h * kLog2e : -INFINITY;
     float l = (sink_finite && c == 0) ? 1.0f : 0.0f;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
     bool ok = true;
     for (int it = 0; it < num; ++it) {
-      if (!mbar_wait_warp(&s_full, it & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int j0 = (lo + it) * kBlockN + 64 * c;              // first key of this half
-      const bool need_mask = (j0 + 64 > sp.nk) ||
-                             (p.causal && (j0 + 63 > i0 + off ||
-                                           (p.window > 0 && j0 <= tile_r1 + off - p.window)));
-      // S of this half, read from TMEM once (each tcgen05.ld competes with the
-      // MMAs for TMEM, so S is not read a second time for the exponentials).
+      // S(it) -> registers; S columns are then free for S(it + 1)
       uint32_t a[64];
-      tmem_ld_x32(tS, a);
-      tmem_ld_x32(tS + 32, a + 32);
-      tmem_ld_wait();
-      if (need_mask) {
-        #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const int j = j0 + e;
-          if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+      bool got = mbar_wait_warp(&s_full, it & 1, &abort_flag);
+      float mx_half = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        tmem_ld_x32(tS, a);
+        tmem_ld_x32(tS + 32, a + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&s_free);
+        const int j0 = (lo + it) * kBlockN + 64 * c;            // first key of this half
+        const bool need_mask = (j0 + 64 > sp.nk) ||
+                               (p.causal && (j0 + 63 > i0 + off ||
+                                             (p.window > 0 && j0 <= tile_r1 + off - p.window)));
+        if (need_mask) {
+          #pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int j = j0 + e;
+            if (j > jmax || j < jmin) a[e] = __float_as_uint(-INFINITY);
+          }
         }
+        // row max over the 64 columns: four independent 3-input max chains
+        float q0 = __uint_as_float(a[0]), q1 = __uint_as_float(a[1]);
+        float q2 = __uint_as_float(a[2]), q3 = __uint_as_float(a[3]);
+        #pragma unroll
+        for (int e = 4; e < 64; e += 8) {
+          q0 = fmax3(q0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
+          q1 = fmax3(q1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
+          q2 = fmax3(q2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
+          q3 = fmax3(q3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
+        }
+        mx_half = fmaxf(fmax3(q0, q1, q2), q3);
+        s_mx[it & 1][c][r] = mx_half;
       }
-      // row max over the 64 columns: four independent 3-input max chains
-      float q0 = __uint_as_float(a[0]), q1 = __uint_as_float(a[1]);
-      float q2 = __uint_as_float(a[2]), q3 = __uint_as_float(a[3]);
-      #pragma unroll
-      for (int e = 4; e < 64; e += 8) {
-        q0 = fmax3(q0, __uint_as_float(a[e]), __uint_as_float(a[e + 1]));
-        q1 = fmax3(q1, __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3]));
-        q2 = fmax3(q2, __uint_as_float(a[e + 4]), __uint_as_float(a[e + 5]));
-        q3 = fmax3(q3, __uint_as_float(a[e + 6]), __uint_as_float(a[e + 7]));
-      }
-      const float mx = fmaxf(fmax3(q0, q1, q2), q3) * sl2;
+      // Both halves of every row meet here once per tile (and leave together if
+      // any warp's wait failed).  The exchange buffer alternates between tiles.
+      if (!named_barrier_and(2, 2 * kBlockM, got && ok)) { ok = false; break; }
+      const float mx = fmaxf(mx_half, s_mx[it & 1][c ^ 1][r]) * sl2;
       // Lazy rescale: the max only moves when it grows by more than the threshold.
       float alpha = 1.0f;
       if (mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY)) {
         alpha = ex2_approx(m - mx);
         m = mx;
       }
-      // S(it) completing implies PV_c(it - 1) completed (issued before it by the
-      // same thread): O_c may be rescaled and P_c overwritten.
-      if (it > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        #pragma unroll
-        for (int q = 0; q < 64; q += 16) {
-          uint32_t o[16];
-          tmem_ld_x16(tO + q, o);
-          tmem_ld_wait();
-          #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_x16(tO + q, o);
-        }
-      }
-      // P = exp2(S * scale * log2 e - m), fp16, over the first 32 columns of this
-      // half of S (already read into registers).  The scale-and-subtract and the
-      // row sum run on pairs of columns (packed fp32 pair instructions), two
-      // running pair sums in turn.
+      // P = exp2(S * scale * log2 e - m), fp16; row sum on pairs of columns
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      const uint64_t sl2x2 = f2(sl2, sl2), negm2 = f2(-m_use, -m_use);
+      const uint64_t negm2 = f2(-m_use, -m_use);
       uint64_t rs = f2(0.0f, 0.0f);
+      uint32_t pk[16];
       #pragma unroll
-      for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t pk[16];
+      for (int e = 0; e < 32; e += 2) {
+        const uint64_t x =
+            ffma2(f2(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), sl2x2, negm2);
+        const float e0 = ex2_approx(f2_lo(x));
+        const float e1 = ex2_approx(f2_hi(x));
+        rs = fadd2(rs, f2(e0, e1));
+        pk[e >> 1] = pack_f16x2(e0, e1);
+      }
+      // PV(it - 1) has read the P columns and updated O
+      if (it > 0 && !mbar_wait_warp(&pv_done, (it - 1) & 1, &abort_flag)) ok = false;
+      if (ok) {
+        tc_fence_after();
+        tmem_st_x16(tP, pk);
         #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const uint64_t x = ffma2(f2(__uint_as_float(a[cc + e]), __uint_as_float(a[cc + e + 1])),
-                                   sl2x2, negm2);
+          const uint64_t x =
+              ffma2(f2(__uint_as_float(a[32 + e]), __uint_as_float(a[33 + e])), sl2x2, negm2);
           const float e0 = ex2_approx(f2_lo(x));
           const float e1 = ex2_approx(f2_hi(x));
           rs = fadd2(rs, f2(e0, e1));
           pk[e >> 1] = pack_f16x2(e0, e1);
         }
-        tmem_st_x16(tP + (cc >> 1), pk);
+        tmem_st_x16(tP + 16, pk);
+        l = l * alpha + (f2_lo(rs) + f2_hi(rs));
+        // O columns [32c, 32c+32) of this row move with the max
+        if (it > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          #pragma unroll
+          for (int q = 0; q < 32; q += 16) {
+            uint32_t o[16];
+            tmem_ld_x16(tO + q, o);
+            tmem_ld_wait();
+            #pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_x16(tO + q, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full);
+      } else {
+        abort_flag = 1;
       }
-      l = l * alpha + (f2_lo(rs) + f2_hi(rs));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full);
     }
-    // Both halves' last PV have landed in O_0 / O_1.
-    bool fin = ok;
-    if (fin)
-      fin = mbar_wait_warp(&pv_done[0], 0, &abort_flag) &&
-            mbar_wait_warp(&pv_done[1], 0, &abort_flag);
-    s_red_m[c][r] = m;
+    // The last PV has landed in O.
+    bool fin = ok && mbar_wait_warp(&pv_done, (num - 1) & 1, &abort_flag);
     s_red_l[c][r] = l;
     fin = named_barrier_and(1, 2 * kBlockM, fin);
     if (!fin) {
@@ -423,23 +461,16 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 3);
     } else {
       tc_fence_after();
-      // merge the halves: m_t = max(m_0, m_1), weights 2^(m_c - m_t)
-      const float m0 = s_red_m[0][r], m1 = s_red_m[1][r];
-      const float mt = fmaxf(m0, m1);
-      const float w0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - mt);
-      const float w1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - mt);
-      const float lt = s_red_l[0][r] * w0 + s_red_l[1][r] * w1;
+      const float lt = s_red_l[0][r] + s_red_l[1][r];
       const float inv_l = (lt > 0.0f) ? 1.0f / lt : 0.0f;
       const bool valid = i < sp.nq;
       const size_t row = (size_t)(sp.q0 + i);
-      // this half writes output columns [32c, 32c + 32); the loads run with the
+      // this half writes output columns [32c, 32c + 32); the load runs with the
       // whole warp (rows past the tail included), only the stores are guarded
-      uint32_t o0[32], o1[32];
-      tmem_ld_x32(tO0 + 32 * c, o0);
-      tmem_ld_x32(tO0 + 64 + 32 * c, o1);
+      uint32_t o[32];
+      tmem_ld_x32(tO, o);
       tmem_ld_wait();
       if (valid) {
-        const float s0 = w0 * inv_l, s1 = w1 * inv_l;
         const size_t base = (row * p.heads_q + h) * kHeadDim + 32 * c;
         uint4* dst = reinterpret_cast<uint4*>(p.out + base);
         uint4* dlo = p.out_lo ? reinterpret_cast<uint4*>(p.out_lo + base) : nullptr;
@@ -448,8 +479,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           float f[8];
           uint32_t hi[4], lo2[4];
           #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            f[e] = __uint_as_float(o0[8 * u + e]) * s0 + __uint_as_float(o1[8 * u + e]) * s1;
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * u + e]) * inv_l;
           #pragma unroll
           for (int e = 0; e < 4; ++e) {
             hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
@@ -459,7 +489,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
           if (dlo) dlo[u] = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
         }
         if (c == 0)
-          p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (mt + __log2f(lt)) * kLn2 : -INFINITY;
+          p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
       }
     }
   }
