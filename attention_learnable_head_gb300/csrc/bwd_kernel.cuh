@@ -33,7 +33,7 @@
 
 namespace attn_sink {
 
-constexpr int kBwdStages = 2;
+constexpr int kBwdStages = 3;       // Q / dO ring depth
 // warps 0-3 compute queries 0-63 of a step, 4-7 queries 64-127, 8 TMA, 9 MMA issuer A
 // (S^T, dP^T, dV), 10-13 dQ, 14 MMA issuer B (dK, dQ)
 constexpr int kBwdThreads = 480;
@@ -42,7 +42,7 @@ constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdDqWarp0 = 10;
 constexpr int kBwdMma2Warp = 14;
 constexpr int kPreRows = 128;      // rows per bwd_pre CTA
-constexpr uint32_t kDqStageBytes = kBlockM * kHeadDim * 4;   // 32 KB fp32 dQ tile
+constexpr uint32_t kDqStageBytes = kBlockM * 32 * 4;   // 16 KB: half of a fp32 dQ tile
 // K, V, kBwdStages x (Q, dO), 2 x dS^T, the dQ staging tile
 constexpr int kBwdSmemBytes = 1024 + 2 * (int)kTileBytes + kBwdStages * 2 * (int)kTileBytes +
                               2 * (int)kPTileBytes + (int)kDqStageBytes;
@@ -303,37 +303,51 @@ __device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, 
   }
 }
 
-// P^T and dS^T of 32 queries of one key row (thread = key), fp16-packed:
-//   P  = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
-//   dS = P (dP - D)
-// nl_row / d_row hold -lse * log2 e and D of the 32 queries.  Pairs of
-// queries go through the packed fp32 pair instructions (scale-and-subtract,
-// dP - D, the product with P); the exponentials stay per element.
-// With kMask, entries whose (query, key) pair is not visible, or whose row or
-// key lies past the sequence, are exact zeros.
+// P^T of 64 queries of one key row (thread = key), fp16-packed:
+//   P = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
+// nl_row holds -lse * log2 e of the 64 queries.  Pairs of queries go through
+// the packed fp32 pair instructions; the exponentials stay per element.  With
+// kMask, entries whose (query, key) pair is not visible, or whose row or key
+// lies past the sequence, are exact zeros.
 template <bool kMask>
-__device__ __forceinline__ void bwd_pds_chunk(const uint32_t* sr, const uint32_t* dr,
-                                              const float* nl_row, const float* d_row,
-                                              uint64_t sl2x2, int i_first, int imin, int imax,
-                                              int nq, bool key_ok, uint32_t* pk, uint32_t* dk) {
+__device__ __forceinline__ void bwd_p_chunk(const uint32_t* sr, const float* nl_row,
+                                            uint64_t sl2x2, int i_first, int imin, int imax,
+                                            int nq, bool key_ok, uint32_t* pk) {
   #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float2 nl = *reinterpret_cast<const float2*>(nl_row + e);
-    const float2 dd = *reinterpret_cast<const float2*>(d_row + e);
-    const uint64_t x =
-        ffma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, f2(nl.x, nl.y));
-    float p0 = ex2_approx(f2_lo(x));
-    float p1 = ex2_approx(f2_hi(x));
-    if (kMask) {
-      const int i = i_first + e;
-      if (!key_ok || i < imin || i > imax || i >= nq) p0 = 0.0f;
-      if (!key_ok || i + 1 < imin || i + 1 > imax || i + 1 >= nq) p1 = 0.0f;
+  for (int e = 0; e < 64; e += 4) {
+    const float4 nl = *reinterpret_cast<const float4*>(nl_row + e);
+    #pragma unroll
+    for (int u = 0; u < 4; u += 2) {
+      const uint64_t x = ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])),
+                               sl2x2, u == 0 ? f2(nl.x, nl.y) : f2(nl.z, nl.w));
+      float p0 = ex2_approx(f2_lo(x));
+      float p1 = ex2_approx(f2_hi(x));
+      if (kMask) {
+        const int i = i_first + e + u;
+        if (!key_ok || i < imin || i > imax || i >= nq) p0 = 0.0f;
+        if (!key_ok || i + 1 < imin || i + 1 > imax || i + 1 >= nq) p1 = 0.0f;
+      }
+      pk[(e + u) >> 1] = pack_f16x2(p0, p1);
     }
-    const uint64_t ds =
-        fmul2(f2(p0, p1), fsub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                f2(dd.x, dd.y)));
-    pk[e >> 1] = pack_f16x2(p0, p1);
-    dk[e >> 1] = pack_f16x2(f2_lo(ds), f2_hi(ds));
+  }
+}
+
+// dS^T = P^T o (dP^T - D) of 32 queries of one key row, fp16-packed, from the
+// fp16 P^T this thread stored for the dV product (pk, 16 words), dP^T (dr) and
+// the queries' D (d_row).  Masked entries have P = 0, hence dS = 0.
+__device__ __forceinline__ void bwd_ds_chunk(const uint32_t* dr, const uint32_t* pk,
+                                             const float* d_row, uint32_t* dk) {
+  #pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    const float4 dd = *reinterpret_cast<const float4*>(d_row + e);
+    #pragma unroll
+    for (int u = 0; u < 4; u += 2) {
+      const uint64_t pp = f16x2_to_f2(pk[(e + u) >> 1]);
+      const uint64_t ds = fmul2(
+          pp, fsub2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                    u == 0 ? f2(dd.x, dd.y) : f2(dd.z, dd.w)));
+      dk[(e + u) >> 1] = pack_f16x2(f2_lo(ds), f2_hi(ds));
+    }
   }
 }
 
@@ -342,7 +356,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t kv_full, kv_tmem, mma2_done, drained;
   __shared__ __align__(8) uint64_t q_full[kBwdStages], q_empty[kBwdStages];
-  __shared__ __align__(8) uint64_t s_full[2], p_full[2], ds_free[2];
+  __shared__ __align__(8) uint64_t s_full, dp_full, p_ready, ds_ready, dq_free;
+  __shared__ __align__(8) uint64_t ds_free[2], dpt_issued[2];
   __shared__ __align__(16) float s_nL[kBwdStages][kBlockM];   // -lse * log2 e of the step's rows
   __shared__ __align__(16) float s_D[kBwdStages][kBlockM];    // D of the step's rows
   __shared__ uint32_t tmem_base_sh;
@@ -392,7 +407,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint8_t* sQ = sV + kTileBytes;                      // kBwdStages tiles
   uint8_t* sdO = sQ + kBwdStages * kTileBytes;        // kBwdStages tiles
   uint8_t* sdS = sdO + kBwdStages * kTileBytes;       // 2 x [128 keys][128 queries] fp16
-  uint8_t* sdQ = sdS + 2 * kPTileBytes;                // 2 x [128 queries][32] fp32, swizzled
+  uint8_t* sdQ = sdS + 2 * kPTileBytes;                // [128 queries][32] fp32, swizzled
 
   if (tid == 0) {
     abort_flag = 0;
@@ -404,13 +419,15 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&q_full[s], 1 + 32);      // TMA arrival + 32 lanes' cp.async (lse / D)
       mbar_init(&q_empty[s], 2);          // read by both issuers' MMAs
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&ds_free[b], 1);   // dS^T buffer b read
-    for (int hh = 0; hh < 2; ++hh) {
-      mbar_init(&s_full[hh], 1);
-      // half 1 also waits for the dQ warps to have read the previous dQ out of
-      // TMEM (they arrive on it), so the MMA issuers need no separate wait
-      mbar_init(&p_full[hh], kBlockN + (hh == 1 && !p.skip_dq ? kBlockM : 0));
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ds_free[b], 1);          // dS^T buffer b read by issuer B's MMAs
+      mbar_init(&dpt_issued[b], 1);       // issuer A has issued the next dP^T
     }
+    mbar_init(&s_full, 1);
+    mbar_init(&dp_full, 1);
+    mbar_init(&p_ready, 2 * kBlockN);     // both compute warpgroups
+    mbar_init(&ds_ready, 2 * kBlockN);
+    mbar_init(&dq_free, kBlockM);         // the dQ warps have read dQ out of TMEM
     fence_mbarrier_init();
   }
   if (warp == kBwdMmaWarp) {
@@ -452,7 +469,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tma_load_3d(&p.tm_do, &q_full[st], sdO + st * kTileBytes, 0, h, sp.q0 + i0);
       }
       // (-lse log2 e, D) of the step's 128 query rows, copied asynchronously into
-      // two planes (so that pairs of rows load as one 8-byte word); rows past the
+      // two planes (so that runs of rows load as one vector); rows past the
       // sequence read a valid row and are masked by the compute warps.
       #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -472,17 +489,21 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     }
   } else if (warp == kBwdMmaWarp || warp == kBwdMma2Warp) {
     // ---------------------------------------------------------------- MMA issuers
-    // Two issuing threads, so that one issuer's mbarrier waits (each leaves the
-    // tensor pipe idle for ~200 cycles) are covered by the other's MMAs.  Each
-    // accumulator has one issuer, whose MMAs run in issue order:
-    //   A (warp 9):  S^T / dP^T of every half, dV += P^T dO
-    //   B (warp 14): dK += dS^T Q, dQ = dS K
-    // A reads K, V and P^T from TMEM and the Q / dO stage; B reads the dS^T SMEM
-    // buffer, the Q stage and K.  A stage is refilled once both issuers' commits
-    // on q_empty have landed; B's commit on ds_free[b] releases dS^T buffer b.
+    // Each step (one query head, 128 queries) splits the compute warps' work in
+    // two phases, P^T then dS^T, so that the products waiting on P^T start
+    // while dS^T is still being formed.  Two issuing threads, each owning its
+    // accumulators so that its MMAs run in issue order:
+    //   A (warp 9):  dV += P^T dO (after phase 1), S^T of the next step (into
+    //                the columns phase 1 has read), dP^T of the next step (after
+    //                phase 2 has read dP^T), all N = 128 / K = 128 queries
+    //   B (warp 14): dK += dS^T Q, dQ = dS K (after phase 2), once A has issued
+    //                the next dP^T, so that the compute warps' next operand is
+    //                ahead of them in the tensor pipe
+    // A stage of Q/dO is refilled once both issuers' commits on q_empty have
+    // landed; B's commit on ds_free[b] releases dS^T buffer b two steps later.
     if (lane == 0) {
       const bool issuer_a = warp == kBwdMmaWarp;
-      const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM / 2, false, false);
+      const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM, false, false);
       const uint32_t id_dvdk = make_idesc(kFmtF16, kBlockN, kHeadDim, false, true);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, true, true);
       // Shared-memory descriptors, built once; an operand at byte offset o from
@@ -495,16 +516,20 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const uint64_t dS_k = make_sdesc_sw128(smem_u32(sdS), 16, 1024);     // buffer 0
       const uint64_t dS_mn = make_sdesc_sw128(smem_u32(sdS), 16384, 1024);
       constexpr uint32_t kTileU = kTileBytes >> 4, kPTileU = kPTileBytes >> 4;
-      // S^T / dP^T for the query half hh of step m (64 queries, N = 64).
-      auto issue_s = [&](int m, int hh) {
-        const uint32_t qo = (m % kBwdStages) * kTileU + hh * (kTileU / 2);
+      // S^T = K Q^T or dP^T = V dO^T of step m over its 128 queries (N = 128).
+      auto issue_s = [&](int m) {
+        const uint32_t qo = (m % kBwdStages) * kTileU;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ts(tmem + kColST + 64 * hh, tmem + kColK + 8 * k, dQ_k + qo + 2 * k, id_s, k > 0);
+          mma_ts(tmem + kColST, tmem + kColK + 8 * k, dQ_k + qo + 2 * k, id_s, k > 0);
+        mma_commit(&s_full);
+      };
+      auto issue_dp = [&](int m) {
+        const uint32_t qo = (m % kBwdStages) * kTileU;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ts(tmem + kColDPT + 64 * hh, tmem + kColV + 8 * k, dO_k + qo + 2 * k, id_s, k > 0);
-        mma_commit(&s_full[hh]);
+          mma_ts(tmem + kColDPT, tmem + kColV + 8 * k, dO_k + qo + 2 * k, id_s, k > 0);
+        mma_commit(&dp_full);
       };
       bool ok = true;
       if (issuer_a) {
@@ -512,57 +537,61 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         ok = mbar_wait(&kv_tmem, 0, &abort_flag) && mbar_wait(&q_full[0], 0, &abort_flag);
         if (ok) {
           tc_fence_after();
-          issue_s(0, 0);
-          issue_s(0, 1);
+          issue_s(0);
+          issue_dp(0);
         }
-      }
-      for (int m = 0; ok && m < num; ++m) {
-        const int st = m % kBwdStages;
-        const uint32_t so = (m & 1) * kPTileU;            // dS^T buffer of this step
-        const bool more = m + 1 < num;
-        for (int hh = 0; hh < 2; ++hh) {
-          // p_full[hh]: this half's P^T is in TMEM and its dS^T in SMEM (for half
-          // 1 also: the dQ warps have read the previous dQ out of TMEM)
-          if (!mbar_wait(&p_full[hh], m & 1, &abort_flag)) { ok = false; break; }
+        for (int m = 0; ok && m < num; ++m) {
+          const int st = m % kBwdStages;
+          const bool more = m + 1 < num;
+          // phase 1 done: P^T in TMEM (over the S^T columns it has read)
+          if (!mbar_wait(&p_ready, m & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
-          // B operands step 16 query rows (2048 bytes) per k (K = 64 queries)
-          const uint32_t ho = st * kTileU + hh * (kTileU / 2);
-          if (issuer_a) {
-            // dV += P^T dO over this half's 64 queries
-            #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ts(tmem + kColDV, tmem + kColST + 64 * hh + 8 * k, dO_mn + ho + 128 * k,
-                     id_dvdk, (m > 0 || hh > 0 || k > 0));
-            if (hh == 1) mma_commit(&q_empty[st]);
-            if (more) {
-              // next step's half hh: its S^T / dP^T columns were read by this half
-              // (Q / dO of the next step are waited for once, before its half 0)
-              if (hh == 0 && !mbar_wait(&q_full[(m + 1) % kBwdStages],
-                                        ((m + 1) / kBwdStages) & 1, &abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_s(m + 1, hh);
+          // dV += P^T dO over the step's 128 queries; P^T of queries 64hh.. sits
+          // in the first 32 columns of S^T half hh
+          #pragma unroll
+          for (int k = 0; k < kBlockM / 16; ++k)
+            mma_ts(tmem + kColDV, tmem + kColST + 64 * (k >> 2) + 8 * (k & 3),
+                   dO_mn + st * kTileU + 128 * k, id_dvdk, (m > 0 || k > 0));
+          mma_commit(&q_empty[st]);
+          if (more) {
+            if (!mbar_wait(&q_full[(m + 1) % kBwdStages], ((m + 1) / kBwdStages) & 1,
+                           &abort_flag)) {
+              ok = false;
+              break;
             }
-          } else {
-            // dK += dS^T Q over this half's 64 queries
-            #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + kColDK, dS_k + so + hh * kTileU + 2 * k, dQ_mn + ho + 128 * k,
-                     id_dvdk, (m > 0 || hh > 0 || k > 0));
-            if (hh == 1) {
-              if (!p.skip_dq) {
-                // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
-                #pragma unroll
-                for (int k = 0; k < kBlockN / 16; ++k)
-                  mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
-                mma_commit(&mma2_done);
-              }
-              mma_commit(&ds_free[m & 1]);
-              mma_commit(&q_empty[st]);
-            }
+            tc_fence_after();
+            issue_s(m + 1);
           }
+          // phase 2 done: dS^T in SMEM, dP^T read
+          if (!mbar_wait(&ds_ready, m & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (more) issue_dp(m + 1);
+          mbar_arrive(&dpt_issued[m & 1]);
+        }
+      } else {
+        for (int m = 0; ok && m < num; ++m) {
+          const int st = m % kBwdStages;
+          const uint32_t so = (m & 1) * kPTileU;            // dS^T buffer of this step
+          // A has seen phase 2 of this step and issued the next dP^T
+          if (!mbar_wait(&dpt_issued[m & 1], (m >> 1) & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // dK += dS^T Q over the step's 128 queries (dS^T tile hh holds queries 64hh..)
+          #pragma unroll
+          for (int k = 0; k < kBlockM / 16; ++k)
+            mma_ss(tmem + kColDK, dS_k + so + (k >> 2) * kTileU + 2 * (k & 3),
+                   dQ_mn + st * kTileU + 128 * k, id_dvdk, (m > 0 || k > 0));
+          if (!p.skip_dq) {
+            // the dQ warps have read the previous dQ out of TMEM
+            if (!mbar_wait(&dq_free, m & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            // dQ = dS K  (A: dS^T read MN-major, M = queries; B: K read MN-major)
+            #pragma unroll
+            for (int k = 0; k < kBlockN / 16; ++k)
+              mma_ss(tmem + kColDQ, dS_mn + so + 128 * k, dK_mn + 128 * k, id_dq, k > 0);
+            mma_commit(&mma2_done);
+          }
+          mma_commit(&ds_free[m & 1]);
+          mma_commit(&q_empty[st]);
         }
       }
       if (!ok) {
@@ -603,17 +632,15 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     }
     tc_fence_before();
     mbar_arrive(&kv_tmem);
+    const uint32_t tST = tmem + lane_base + kColST + 64 * hh;
+    const uint32_t tDPT = tmem + lane_base + kColDPT + 64 * hh;
     for (int m = 0; ok && m < num; ++m) {
       const int st = m % kBwdStages;
       const int i0 = (qt_first + m % nqt) * kBlockM + 64 * hh;   // first query of this half
       // q_full: the producer's lse / D rows of this step are in SMEM.
-      // s_full: this half's S^T / dP^T, and every earlier MMA of issuer A (dV,
-      // the reader of the P^T half) has completed.
-      // ds_free: issuer B's MMAs of step m - 2 (the last readers of this step's
-      // dS^T buffer) have completed; buffer m & 1 is released once per two steps.
+      // s_full: S^T of this step (and every earlier MMA of issuer A) has completed.
       if (!mbar_wait_warp(&q_full[st], (m / kBwdStages) & 1, &abort_flag) ||
-          !mbar_wait_warp(&s_full[hh], m & 1, &abort_flag) ||
-          (m >= 2 && !mbar_wait_warp(&ds_free[m & 1], ((m >> 1) - 1) & 1, &abort_flag))) {
+          !mbar_wait_warp(&s_full, m & 1, &abort_flag)) {
         ok = false;
         break;
       }
@@ -621,36 +648,53 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const bool need_mask = (j0 + kBlockN > sp.nk) || (i0 + 64 > sp.nq) ||
                              (p.causal && (j0 + kBlockN - 1 > i0 + off ||
                                            (p.window > 0 && j0 <= i0 + 63 + off - p.window)));
+      // Phase 1: P^T of this half's 64 queries, written (fp16) over the first 32
+      // S^T columns of the half once S^T has been read.  The mask test is hoisted
+      // out of the element loop (a branch per element keeps the compiler from
+      // interleaving the elements' exponentials).
+      uint32_t pk[32];
+      {
+        uint32_t sr[64];
+        tmem_ld_x32(tST, sr);
+        tmem_ld_x32(tST + 32, sr + 32);
+        tmem_ld_wait();
+        const float* nl_row = &s_nL[st][64 * hh];
+        if (need_mask)
+          bwd_p_chunk<true>(sr, nl_row, sl2x2, i0, imin, imax, sp.nq, key_ok, pk);
+        else
+          bwd_p_chunk<false>(sr, nl_row, sl2x2, i0, imin, imax, sp.nq, key_ok, pk);
+      }
+      tmem_st_x16(tST, pk);
+      tmem_st_x16(tST + 16, pk + 16);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_ready);
+      // Phase 2: dS^T = P^T o (dP^T - D) into the step's SMEM buffer.
+      // dp_full: dP^T of this step has completed.  ds_free: issuer B's MMAs of
+      // step m - 2 (the last readers of this step's dS^T buffer) have completed;
+      // buffer m & 1 is released once per two steps.
+      if (!mbar_wait_warp(&dp_full, m & 1, &abort_flag) ||
+          (m >= 2 && !mbar_wait_warp(&ds_free[m & 1], ((m >> 1) - 1) & 1, &abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       const uint32_t sbase = smem_u32(sdS + (m & 1) * kPTileBytes) + hh * kTileBytes;
       #pragma unroll
       for (int c = 0; c < 64; c += 32) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tmem + lane_base + kColST + 64 * hh + c, sr);
-        tmem_ld_x32(tmem + lane_base + kColDPT + 64 * hh + c, dr);
+        uint32_t dr[32], dk[16];
+        tmem_ld_x32(tDPT + c, dr);
         tmem_ld_wait();
-        uint32_t pk[16], dk[16];
-        // The mask test is hoisted out of the element loop (a branch per element
-        // keeps the compiler from interleaving the elements' exponentials).
-        const float* nl_row = &s_nL[st][64 * hh + c];
-        const float* d_row = &s_D[st][64 * hh + c];
-        if (need_mask)
-          bwd_pds_chunk<true>(sr, dr, nl_row, d_row, sl2x2, i0 + c, imin, imax, sp.nq, key_ok,
-                              pk, dk);
-        else
-          bwd_pds_chunk<false>(sr, dr, nl_row, d_row, sl2x2, i0 + c, imin, imax, sp.nq, key_ok,
-                               pk, dk);
-        // P^T over S^T columns this thread has already read (chunk c -> c / 2)
-        tmem_st_x16(tmem + lane_base + kColST + 64 * hh + (c >> 1), pk);
+        bwd_ds_chunk(dr, pk + (c >> 1), &s_D[st][64 * hh + c], dk);
         // dS^T row r, queries c..c+31 of this half: 4 chunks of 16 bytes
         #pragma unroll
         for (int u = 0; u < 4; ++u)
           st_shared_v4(sbase + sw128_offset(r, (c >> 3) + u), dk[4 * u], dk[4 * u + 1],
                        dk[4 * u + 2], dk[4 * u + 3]);
       }
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[hh]);
+      mbar_arrive(&ds_ready);
     }
     // `drained` completes once, after the MMA warp's last commit: every MMA into
     // dK / dV has landed.  (A parity wait on the per-step barriers could be two
@@ -675,10 +719,10 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   } else if (warp >= kBwdDqWarp0 && warp < kBwdDqWarp0 + 4) {
     // ---------------------------------------------------------------- dQ warps
     // Each step's dQ tile (128 queries x 64, fp32, times the softmax scale) is
-    // staged in SMEM (two 128-byte-swizzled halves of 32 columns) and added to the
-    // fp32 accumulator with two TMA reduce-adds.  Rows past the sequence end are
-    // exact zeros (their dS is masked), so adding them into the next sequence's
-    // rows changes nothing.
+    // read out of TMEM and added to the fp32 accumulator in two halves of 32
+    // columns, each staged in one 128-byte-swizzled SMEM tile and summed by a
+    // TMA reduce-add.  Rows past the sequence end are exact zeros (their dS is
+    // masked), so adding them into the next sequence's rows changes nothing.
     const int r = 32 * (warp & 3) + lane;            // query row in tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const bool leader = (warp == kBwdDqWarp0 && lane == 0);
@@ -686,13 +730,11 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     bool ok = true;
     // (with skip_dq there is no dQ here: the loop does not run)
     // The dQ TMEM columns are free for step 0.
-    if (!p.skip_dq && num > 0) mbar_arrive(&p_full[1]);
+    if (!p.skip_dq && num > 0) mbar_arrive(&dq_free);
     for (int m = 0; m < (p.skip_dq ? 0 : num); ++m) {
       const int h = h_first + m / nqt;
       const int i0 = (qt_first + m % nqt) * kBlockM;
       const bool waited = mbar_wait_warp(&mma2_done, m & 1, &abort_flag);
-      // the previous step's reduce-adds have read the staging tile
-      if (leader) bulk_wait_group_read0();
       // all four warps agree on the wait's outcome (and leave together)
       if (!named_barrier_and(1, 128, waited)) { ok = false; break; }
       tc_fence_after();
@@ -701,26 +743,28 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tmem_ld_x32(tmem + lane_base + kColDQ + 32, v + 32);
       tmem_ld_wait();
       tc_fence_before();
-      // dQ TMEM is free for the next step: arrive on its half-1 P barrier
-      if (m + 1 < num) mbar_arrive(&p_full[1]);
+      // dQ TMEM is free for the next step
+      if (m + 1 < num) mbar_arrive(&dq_free);
       #pragma unroll
       for (int half = 0; half < 2; ++half) {
+        // the previous reduce-add has read the staging tile
+        if (leader) bulk_wait_group_read0();
+        named_barrier_sync(1, 128);
         #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t* w = v + 32 * half + 4 * c;
-          st_shared_v4(stage + half * (kDqStageBytes / 2) + sw128_offset(r, c),
+          st_shared_v4(stage + sw128_offset(r, c),
                        __float_as_uint(__uint_as_float(w[0]) * p.scale),
                        __float_as_uint(__uint_as_float(w[1]) * p.scale),
                        __float_as_uint(__uint_as_float(w[2]) * p.scale),
                        __float_as_uint(__uint_as_float(w[3]) * p.scale));
         }
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 128);
-      if (leader) {
-        tma_reduce_add_3d(&p.tm_dq, sdQ, 0, h, sp.q0 + i0);
-        tma_reduce_add_3d(&p.tm_dq, sdQ + kDqStageBytes / 2, 32, h, sp.q0 + i0);
-        bulk_commit_group();
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (leader) {
+          tma_reduce_add_3d(&p.tm_dq, sdQ, 32 * half, h, sp.q0 + i0);
+          bulk_commit_group();
+        }
       }
     }
     if (leader) bulk_wait_group0();

@@ -393,9 +393,14 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
         mx_half = fmaxf(fmax3(q0, q1, q2), q3);
         s_mx[it & 1][c][r] = mx_half;
       }
-      // Both halves of every row meet here once per tile (and leave together if
-      // any warp's wait failed).  The exchange buffer alternates between tiles.
-      if (!named_barrier_and(2, 2 * kBlockM, got && ok)) { ok = false; break; }
+      // The two warps that hold the halves of the same 32 rows (w and w + 4) meet
+      // here once per tile, and leave together if either's wait failed.  The
+      // exchange buffer alternates between tiles.
+      if (!named_barrier_and(2 + (warp & 3), 64, got && ok)) {
+        ok = false;
+        abort_flag = 1;   // the other warp pairs stop at their next wait
+        break;
+      }
       const float mx = fmaxf(mx_half, s_mx[it & 1][c ^ 1][r]) * sl2;
       // Lazy rescale: the max only moves when it grows by more than the threshold.
       float alpha = 1.0f;

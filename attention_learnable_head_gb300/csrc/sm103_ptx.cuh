@@ -505,6 +505,18 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Two fp16 (one 32-bit word, low half first) widened to an fp32 pair exactly.
+__device__ __forceinline__ uint64_t f16x2_to_f2(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return f2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
