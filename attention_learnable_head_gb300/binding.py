@@ -83,7 +83,15 @@ def lib():
         raise RuntimeError(
             f"{LIB_PATH} is missing: build it with "
             "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
-    L = ctypes.CDLL(LIB_PATH)
+    _LIB = load_library(LIB_PATH)
+    return _LIB
+
+
+def load_library(path: str):
+    """A ctypes handle on a build of the library at `path` with the C
+    signatures of include/attn_sink.h attached (the product library, or the
+    test build that also exports attn_sink_test_withhold)."""
+    L = ctypes.CDLL(path)
     P = ctypes.POINTER(AttnSinkParams)
     L.attn_sink_fwd.argtypes = [P, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
@@ -132,7 +140,9 @@ def lib():
     L.attn_sink_kernel_time.argtypes = [c_int, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_ulonglong)]
     L.attn_sink_kernel_time.restype = c_int
-    _LIB = L
+    if hasattr(L, "attn_sink_test_withhold"):
+        L.attn_sink_test_withhold.argtypes = [c_int, c_int]
+        L.attn_sink_test_withhold.restype = c_int
     return L
 
 

@@ -11,6 +11,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libattn_sink.so")
+# Test build: the same sources with the bounded waits lowered to 2 ms and the
+# hooks that let a test withhold one tile (exercises the timeout path).
+TEST_LIB_PATH = os.path.join(LIB_DIR, "libattn_sink_test.so")
+TEST_FLAGS = ["-DATTN_SINK_TEST_HOOKS", "-DATTN_SINK_WAIT_LIMIT_NS=2000000ull"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,16 +32,19 @@ def _sources() -> list[str]:
     return files
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build the shared library if any source is newer than it; return its path."""
+def build(force: bool = False, verbose: bool = False, test: bool = False) -> str:
+    """Build the shared library (or, with test=True, the test build) if any
+    source is newer than it; return its path."""
+    path = TEST_LIB_PATH if test else LIB_PATH
     srcs = _sources()
-    if (not force and os.path.exists(LIB_PATH)
-            and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(s) for s in srcs)):
-        return LIB_PATH
+    if (not force and os.path.exists(path)
+            and os.path.getmtime(path) >= max(os.path.getmtime(s) for s in srcs)):
+        return path
     os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = LIB_PATH + ".tmp"
+    tmp = path + ".tmp"
     cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-           "-shared", "-I", INCLUDE, "-o", tmp, os.path.join(CSRC, "attn_sink_api.cu")]
+           "-shared", "-I", INCLUDE, *(TEST_FLAGS if test else []), "-o", tmp,
+           os.path.join(CSRC, "attn_sink_api.cu")]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
@@ -46,8 +53,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
     if verbose:
         print(res.stdout + res.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":

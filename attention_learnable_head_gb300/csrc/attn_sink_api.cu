@@ -99,6 +99,12 @@ void timing_end(const TimedLaunch& t, cudaStream_t s, bool ok) {
   }
 }
 
+#ifdef ATTN_SINK_TEST_HOOKS
+// Test build only: tiles the next launches withhold (see attn_sink_test_withhold).
+std::atomic<int> g_test_skip_k_tile{-1};
+std::atomic<int> g_test_skip_q_step{-1};
+#endif
+
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -392,6 +398,9 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   fp.chunk = chunk ? 1 : 0;
   fp.q_pos0 = chunk ? q_pos0 : 0;
   fp.n_qtiles = (g.max_q + kBlockM - 1) / kBlockM;
+#ifdef ATTN_SINK_TEST_HOOKS
+  fp.skip_k_tile = g_test_skip_k_tile.load();
+#endif
   if (fp.n_qtiles == 0) return ATTN_SINK_OK;
   dim3 grid(params->heads_q, g.num_seqs, fp.n_qtiles);
   const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_FWD, static_cast<cudaStream_t>(stream));
@@ -724,6 +733,9 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
     bp.n_ktiles = n_ktiles;
     bp.grad_fp32 = params->grad_dtype;
     bp.skip_dq = deterministic ? 1 : 0;
+#ifdef ATTN_SINK_TEST_HOOKS
+    bp.skip_q_step = g_test_skip_q_step.load();
+#endif
     dim3 grid(params->heads_kv * L.split, g.num_seqs, n_ktiles);
     const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_BWD_MAIN, s);
     attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
@@ -868,6 +880,18 @@ int attn_sink_fwd_noalloc(const attn_sink_params* params, const void* q, const v
   return attn_sink_fwd(params, q, k, v, sink, cu_seqlens_q, cu_seqlens_k, out, out_residual, lse,
                        ptr, (size_t)ATTN_SINK_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+#ifdef ATTN_SINK_TEST_HOOKS
+// Test build only (not in attn_sink.h): from the next launch on, the forward's
+// producer withholds K tile `fwd_k_tile` of every CTA and the backward's
+// producer the Q/dO tiles of step `bwd_q_step` (-1: none), so that the waits
+// for them run out and the bounded-wait path returns an error code.
+int attn_sink_test_withhold(int fwd_k_tile, int bwd_q_step) {
+  g_test_skip_k_tile.store(fwd_k_tile);
+  g_test_skip_q_step.store(bwd_q_step);
+  return ATTN_SINK_OK;
+}
+#endif
 
 int attn_sink_kernel_timing(int on) {
   g_timing_on.store(on != 0, std::memory_order_relaxed);

@@ -82,6 +82,9 @@ struct BwdParams {
   int n_ktiles;        // key tiles of the longest sequence
   int grad_fp32;
   int skip_dq;         // 1: no dQ here (the deterministic dQ kernel computes it)
+#ifdef ATTN_SINK_TEST_HOOKS
+  int skip_q_step;     // test build: the producer never loads this step's Q/dO (-1: none)
+#endif
 };
 
 // ------------------------------------------------------------------ bwd_pre
@@ -463,6 +466,18 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
       }
       const int h = h_first + m / nqt;
       const int i0 = (qt_first + m % nqt) * kBlockM;
+#ifdef ATTN_SINK_TEST_HOOKS
+      if (m == p.skip_q_step) {
+        // test build: withhold this step's tiles; every wait for them runs out
+        const unsigned long long t0 = global_timer_ns();
+        while (!abort_flag && global_timer_ns() - t0 <= kWaitLimitNs) __nanosleep(1000);
+        if (lane == 0) {
+          abort_flag = 1;
+          atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 1);
+        }
+        break;
+      }
+#endif
       if (lane == 0) {
         mbar_arrive_expect_tx(&q_full[st], 2 * kTileBytes);
         tma_load_3d(&p.tm_q, &q_full[st], sQ + st * kTileBytes, 0, h, sp.q0 + i0);

@@ -53,6 +53,14 @@ constexpr int kHeadDim = 64;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 16 KB bf16 tile
 constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bwd dS)
 
+#ifdef ATTN_SINK_TEST_HOOKS
+// test build: K tile n is issued unless the params say to withhold it, so that
+// the waits for it run out (the bounded-wait path is exercised without a fault)
+#define TEST_HOOK_FWD_ISSUE_K(n) ((n) != p.skip_k_tile)
+#else
+#define TEST_HOOK_FWD_ISSUE_K(n) true
+#endif
+
 constexpr int kFwdKStages = 3;      // K ring depth
 constexpr int kFwdVStages = 2;      // V ring depth
 constexpr int kFwdThreads = 320;    // 8 softmax warps, TMA warp, MMA warp
@@ -89,6 +97,9 @@ struct FwdParams {
   // position i + q_pos0 (the default is bottom-right: q_pos0 = N_k - N_q).
   int chunk;
   int q_pos0;
+#ifdef ATTN_SINK_TEST_HOOKS
+  int skip_k_tile;    // test build: the producer never issues this K tile (-1: none)
+#endif
 };
 
 struct SeqSpan {
@@ -237,7 +248,7 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       while (nk < num || nv < num) {
         bool progress = false;
         // K(nk): its stage was last read by S(nk - 3)
-        if (nk < num && (nk < kFwdKStages ||
+        if (nk < num && TEST_HOOK_FWD_ISSUE_K(nk) && (nk < kFwdKStages ||
                          mbar_test_wait(smem_u32(&k_empty[nk % kFwdKStages]),
                                         ((nk / kFwdKStages) & 1) ^ 1))) {
           const int st = nk % kFwdKStages;

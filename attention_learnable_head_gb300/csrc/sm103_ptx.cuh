@@ -32,8 +32,13 @@ enum : int {
 };
 
 // Give up on an mbarrier after this many nanoseconds.  Every legitimate wait
-// in these kernels lasts microseconds; a full launch lasts milliseconds.
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+// in these kernels lasts microseconds; a full launch lasts milliseconds.  The
+// test build of the library lowers it (ATTN_SINK_WAIT_LIMIT_NS) so that a test
+// can make a wait run out quickly.
+#ifndef ATTN_SINK_WAIT_LIMIT_NS
+#define ATTN_SINK_WAIT_LIMIT_NS (1000ull * 1000ull * 1000ull)
+#endif
+constexpr unsigned long long kWaitLimitNs = ATTN_SINK_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -32,6 +32,18 @@ def test_exports_every_declared_symbol():
     lib = binding.lib()
     for n in names:
         assert hasattr(lib, n), n
+    # the tile-withholding hook exists only in the test build
+    assert not hasattr(lib, "attn_sink_test_withhold")
+
+
+def test_test_build_exports_the_withholding_hook():
+    """The test build (waits lowered to 2 ms, one tile can be withheld) exports
+    every declared entry point plus attn_sink_test_withhold."""
+    from attention_learnable_head_gb300.build import build
+    L = binding.load_library(build(test=True))
+    for n in binding.header_functions():
+        assert hasattr(L, n), n
+    assert L.attn_sink_test_withhold(-1, -1) == 0
 
 
 def test_params_struct_layout():
