@@ -2,6 +2,7 @@
 // launch configuration and workspace carving for the C ABI in attn_sink.h.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cmath>
@@ -158,6 +159,16 @@ int device_state(int* sm_count, int** err) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An NVTX range around one entry point's host work (validation, tensor maps,
+// launches), so that a profiler's timeline names the library's calls.  NVTX is
+// header-only here: without a profiler attached a range costs a branch.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Problem geometry resolved from the params (dense or packed).
 struct Geometry {
@@ -340,6 +351,7 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
              const void* sink, const int* cu_seqlens_q, const int* cu_seqlens_k, void* out,
              void* out_residual, float* lse, void* workspace, size_t workspace_bytes,
              void* stream, bool chunk, int q_pos0, bool sink_bf16) {
+  NvtxRange range(chunk ? "attn_sink_fwd_chunk" : "attn_sink_fwd");
   Geometry g;
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
@@ -443,6 +455,7 @@ int attn_sink_fwd_chunk(const attn_sink_params* params, int q_pos0, const void* 
 int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, const void* o_parts,
                     const void* o_residual_parts, const float* lse_parts, const float* sink,
                     void* out, void* out_residual, float* lse, void* stream) {
+  NvtxRange range("attn_sink_merge");
   if (num_chunks < 1 || total_q < 0 || heads_q < 1) return ATTN_SINK_ERR_INVALID_ARG;
   if (head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
   if (total_q == 0) return ATTN_SINK_OK;
@@ -529,6 +542,7 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
                      const void* v_cache, const int* block_table, const int* seq_lens,
                      const float* sink, void* out, void* out_residual, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange range("attn_sink_decode");
   if (params == nullptr) return ATTN_SINK_ERR_INVALID_ARG;
   if (params->head_dim != kHeadDim) return ATTN_SINK_ERR_UNSUPPORTED;
   // launch-grid limits: kv heads in grid.y, sequences in grid.z
@@ -624,6 +638,7 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
              void* dq, void* dk, void* dv, void* dsink, void* workspace,
              size_t workspace_bytes, void* stream, int flags) {
   const bool deterministic = (flags & ATTN_SINK_FLAG_DETERMINISTIC) != 0;
+  NvtxRange range(deterministic ? "attn_sink_bwd_deterministic" : "attn_sink_bwd");
   const bool sink_bf16 = (flags & ATTN_SINK_FLAG_SINK_BF16) != 0;
   const bool accumulate = (flags & ATTN_SINK_FLAG_ACCUMULATE_DSINK) != 0;
   Geometry g;
