@@ -751,7 +751,7 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
 #ifdef ATTN_SINK_TEST_HOOKS
     bp.skip_q_step = g_test_skip_q_step.load();
 #endif
-    dim3 grid(params->heads_kv * L.split, g.num_seqs, n_ktiles);
+    dim3 grid(params->heads_kv * L.split, n_ktiles, g.num_seqs);
     const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_BWD_MAIN, s);
     attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
     const bool ok = launched();

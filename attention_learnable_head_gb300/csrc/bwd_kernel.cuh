@@ -370,8 +370,10 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   const int part = blockIdx.x % p.split;   // which slice of the GQA group
   const int hpc = p.group / p.split;       // query heads handled by this CTA
   const int h_first = g * p.group + part * hpc;
-  const int seq = blockIdx.y;
-  const int ktile = blockIdx.z;            // low key tiles carry the most work: first
+  // Key tiles vary before sequences (low key tiles carry the most work: first),
+  // so the CTAs resident at one time work on one sequence.
+  const int ktile = blockIdx.y;
+  const int seq = blockIdx.z;
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
   const int j0 = ktile * kBlockN;
   if (j0 >= sp.nk) return;                 // uniform per CTA
@@ -388,7 +390,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   }
   const int qt_first = q_lo / kBlockM;
   const int nqt = (q_hi > q_lo) ? ((q_hi + kBlockM - 1) / kBlockM - qt_first) : 0;
-  const int num = nqt * hpc;               // steps: (query head) x (query tile)
+  const int num = nqt * hpc;               // steps: (query tile) x (query head), heads fastest
 
   if (num == 0) {
     // No query sees these keys: dK = dV = 0.
@@ -464,8 +466,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         }
         break;
       }
-      const int h = h_first + m / nqt;
-      const int i0 = (qt_first + m % nqt) * kBlockM;
+      const int h = h_first + m % hpc;
+      const int i0 = (qt_first + m / hpc) * kBlockM;
 #ifdef ATTN_SINK_TEST_HOOKS
       if (m == p.skip_q_step) {
         // test build: withhold this step's tiles; every wait for them runs out
@@ -651,7 +653,7 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const uint32_t tDPT = tmem + lane_base + kColDPT + 64 * hh;
     for (int m = 0; ok && m < num; ++m) {
       const int st = m % kBwdStages;
-      const int i0 = (qt_first + m % nqt) * kBlockM + 64 * hh;   // first query of this half
+      const int i0 = (qt_first + m / hpc) * kBlockM + 64 * hh;   // first query of this half
       // q_full: the producer's lse / D rows of this step are in SMEM.
       // s_full: S^T of this step (and every earlier MMA of issuer A) has completed.
       if (!mbar_wait_warp(&q_full[st], (m / kBwdStages) & 1, &abort_flag) ||
@@ -747,8 +749,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     // The dQ TMEM columns are free for step 0.
     if (!p.skip_dq && num > 0) mbar_arrive(&dq_free);
     for (int m = 0; m < (p.skip_dq ? 0 : num); ++m) {
-      const int h = h_first + m / nqt;
-      const int i0 = (qt_first + m % nqt) * kBlockM;
+      const int h = h_first + m % hpc;
+      const int i0 = (qt_first + m / hpc) * kBlockM;
       const bool waited = mbar_wait_warp(&mma2_done, m & 1, &abort_flag);
       // all four warps agree on the wait's outcome (and leave together)
       if (!named_barrier_and(1, 128, waited)) { ok = false; break; }
