@@ -414,7 +414,7 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   fp.skip_k_tile = g_test_skip_k_tile.load();
 #endif
   if (fp.n_qtiles == 0) return ATTN_SINK_OK;
-  dim3 grid(params->heads_q, g.num_seqs, fp.n_qtiles);
+  dim3 grid(params->heads_q, fp.n_qtiles, g.num_seqs);
   const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_FWD, static_cast<cudaStream_t>(stream));
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
   const bool ok = launched();

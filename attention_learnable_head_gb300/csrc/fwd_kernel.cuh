@@ -157,9 +157,12 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
   __shared__ float s_mx[2][2][kBlockM];   // [tile parity][half][row]: the halves' row maxima
   __shared__ float s_red_l[2][kBlockM];   // [half][row], epilogue only
 
+  // Heads vary fastest (the query heads of a GQA group share K/V tiles in L2),
+  // then query tiles, longest work first, then sequences, so the CTAs resident
+  // at one time read one sequence's keys.
   const int h = blockIdx.x;
-  const int seq = blockIdx.y;
-  const int qtile = p.n_qtiles - 1 - (int)blockIdx.z;    // longest work first
+  const int qtile = p.n_qtiles - 1 - (int)blockIdx.y;
+  const int seq = blockIdx.z;
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
   const int i0 = qtile * kBlockM;
   if (i0 >= sp.nq) return;                                // uniform per CTA
