@@ -217,7 +217,7 @@ int validate(const attn_sink_params* p, const int* cu_q, const int* cu_k, Geomet
     g->max_q = p->seqlen_q;
     g->max_k = p->seqlen_k;
   }
-  // Launch-grid limits (sequences in grid.y, tiles in grid.z).
+  // Launch-grid limits (tiles in grid.y, sequences in grid.z).
   if (g->num_seqs > 65535) return ATTN_SINK_ERR_UNSUPPORTED;
   if ((g->max_q + kBlockM - 1) / kBlockM > 65535 || (g->max_k + kBlockN - 1) / kBlockN > 65535)
     return ATTN_SINK_ERR_UNSUPPORTED;

@@ -57,12 +57,15 @@ struct DecodeParams {
 
 // G = query heads per kv head (1, 2, 4 or 8).
 template <int G>
-__global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const DecodeParams p) {
   __shared__ __align__(128) uint8_t s_kv[kDecStages][2][kDecKeys * 128];   // K, V blocks
   __shared__ uint8_t s_valid[kDecStages][kDecKeys];    // key inside the slice, page in range
   __shared__ float s_m[kDecWarps][kDecMaxGroup];
   __shared__ float s_l[kDecWarps][kDecMaxGroup];
-  __shared__ float s_o[kDecWarps][kDecMaxGroup][64];
+  // the warps' O rows for the final merge reuse the K/V stages (free by then)
+  float (*s_o)[kDecMaxGroup][64] = reinterpret_cast<float (*)[kDecMaxGroup][64]>(&s_kv[0][0][0]);
+  static_assert(sizeof(float) * kDecWarps * kDecMaxGroup * 64 <= sizeof(s_kv),
+                "merge buffer larger than the K/V stages");
 
   const int split = blockIdx.x;
   const int g = blockIdx.y;
@@ -101,34 +104,41 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
     }
   }
 
-  // Block `blk` of the slice into stage `st`: 64 keys x (K, V) x 8 chunks of 16
-  // bytes, 8 per thread.  A key past the slice, or whose table entry is out of
-  // range (reported, nothing read), is zero-filled and marked invalid.
-  auto load_block = [&](int blk, int st) {
-    const int base = k0 + blk * kDecKeys;
+  // Each thread copies 8 of a block's 16-byte chunks: K and V of the keys
+  // kq(u) = (tid / 8 + 16 u) % 64, u = 0..3, chunk tid % 8.  The block-table
+  // entries of its keys are read one block ahead (pages of block blk + 2 while
+  // block blk + 1 is copied), so the copies never wait on a table lookup.
+  auto fetch_pages = [&](int blk, int* pg) {
     #pragma unroll
-    for (int i = 0; i < (2 * kDecKeys * 8) / kDecThreads; ++i) {
-      const int q = tid + kDecThreads * i;
-      const int kv = q / (kDecKeys * 8);
-      const int key = (q >> 3) & (kDecKeys - 1);
-      const int c = q & 7;
+    for (int u = 0; u < 4; ++u) {
+      const int j = k0 + blk * kDecKeys + (((tid >> 3) + 16 * u) & (kDecKeys - 1));
+      pg[u] = (blk < nblk && j < k1)
+                  ? __ldg(p.block_table + (size_t)b * p.max_pages + j / p.page_size)
+                  : -1;
+    }
+  };
+  // Block `blk` of the slice into stage `st`, with the table entries pg of its
+  // keys.  A key past the slice, or whose table entry is out of range
+  // (reported, nothing read), is zero-filled and marked invalid.
+  auto load_block = [&](int blk, int st, const int* pg) {
+    const int base = k0 + blk * kDecKeys;
+    const int c = tid & 7;
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int key = ((tid >> 3) + 16 * u) & (kDecKeys - 1);
       const int j = base + key;
-      const __nv_bfloat16* cache = kv ? p.v_cache : p.k_cache;
-      const __nv_bfloat16* src = p.q;        // read by no copy (0 bytes): any valid address
-      uint32_t bytes = 0;
-      bool valid = false;
-      if (j < k1) {
-        const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + j / p.page_size);
-        valid = pg >= 0 && pg < p.num_pages;
-        if (valid) {
-          src = cache + ((size_t)pg * p.page_size + j % p.page_size) * row_stride + g * 64 + 8 * c;
-          bytes = 16;
-        } else if (kv == 0 && c == 0) {
-          atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
-        }
-      }
-      if (kv == 0 && c == 0) s_valid[st][key] = valid ? 1 : 0;
-      cp_async_16_zfill(smem_u32(&s_kv[st][kv][0]) + sw128_offset(key, c), src, bytes);
+      const bool inside = j < k1;
+      const bool valid = inside && pg[u] >= 0 && pg[u] < p.num_pages;
+      if (inside && !valid && c == 0) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
+      if (c == 0) s_valid[st][key] = valid ? 1 : 0;
+      const size_t off = valid ? ((size_t)pg[u] * p.page_size + j % p.page_size) * row_stride +
+                                     g * 64 + 8 * c
+                               : 0;
+      // with 0 bytes nothing is read: q is any valid address
+      const __nv_bfloat16* ksrc = valid ? p.k_cache + off : p.q;
+      const __nv_bfloat16* vsrc = valid ? p.v_cache + off : p.q;
+      cp_async_16_zfill(smem_u32(&s_kv[st][0][0]) + sw128_offset(key, c), ksrc, valid ? 16 : 0);
+      cp_async_16_zfill(smem_u32(&s_kv[st][1][0]) + sw128_offset(key, c), vsrc, valid ? 16 : 0);
     }
     cp_async_commit();
   };
@@ -141,15 +151,24 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
     #pragma unroll
     for (int e = 0; e < 4; ++e) oacc[nd][e] = 0.0f;
   }
-  bool overflow = false;
+  uint32_t vmag = 0;    // largest fp16 magnitude pattern of the converted V halves
   const int mi = lane >> 3, ri = lane & 7;   // ldmatrix: matrix and row this lane addresses
   const int kb = 16 * warp;                  // this warp's keys within a block
 
-  if (nblk > 0) load_block(0, 0);
+  // two-stage ring: block blk + 1 is in flight while blk is used (five CTAs per
+  // SM keep ten blocks in flight; measured better than three stages at four
+  // CTAs per SM)
+  int pg[4], pg_next[4];
+  fetch_pages(0, pg);
+  if (nblk > 0) load_block(0, 0, pg);
+  fetch_pages(1, pg_next);
   for (int blk = 0; blk < nblk; ++blk) {
-    const int st = blk & 1;
+    const int st = blk % kDecStages;
     if (blk + 1 < nblk) {
-      load_block(blk + 1, st ^ 1);
+      #pragma unroll
+      for (int u = 0; u < 4; ++u) pg[u] = pg_next[u];
+      fetch_pages(blk + 2, pg_next);
+      load_block(blk + 1, (blk + 1) % kDecStages, pg);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
@@ -220,14 +239,17 @@ __global__ void __launch_bounds__(kDecThreads) attn_sink_decode_kernel(const Dec
       uint32_t v0, v1, v2, v3;
       ldmatrix_x4_trans(vt + sw128_offset(kb + (mi & 1) * 8 + ri, 2 * u + (mi >> 1)), v0, v1,
                         v2, v3);
-      mma_16816_f16(oacc[2 * u], pa0, 0u, pa2, 0u, bf16x2_to_f16x2(v0, &overflow),
-                    bf16x2_to_f16x2(v1, &overflow));
-      mma_16816_f16(oacc[2 * u + 1], pa0, 0u, pa2, 0u, bf16x2_to_f16x2(v2, &overflow),
-                    bf16x2_to_f16x2(v3, &overflow));
+      const uint32_t h0 = bf16x2_to_f16x2_fast(v0), h1 = bf16x2_to_f16x2_fast(v1);
+      const uint32_t h2 = bf16x2_to_f16x2_fast(v2), h3 = bf16x2_to_f16x2_fast(v3);
+      vmag = __vmaxu2(vmag, __vmaxu2(h0 & 0x7fff7fffu, h1 & 0x7fff7fffu));
+      vmag = __vmaxu2(vmag, __vmaxu2(h2 & 0x7fff7fffu, h3 & 0x7fff7fffu));
+      mma_16816_f16(oacc[2 * u], pa0, 0u, pa2, 0u, h0, h1);
+      mma_16816_f16(oacc[2 * u + 1], pa0, 0u, pa2, 0u, h2, h3);
     }
     __syncthreads();   // every warp is done with stage st before it is refilled
   }
-  if (overflow) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
+  // a value that rounded to fp16 infinity (or a NaN) lies outside the fp16 range
+  if ((vmag & 0xffffu) >= 0x7c00u || (vmag >> 16) >= 0x7c00u) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
 
   // the row sum over the 4 lanes of row gr, then the 4 warps' states merged
   l_r += __shfl_xor_sync(0xffffffffu, l_r, 1);

@@ -544,6 +544,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool* overflow) 
   return pack_f16x2(a, b);
 }
 
+// bf16x2 -> f16x2 (round to nearest even) without a range check: a value
+// outside the fp16 range becomes +-inf, which the caller can test on the result.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_fast(uint32_t w) {
+  return pack_f16x2(bf16_lo(w), bf16_hi(w));
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled
 // tile whose rows are 128 bytes apart.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
