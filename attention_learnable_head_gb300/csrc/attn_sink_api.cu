@@ -224,15 +224,16 @@ int validate(const attn_sink_params* p, const int* cu_q, const int* cu_k, Geomet
   return ATTN_SINK_OK;
 }
 
-// 3-D map over a [tokens][heads][64] tensor with a (128 bytes) x 1 x 128-row box
+// 3-D map over a [tokens][heads][64] tensor with a (128 bytes) x 1 x box_rows box
 // and 128-byte swizzle: 64 columns of a 16-bit type, or 32 of fp32.
-int encode_rows(CUtensorMap* m, const void* ptr, int tokens, int heads,
-                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+int encode_rows(CUtensorMap* m, const void* ptr, long long tokens, int heads,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                int box_rows = kBlockM) {
   if (!load_encode()) return ATTN_SINK_ERR_CUDA;
   const cuuint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * esize, (cuuint64_t)heads * kHeadDim * esize};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)kBlockM};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, dtype, 3, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -591,12 +592,30 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
   dp.window = params->window > 0 ? params->window : 0;
   dp.splits = L.splits;
   dp.scale_log2 = params->softmax_scale * kLog2e;
+  // Whole pages by TMA for power-of-two page sizes of 8 keys or more (and a
+  // pool whose rows fit the copy coordinates); per-thread copies otherwise.
+  const long long rows = (long long)params->num_pages * params->page_size;
+  const bool tma = decode_tma_page(params->page_size) && rows > 0 && rows < (1ll << 31);
+  dp.log2_page = 0;
+  while ((1 << dp.log2_page) < params->page_size) ++dp.log2_page;
+  if (tma) {
+    const int box = std::min(params->page_size, kDecKeys);
+    if ((st = encode_rows(&dp.tm_k, k_cache, rows, params->heads_kv,
+                          CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, box)) != ATTN_SINK_OK ||
+        (st = encode_rows(&dp.tm_v, v_cache, rows, params->heads_kv,
+                          CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, box)) != ATTN_SINK_OK)
+      return st;
+  }
   const dim3 grid(L.splits, params->heads_kv, params->batch);
-  switch (params->heads_q / params->heads_kv) {
-    case 1: attn_sink_decode_kernel<1><<<grid, kDecThreads, 0, s>>>(dp); break;
-    case 2: attn_sink_decode_kernel<2><<<grid, kDecThreads, 0, s>>>(dp); break;
-    case 4: attn_sink_decode_kernel<4><<<grid, kDecThreads, 0, s>>>(dp); break;
-    default: attn_sink_decode_kernel<8><<<grid, kDecThreads, 0, s>>>(dp); break;
+  switch ((params->heads_q / params->heads_kv) * 2 + (tma ? 1 : 0)) {
+    case 2: attn_sink_decode_kernel<1, false><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 3: attn_sink_decode_kernel<1, true><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 4: attn_sink_decode_kernel<2, false><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 5: attn_sink_decode_kernel<2, true><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 8: attn_sink_decode_kernel<4, false><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 9: attn_sink_decode_kernel<4, true><<<grid, kDecThreads, 0, s>>>(dp); break;
+    case 16: attn_sink_decode_kernel<8, false><<<grid, kDecThreads, 0, s>>>(dp); break;
+    default: attn_sink_decode_kernel<8, true><<<grid, kDecThreads, 0, s>>>(dp); break;
   }
   if (!launched()) return ATTN_SINK_ERR_CUDA;
   return attn_sink_merge(L.splits, params->batch, params->heads_q, kHeadDim, dp.o_part,

@@ -39,6 +39,8 @@ constexpr int kDecStages = 2;
 constexpr float kLn2Dec = 0.6931471805599453f;
 
 struct DecodeParams {
+  CUtensorMap tm_k;               // k_cache as [num_pages * page_size][H_kv][64], box
+  CUtensorMap tm_v;               //   64 x 1 x min(page_size, 64), 128B swizzle (TMA path)
   const __nv_bfloat16* q;         // [B][H_q][64]
   const __nv_bfloat16* k_cache;   // [num_pages][page_size][H_kv][64]
   const __nv_bfloat16* v_cache;
@@ -52,14 +54,26 @@ struct DecodeParams {
   int page_size, num_pages, max_pages;
   int window;
   int splits;
+  int log2_page;                  // TMA path: log2(page_size)
   float scale_log2;               // softmax_scale * log2(e)
 };
 
-// G = query heads per kv head (1, 2, 4 or 8).
-template <int G>
-__global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const DecodeParams p) {
-  __shared__ __align__(128) uint8_t s_kv[kDecStages][2][kDecKeys * 128];   // K, V blocks
+// Page sizes the TMA path copies whole: a multiple of 8 keys (whole 128-byte
+// swizzle atoms) that divides the 64-key block or is a multiple of it.
+__host__ __device__ constexpr bool decode_tma_page(int page_size) {
+  return page_size >= 8 && (page_size & (page_size - 1)) == 0;
+}
+
+// G = query heads per kv head (1, 2, 4 or 8).  kTma: the blocks' pages are
+// copied by TMA (one thread issues them; page sizes of decode_tma_page),
+// otherwise by every thread with 16-byte cp.async.
+template <int G, bool kTma>
+__global__ void __launch_bounds__(kDecThreads, 5)
+attn_sink_decode_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ __align__(1024) uint8_t s_kv[kDecStages][2][kDecKeys * 128];   // K, V blocks
   __shared__ uint8_t s_valid[kDecStages][kDecKeys];    // key inside the slice, page in range
+  __shared__ uint8_t s_pageok[kDecStages][8];          // TMA path: copy i of the block is a page
+  __shared__ __align__(8) uint64_t kv_full[kDecStages];   // TMA path: the stage's copies landed
   __shared__ float s_m[kDecWarps][kDecMaxGroup];
   __shared__ float s_l[kDecWarps][kDecMaxGroup];
   // the warps' O rows for the final merge reuse the K/V stages (free by then)
@@ -82,9 +96,12 @@ __global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const 
     if (tid == 0) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
     L = max(0, min(L, cap));
   }
+  // The slices start on 64-key block boundaries (so the TMA path copies whole
+  // pages into a block); keys before the window start are masked.
   const int lo = p.window > 0 ? max(0, L - p.window) : 0;
-  const int per = (L - lo + p.splits - 1) / p.splits;
-  const int k0 = lo + split * per;
+  const int lo_blk = lo & ~(kDecKeys - 1);
+  const int per = ((L - lo_blk + p.splits - 1) / p.splits + kDecKeys - 1) & ~(kDecKeys - 1);
+  const int k0 = lo_blk + split * per;
   const int k1 = min(L, k0 + per);
   const int nblk = k1 > k0 ? (k1 - k0 + kDecKeys - 1) / kDecKeys : 0;
   const size_t row_stride = (size_t)p.heads_kv * 64;     // one key of the cache
@@ -127,7 +144,7 @@ __global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const 
     for (int u = 0; u < 4; ++u) {
       const int key = ((tid >> 3) + 16 * u) & (kDecKeys - 1);
       const int j = base + key;
-      const bool inside = j < k1;
+      const bool inside = j >= lo && j < k1;
       const bool valid = inside && pg[u] >= 0 && pg[u] < p.num_pages;
       if (inside && !valid && c == 0) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
       if (c == 0) s_valid[st][key] = valid ? 1 : 0;
@@ -155,25 +172,94 @@ __global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const 
   const int mi = lane >> 3, ri = lane & 7;   // ldmatrix: matrix and row this lane addresses
   const int kb = 16 * warp;                  // this warp's keys within a block
 
+  // TMA path: thread 0 copies the pages of a block (boxes of min(page, 64)
+  // keys; a page outside the cache is read at a coordinate beyond the tensor,
+  // which fills zeros, and marked as such) and reads the block's table entries
+  // one block ahead.  The consumers mask keys outside [lo, k1) and keys of a
+  // page marked absent.
+  const int log2_box = kTma ? min(p.log2_page, 6) : 0;
+  const int box = 1 << log2_box;
+  const int npg = kTma ? kDecKeys >> log2_box : 0;      // copies per block and tensor
+  auto tma_fetch = [&](int blk, int* pe) {
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = k0 + blk * kDecKeys + i * box;       // first key of copy i
+      pe[i] = (i < npg && blk < nblk && j < k1)
+                  ? __ldg(p.block_table + (size_t)b * p.max_pages + (j >> p.log2_page))
+                  : -1;
+    }
+  };
+  auto tma_issue = [&](int blk, int st, const int* pe) {
+    const int base = k0 + blk * kDecKeys;
+    const int oob = p.num_pages * p.page_size;           // first row past the cache
+    int row[8];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = base + i * box;
+      const bool needed = i < npg && j < k1 && j + box > lo;
+      const bool ok = pe[i] >= 0 && pe[i] < p.num_pages;
+      if (needed && !ok) atomicCAS(p.err, 0, DEVERR_DECODE_INPUT);
+      row[i] = ok ? pe[i] * p.page_size + (j & (p.page_size - 1)) : oob;
+      if (i < npg) s_pageok[st][i] = ok ? 1 : 0;
+    }
+    mbar_arrive_expect_tx(&kv_full[st], 2 * kDecKeys * 128);
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < npg) {
+        tma_load_3d(&p.tm_k, &kv_full[st], &s_kv[st][0][i * box * 128], 0, g, row[i]);
+        tma_load_3d(&p.tm_v, &kv_full[st], &s_kv[st][1][i * box * 128], 0, g, row[i]);
+      }
+    }
+  };
+  int issued = 0;                                         // TMA path: blocks issued
+  if (kTma) {
+    if (tid == 0) {
+      for (int st = 0; st < kDecStages; ++st) mbar_init(&kv_full[st], 1);
+      fence_mbarrier_init();
+    }
+    __syncthreads();
+  }
+
   // two-stage ring: block blk + 1 is in flight while blk is used (five CTAs per
   // SM keep ten blocks in flight; measured better than three stages at four
   // CTAs per SM)
-  int pg[4], pg_next[4];
-  fetch_pages(0, pg);
-  if (nblk > 0) load_block(0, 0, pg);
-  fetch_pages(1, pg_next);
+  int pg[8], pg_next[8];
+  bool ok = true;
+  if (kTma) {
+    if (tid == 0) {
+      tma_fetch(0, pg);
+      if (nblk > 0) tma_issue(0, 0, pg);
+      tma_fetch(1, pg);
+      if (nblk > 1) tma_issue(1, 1, pg);
+      issued = min(nblk, 2);
+      tma_fetch(2, pg_next);
+    }
+  } else {
+    fetch_pages(0, pg);
+    if (nblk > 0) load_block(0, 0, pg);
+    fetch_pages(1, pg_next);
+  }
   for (int blk = 0; blk < nblk; ++blk) {
     const int st = blk % kDecStages;
-    if (blk + 1 < nblk) {
-      #pragma unroll
-      for (int u = 0; u < 4; ++u) pg[u] = pg_next[u];
-      fetch_pages(blk + 2, pg_next);
-      load_block(blk + 1, (blk + 1) % kDecStages, pg);
-      cp_async_wait<1>();
+    if (kTma) {
+      // bounded wait; the whole CTA agrees on the outcome
+      const bool landed = mbar_wait_warp(&kv_full[st], (blk / kDecStages) & 1, nullptr);
+      if (!__syncthreads_and(landed)) {
+        ok = false;
+        break;
+      }
     } else {
-      cp_async_wait<0>();
+      if (blk + 1 < nblk) {
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) pg[u] = pg_next[u];
+        fetch_pages(blk + 2, pg_next);
+        load_block(blk + 1, (blk + 1) % kDecStages, pg);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
     }
-    __syncthreads();
     const uint32_t kt = smem_u32(&s_kv[st][0][0]);
     const uint32_t vt = smem_u32(&s_kv[st][1][0]);
 
@@ -201,7 +287,14 @@ __global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const 
     for (int nt = 0; nt < 2; ++nt) {
       #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const bool valid = s_valid[st][kb + 8 * nt + 2 * t4 + e] != 0;
+        const int key = kb + 8 * nt + 2 * t4 + e;
+        bool valid;
+        if (kTma) {
+          const int j = k0 + blk * kDecKeys + key;
+          valid = s_pageok[st][key >> log2_box] != 0 && j >= lo && j < k1;
+        } else {
+          valid = s_valid[st][key] != 0;
+        }
         x[nt][e] = valid ? sc[nt][e] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, x[nt][e]);
       }
@@ -247,6 +340,24 @@ __global__ void __launch_bounds__(kDecThreads, 5) attn_sink_decode_kernel(const 
       mma_16816_f16(oacc[2 * u + 1], pa0, 0u, pa2, 0u, h2, h3);
     }
     __syncthreads();   // every warp is done with stage st before it is refilled
+    if (kTma && tid == 0 && blk + 2 < nblk) {
+      #pragma unroll
+      for (int i = 0; i < 8; ++i) pg[i] = pg_next[i];
+      tma_fetch(blk + 3, pg_next);
+      tma_issue(blk + 2, st, pg);
+      issued = blk + 3;
+    }
+  }
+  if (!ok) {
+    // a copy that did not land within the wait limit (the whole CTA agreed):
+    // report it, give the copies still in flight (the last two issued) time to
+    // land before the CTA releases its shared memory, and write nothing
+    if (tid == 0) {
+      atomicCAS(p.err, 0, DEVERR_TIMEOUT_FWD + 5);
+      for (int j = max(0, issued - kDecStages); j < issued; ++j)
+        mbar_wait(&kv_full[j % kDecStages], (j / kDecStages) & 1, nullptr);
+    }
+    return;
   }
   // a value that rounded to fp16 infinity (or a NaN) lies outside the fp16 range
   if ((vmag & 0xffffu) >= 0x7c00u || (vmag >> 16) >= 0x7c00u) atomicCAS(p.err, 0, DEVERR_FP16_RANGE);
