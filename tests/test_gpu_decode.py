@@ -61,6 +61,10 @@ CASES = [
     ("long_g8", [5000, 333], 128, 64, 8, 0),
     ("page1_g1", [50, 7], 1, 4, 4, 0),
     ("g4_window_short", [3, 40, 200], 32, 8, 2, 16),
+    # page 8: the smallest page copied whole by TMA; page 48: not a power of
+    # two, copied by the per-thread path
+    ("page8_window", [9, 77, 513], 8, 16, 2, 70),
+    ("page48_g2", [47, 48, 49, 700], 48, 4, 2, 0),
 ]
 
 
