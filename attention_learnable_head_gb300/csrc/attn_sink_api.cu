@@ -15,6 +15,7 @@
 #include "bwd_dq_kernel.cuh"
 #include "bwd_kernel.cuh"
 #include "decode_kernel.cuh"
+#include "fwd_band_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "merge_kernel.cuh"
 
@@ -145,6 +146,9 @@ int device_state(int* sm_count, int** err) {
   if (!g_attr_set[dev]) {
     if (cudaFuncSetAttribute(attn_sink_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kFwdSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_sink_fwd_band_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBandSmemMax) != cudaSuccess ||
         cudaFuncSetAttribute(attn_sink_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kDqSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(attn_sink_bwd_main_kernel,
@@ -224,16 +228,16 @@ int validate(const attn_sink_params* p, const int* cu_q, const int* cu_k, Geomet
   return ATTN_SINK_OK;
 }
 
-// 3-D map over a [tokens][heads][64] tensor with a (128 bytes) x 1 x box_rows box
-// and 128-byte swizzle: 64 columns of a 16-bit type, or 32 of fp32.
+// 3-D map over a [tokens][heads][64] tensor with a (128 bytes) x box_heads x
+// box_rows box and 128-byte swizzle: 64 columns of a 16-bit type, or 32 of fp32.
 int encode_rows(CUtensorMap* m, const void* ptr, long long tokens, int heads,
                 CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                int box_rows = kBlockM) {
+                int box_rows = kBlockM, int box_heads = 1) {
   if (!load_encode()) return ATTN_SINK_ERR_CUDA;
   const cuuint64_t esize = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * esize, (cuuint64_t)heads * kHeadDim * esize};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)box_rows};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, dtype, 3, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -346,6 +350,77 @@ const char* attn_sink_status_string(int status) {
 
 namespace {
 
+// The band kernel's launch (fwd_band_kernel.cuh): items of 128 / G tokens x the
+// G query heads of a kv group, a window of n_cols keys each; persistent grid of
+// two CTAs per SM.  v16 is the fp16 copy of v already written by the caller.
+int fwd_band(const attn_sink_params* params, const Geometry& g, const void* q, const void* k,
+             const void* v16, const void* sink, const int* cu_seqlens_q,
+             const int* cu_seqlens_k, void* out, void* out_residual, float* lse, void* stream,
+             bool chunk, int q_pos0, bool sink_bf16, int tokens, int n_cols, int sms, int* err) {
+  FwdBandParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  int st;
+  if ((st = encode_rows(&bp.tm_q, q, g.total_q, params->heads_q,
+                        CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tokens, g.group)) != ATTN_SINK_OK)
+    return st;
+  if ((st = encode_rows(&bp.tm_k, k, g.total_k, params->heads_kv,
+                        CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, n_cols)) != ATTN_SINK_OK)
+    return st;
+  if ((st = encode_rows(&bp.tm_v, v16, g.total_k, params->heads_kv,
+                        CU_TENSOR_MAP_DATA_TYPE_FLOAT16, n_cols)) != ATTN_SINK_OK)
+    return st;
+  if ((st = encode_rows(&bp.tm_out, out, g.total_q, params->heads_q,
+                        CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tokens, g.group)) != ATTN_SINK_OK)
+    return st;
+  if ((st = encode_rows(&bp.tm_out_lo, out_residual ? out_residual : out, g.total_q,
+                        params->heads_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tokens, g.group)) !=
+      ATTN_SINK_OK)
+    return st;
+  const long long n_tb = (g.max_q + tokens - 1) / tokens;
+  const long long n_items = (long long)g.num_seqs * n_tb * params->heads_kv;
+  if (n_items >= (1ll << 30)) return ATTN_SINK_ERR_UNSUPPORTED;
+  if (n_items == 0) return ATTN_SINK_OK;
+  bp.cu_q = cu_seqlens_q;
+  bp.cu_k = cu_seqlens_k;
+  bp.sink = sink_bf16 ? nullptr : static_cast<const float*>(sink);
+  bp.sink_bf16 = sink_bf16 ? static_cast<const __nv_bfloat16*>(sink) : nullptr;
+  bp.out = static_cast<__nv_bfloat16*>(out);
+  bp.out_lo = static_cast<__nv_bfloat16*>(out_residual);
+  bp.lse = lse;
+  bp.err = err;
+  bp.seqlen_q = g.varlen ? 0 : params->seqlen_q;
+  bp.seqlen_k = g.varlen ? 0 : params->seqlen_k;
+  bp.total_q = g.total_q;
+  bp.heads_q = params->heads_q;
+  bp.heads_kv = params->heads_kv;
+  bp.group = g.group;
+  bp.log2_group = 0;
+  while ((1 << bp.log2_group) < g.group) ++bp.log2_group;
+  bp.tokens = tokens;
+  bp.n_cols = n_cols;
+  bp.half0_cols = 16 * ((n_cols / 16 + 1) / 2);
+  bp.window = params->window;
+  bp.scale_log2 = params->softmax_scale * kLog2e;
+  bp.chunk = chunk ? 1 : 0;
+  bp.q_pos0 = chunk ? q_pos0 : 0;
+  bp.n_tb = (int)n_tb;
+  bp.n_items = (int)n_items;
+  fast_div_init(params->heads_kv, &bp.div_hkv_mul, &bp.div_hkv_shift);
+  fast_div_init(bp.n_tb, &bp.div_tb_mul, &bp.div_tb_shift);
+#ifdef ATTN_SINK_TEST_HOOKS
+  bp.skip_k_tile = g_test_skip_k_tile.load();
+#endif
+  // At least 80 KB, so that no SM holds a third CTA (two fill its 512 TMEM
+  // columns; a third would wait in its allocation until one of them ends).
+  const int smem = std::max(80 * 1024, band_smem_bytes(n_cols));
+  const int grid = (int)std::min<long long>(n_items, (long long)kBandCtasPerSm * sms);
+  const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_FWD, static_cast<cudaStream_t>(stream));
+  attn_sink_fwd_band_kernel<<<grid, kBandThreads, smem, static_cast<cudaStream_t>(stream)>>>(bp);
+  const bool ok = launched();
+  timing_end(t, static_cast<cudaStream_t>(stream), ok);
+  return ok ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+}
+
 // The forward, with or without the sink; `chunk` selects key-chunk mode (no
 // sink, query row i at key position i + q_pos0 in every sequence).
 int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const void* v,
@@ -392,6 +467,16 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
         static_cast<const __nv_bfloat16*>(v), static_cast<uint16_t*>(workspace), n8, err);
     if (!launched()) return ATTN_SINK_ERR_CUDA;
   }
+  // Sliding-window layers whose item window (128 / G tokens + W - 1 keys) fits
+  // one product go to the band kernel.
+  const int band_tokens = (kBlockM % g.group == 0) ? kBlockM / g.group : 0;
+  const long long band_cols =
+      band_tokens > 0 ? ((long long)band_tokens + params->window - 1 + 15) / 16 * 16 : 0;
+  if (params->causal && params->window > 0 && g.total_k > 0 && band_tokens > 0 &&
+      band_cols <= kBandMaxCols)
+    return fwd_band(params, g, q, k, workspace, sink, cu_seqlens_q, cu_seqlens_k, out,
+                    out_residual, lse, stream, chunk, q_pos0, sink_bf16, band_tokens,
+                    (int)band_cols, sms, err);
   fp.cu_q = cu_seqlens_q;
   fp.cu_k = cu_seqlens_k;
   fp.sink = sink_bf16 ? nullptr : static_cast<const float*>(sink);

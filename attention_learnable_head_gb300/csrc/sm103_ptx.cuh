@@ -175,6 +175,26 @@ __device__ __forceinline__ void tma_load_3d_hint(const CUtensorMap* m, uint64_t*
       : "memory");
 }
 
+// Bring a box of a tensor into L2 ahead of its load (no SMEM, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Store a SMEM tile to global memory through a tensor map (bulk-group
+// completion: bulk_commit_group / bulk_wait_group*).  The tile's SMEM writes
+// must be fenced for the async proxy (fence_proxy_async_smem) first.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* m, const void* src, int c0,
+                                                  int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 // Element-wise atomic add of a SMEM tile into global memory through a tensor
 // map (fp32 add; rows/cols outside the tensor are skipped by the hardware).
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int c0,
@@ -394,6 +414,13 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t* r) {

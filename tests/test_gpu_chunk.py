@@ -61,6 +61,8 @@ CASES = [
     ("window_100", 1, 385, 385, 2, 2, True, 100, [(0, 128), (128, 200), (200, 385)]),
     ("noncausal", 2, 129, 190, 2, 1, False, 0, [(0, 64), (64, 190)]),
     ("invisible_chunk", 1, 64, 400, 2, 1, True, 16, [(0, 256), (256, 400)]),
+    # G = 8 with a window: the chunks take the sliding-window kernel
+    ("window_g8", 2, 500, 500, 16, 2, True, 128, [(0, 200), (200, 263), (263, 500)]),
 ]
 
 

@@ -16,8 +16,8 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def _case():
-    w = small_workload("flags", 701, 8, 2, [300, 129], causal=True)
+def _case(window=0):
+    w = small_workload("flags", 701, 8, 2, [300, 129], causal=True, window=window)
     c = make_case(w)
     cu = torch.tensor(c.cu_seqlens, dtype=torch.int32, device=DEV)
     kw = dict(causal=w.causal, window=w.window, softmax_scale=w.scale, cu_seqlens_q=cu,
@@ -26,8 +26,10 @@ def _case():
     return c, w, kw, t
 
 
-def test_bf16_sink_equals_its_fp32_value():
-    c, w, kw, (q, k, v, do) = _case()
+@pytest.mark.parametrize("window", [0, 128])
+def test_bf16_sink_equals_its_fp32_value(window):
+    """Full causal (the tile kernel) and W = 128 (the sliding-window kernel)."""
+    c, w, kw, (q, k, v, do) = _case(window)
     sink16 = c.sink.to(torch.bfloat16).to(DEV)
     sink32 = sink16.float()
     o16, l16, r16 = binding.forward(q, k, v, sink16, **kw)

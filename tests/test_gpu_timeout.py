@@ -117,3 +117,37 @@ def test_wait_that_runs_out_returns_a_timeout_and_leaves_the_context_usable():
     oref = oracle_bwd(c.q, c.k, c.v, c.sink, c.dout, scale=w.scale, causal=True, window=0,
                       cu_seqlens_q=c.cu_seqlens, cu_seqlens_k=c.cu_seqlens)
     check_against(run_gpu(c), oref)
+
+
+def test_sliding_window_kernel_wait_runs_out():
+    """The sliding-window forward (G = 2, W = 64: items of 64 tokens x 2 heads,
+    one per CTA here): K of each CTA's first item is withheld, so every CTA's
+    products wait for it; the call gives up with a 0x1xx timeout and the next
+    call is clean and matches the oracle."""
+    Lt = binding.load_library(build(test=True))
+    dev = torch.device("cuda:0")
+    w = small_workload("timeout_band", 954, 4, 2, [512, 300], causal=True, window=64)
+    c = make_case(w)
+    t = {n: getattr(c, n).to(dev) for n in ("q", "k", "v", "dout", "sink")}
+    cu = torch.tensor(c.cu_seqlens, dtype=torch.int32, device=dev)
+    p = binding.make_params(c.q.shape, c.k.shape, causal=True, window=64, softmax_scale=w.scale,
+                            num_seqs=len(c.lengths), max_seqlen_q=max(c.lengths),
+                            max_seqlen_k=max(c.lengths))
+    stream = torch.cuda.current_stream().cuda_stream
+    out, res = torch.empty_like(t["q"]), torch.empty_like(t["q"])
+    lse = torch.empty((t["q"].shape[1], t["q"].shape[0]), dtype=torch.float32, device=dev)
+    fws = torch.empty(max(Lt.attn_sink_fwd_workspace_size(ctypes.byref(p)), 1),
+                      dtype=torch.uint8, device=dev)
+    assert Lt.attn_sink_test_withhold(0, -1) == 0
+    t0 = time.perf_counter()
+    assert _fwd(Lt, p, t, cu, out, res, lse, fws, stream) == 0
+    st, code = _device_error(Lt, stream)
+    elapsed = time.perf_counter() - t0
+    assert st == TIMEOUT and code & 0xF00 == 0x100, (st, hex(code))
+    assert elapsed < 1.0, f"the forward took {elapsed:.3f} s to give up"
+    assert Lt.attn_sink_test_withhold(-1, -1) == 0
+    assert _fwd(Lt, p, t, cu, out, res, lse, fws, stream) == 0
+    assert _device_error(Lt, stream) == (0, 0)
+    ref = oracle_bwd(c.q, c.k, c.v, c.sink, c.dout, scale=w.scale, causal=True, window=64,
+                     cu_seqlens_q=c.cu_seqlens, cu_seqlens_k=c.cu_seqlens)
+    check_against({"out": out.cpu(), "out_res": res.cpu(), "lse": lse.cpu()}, ref)
