@@ -193,25 +193,38 @@ __device__ __forceinline__ void band_ld(uint32_t taddr, uint32_t* a) {
   else tmem_ld_x16(taddr, a);
 }
 
-// Columns of a chunk outside [lo, hi] (the row's visible keys, counted from
-// the chunk's first column) become -inf; skipped when no row of the warp has
-// a masked column in this chunk.
 template <int NC>
-__device__ __forceinline__ void band_mask(uint32_t* a, int lo, int hi) {
-  if (__any_sync(0xffffffffu, lo > 0 || hi < NC - 1)) {
-    #pragma unroll
-    for (int e = 0; e < NC; ++e)
-      if (e < lo || e > hi) a[e] = __float_as_uint(-INFINITY);
-  }
+__device__ __forceinline__ void band_st(uint32_t taddr, const uint32_t* a) {
+  if constexpr (NC == 32) tmem_st_x32(taddr, a);
+  else tmem_st_x16(taddr, a);
 }
 
-// Row max of one chunk of S (raw scores), masked.
+// Row max of one chunk of S (raw scores) over the row's visible keys [lo, hi]
+// (counted from the chunk's first column).  Columns outside become -inf, each
+// bound checked only when some row of the warp crosses it in this chunk, and
+// a chunk that had any is written back to TMEM so that the exponentials need
+// no mask.  Returns whether it wrote one back (warp-uniform).
 template <int NC>
-__device__ __forceinline__ float band_chunk_max(uint32_t taddr, int lo, int hi) {
+__device__ __forceinline__ float band_chunk_max(uint32_t taddr, int lo, int hi, bool& wrote) {
   uint32_t a[NC];
   band_ld<NC>(taddr, a);
   tmem_ld_wait();
-  band_mask<NC>(a, lo, hi);
+  const bool cut_lo = __any_sync(0xffffffffu, lo > 0);
+  const bool cut_hi = __any_sync(0xffffffffu, hi < NC - 1);
+  if (cut_lo) {
+    #pragma unroll
+    for (int e = 0; e < NC; ++e)
+      if (e < lo) a[e] = __float_as_uint(-INFINITY);
+  }
+  if (cut_hi) {
+    #pragma unroll
+    for (int e = 0; e < NC; ++e)
+      if (e > hi) a[e] = __float_as_uint(-INFINITY);
+  }
+  if (cut_lo || cut_hi) {
+    band_st<NC>(taddr, a);
+    wrote = true;
+  }
   float q0 = __uint_as_float(a[0]), q1 = __uint_as_float(a[1]);
   #pragma unroll
   for (int e = 2; e + 3 < NC; e += 4) {
@@ -222,15 +235,15 @@ __device__ __forceinline__ float band_chunk_max(uint32_t taddr, int lo, int hi) 
   return fmaxf(q0, q1);
 }
 
-// P = exp2(S * scale log2 e - m) of one chunk (masked columns give 0), summed
-// into rs and written as fp16 pairs to TMEM at tp (NC / 2 columns).
+// P = exp2(S * scale log2 e - m) of one chunk (masked columns hold -inf and
+// give 0), summed into rs and written as fp16 pairs to TMEM at tp (NC / 2
+// columns).
 template <int NC>
-__device__ __forceinline__ void band_chunk_exp(uint32_t ts, uint32_t tp, int lo, int hi,
-                                               uint64_t sl2x2, uint64_t negm2, uint64_t& rs) {
+__device__ __forceinline__ void band_chunk_exp(uint32_t ts, uint32_t tp, uint64_t sl2x2,
+                                               uint64_t negm2, uint64_t& rs) {
   uint32_t a[NC];
   band_ld<NC>(ts, a);
   tmem_ld_wait();
-  band_mask<NC>(a, lo, hi);
   uint32_t pk[NC / 2];
   #pragma unroll
   for (int e = 0; e < NC; e += 2) {
@@ -395,7 +408,9 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
       int li = 0;
       bool ok = true;
       BandWalk w;
-      for (w.start(p); w.more(p); w.advance(p)) {
+      w.start(p);
+      bool have = w.more(p);
+      while (have) {
         const int qs = li & 1;
         if (!mbar_wait(&q_full[qs], (li >> 1) & 1, &abort_flag) ||
             !mbar_wait(&k_full, li & 1, &abort_flag)) {
@@ -409,15 +424,23 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
         mma_commit(&s_full);
         mma_commit(&q_empty[qs]);
         mma_commit(&k_empty);
+        // whether another item follows, found while the softmax works on this one
+        w.advance(p);
+        have = w.more(p);
         if (!mbar_wait(&p_full, li & 1, &abort_flag) || !mbar_wait(&v_full, li & 1, &abort_flag) ||
             (li > 0 && !mbar_wait(&o_free, (li - 1) & 1, &abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int kk = 0; kk < nks; ++kk) {
-          const uint32_t pcol = 8u * kk + (kk < ks0 ? 0u : 8u * ks0);
-          mma_ts(tmem + kBandColO, tmem + pcol, dV + 128u * kk, idesc_o, kk > 0);
+        // P of half 0 in columns [0, N0/2), of half 1 from column N0 on
+        uint32_t a_col = tmem;
+        uint64_t b_desc = dV;
+        mma_ts(tmem + kBandColO, a_col, b_desc, idesc_o, 0);
+        for (int kk = 1; kk < nks; ++kk) {
+          a_col += (kk == ks0) ? 8u + 8u * ks0 : 8u;
+          b_desc += 128u;
+          mma_ts(tmem + kBandColO, a_col, b_desc, idesc_o, 1);
         }
         mma_commit(&pv_done);
         mma_commit(&v_empty);
@@ -484,10 +507,13 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
         float mx = -INFINITY;
         if (got) {
           tc_fence_after();
+          bool wrote = false;
           int cc = 0;
+          #pragma unroll 1
           for (; cc + 32 <= nc; cc += 32)
-            mx = fmaxf(mx, band_chunk_max<32>(tS + cc, lo - cc, hi - cc));
-          if (cc < nc) mx = fmaxf(mx, band_chunk_max<16>(tS + cc, lo - cc, hi - cc));
+            mx = fmaxf(mx, band_chunk_max<32>(tS + cc, lo - cc, hi - cc, wrote));
+          if (cc < nc) mx = fmaxf(mx, band_chunk_max<16>(tS + cc, lo - cc, hi - cc, wrote));
+          if (wrote) tmem_st_wait();   // the masked chunks are back before pass 2 reads them
           s_mx[c][r] = mx;
         }
         ok = named_barrier_and(2 + (warp & 3), 64, got);
@@ -500,10 +526,10 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
           // P of keys [cc, cc + 32) goes to columns [cc / 2, cc / 2 + 16) of the
           // half: S columns this thread has already read.
           int cc = 0;
+          #pragma unroll 1
           for (; cc + 32 <= nc; cc += 32)
-            band_chunk_exp<32>(tS + cc, tS + (cc >> 1), lo - cc, hi - cc, sl2x2, negm2, rs);
-          if (cc < nc)
-            band_chunk_exp<16>(tS + cc, tS + (cc >> 1), lo - cc, hi - cc, sl2x2, negm2, rs);
+            band_chunk_exp<32>(tS + cc, tS + (cc >> 1), sl2x2, negm2, rs);
+          if (cc < nc) band_chunk_exp<16>(tS + cc, tS + (cc >> 1), sl2x2, negm2, rs);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&p_full);
@@ -535,16 +561,17 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
         const bool whole = prem >= p.tokens;      // same for every row of the item
         const int h = pg * p.group + hh;
         const size_t row = (size_t)(ptok + t);
+        const uint64_t inv_l2 = f2(inv_l, inv_l);
         #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          float f[8];
           uint32_t hi2[4], lo2[4];
           #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * u + e]) * inv_l;
-          #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            hi2[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
-            lo2[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi2[e]), f[2 * e + 1] - bf16_hi(hi2[e]));
+            const uint64_t f = fmul2(f2(__uint_as_float(o[8 * u + 2 * e]),
+                                        __uint_as_float(o[8 * u + 2 * e + 1])), inv_l2);
+            hi2[e] = pack_bf16x2(f2_lo(f), f2_hi(f));
+            const uint64_t res = fsub2(f, f2(bf16_lo(hi2[e]), bf16_hi(hi2[e])));
+            lo2[e] = pack_bf16x2(f2_lo(res), f2_hi(res));
           }
           if (whole) {
             // row r of the item's [T][G][64] box, 128B-swizzled like the TMA tile
