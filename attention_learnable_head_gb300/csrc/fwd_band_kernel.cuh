@@ -209,19 +209,24 @@ __device__ __forceinline__ float band_chunk_max(uint32_t taddr, int lo, int hi, 
   uint32_t a[NC];
   band_ld<NC>(taddr, a);
   tmem_ld_wait();
-  const bool cut_lo = __any_sync(0xffffffffu, lo > 0);
-  const bool cut_hi = __any_sync(0xffffffffu, hi < NC - 1);
-  if (cut_lo) {
-    #pragma unroll
-    for (int e = 0; e < NC; ++e)
-      if (e < lo) a[e] = __float_as_uint(-INFINITY);
+  // per 16-column block: a window edge inside a chunk usually crosses one
+  bool cut = false;
+  #pragma unroll
+  for (int b = 0; b < NC; b += 16) {
+    if (__any_sync(0xffffffffu, lo > b)) {
+      cut = true;
+      #pragma unroll
+      for (int e = b; e < b + 16; ++e)
+        if (e < lo) a[e] = __float_as_uint(-INFINITY);
+    }
+    if (__any_sync(0xffffffffu, hi < b + 15)) {
+      cut = true;
+      #pragma unroll
+      for (int e = b; e < b + 16; ++e)
+        if (e > hi) a[e] = __float_as_uint(-INFINITY);
+    }
   }
-  if (cut_hi) {
-    #pragma unroll
-    for (int e = 0; e < NC; ++e)
-      if (e > hi) a[e] = __float_as_uint(-INFINITY);
-  }
-  if (cut_lo || cut_hi) {
+  if (cut) {
     band_st<NC>(taddr, a);
     wrote = true;
   }
