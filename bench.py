@@ -55,6 +55,18 @@ def visible_pairs(lengths, causal: bool, window: int) -> int:
     return total
 
 
+def forward_kernel(w) -> str:
+    """The forward kernel the library launches for a workload: the
+    sliding-window kernel when a causal window's items (128 / G tokens x the G
+    query heads of a kv group) see at most 176 keys, else the tile kernel."""
+    g = w.heads_q // w.heads_kv
+    if w.causal and w.window > 0 and 128 % g == 0:
+        cols = -(-(128 // g + w.window - 1) // 16) * 16
+        if cols <= 176:
+            return "attn_sink_fwd_band_kernel"
+    return "attn_sink_fwd_kernel"
+
+
 def algorithmic(w, lengths):
     """Algorithmic flops (fwd 4 d, bwd 10 d per pair and head) and minimum bytes."""
     pairs = visible_pairs(lengths, w.causal, w.window)
@@ -74,6 +86,8 @@ def algorithmic(w, lengths):
 # GQA split), both of which decide its DRAM traffic
 KERNEL_SOURCES = {
     "attn_sink_fwd_kernel": ("fwd_kernel.cuh", "sm103_ptx.cuh", "attn_sink_api.cu"),
+    "attn_sink_fwd_band_kernel": ("fwd_band_kernel.cuh", "fwd_kernel.cuh", "sm103_ptx.cuh",
+                                  "attn_sink_api.cu"),
     "attn_sink_bwd_main_kernel": ("bwd_kernel.cuh", "sm103_ptx.cuh", "attn_sink_api.cu"),
 }
 
@@ -686,7 +700,7 @@ def main():
 
     rl_bwd = roofline("attn_sink_bwd_main_kernel", bwd_main_tf, bwd_main_gbs, bwd_main_ms,
                       alg["bwd_bytes"], alg["bwd_flops"])
-    rl_fwd = roofline("attn_sink_fwd_kernel", fwd_kernel_tf, fwd_kernel_gbs, fwd_kernel_ms,
+    rl_fwd = roofline(forward_kernel(w), fwd_kernel_tf, fwd_kernel_gbs, fwd_kernel_ms,
                       alg["fwd_bytes"], alg["fwd_flops"])
     dom, other = (rl_bwd, rl_fwd) if bwd_main_ms >= fwd_kernel_ms else (rl_fwd, rl_bwd)
     # Exponential-unit ceiling: one exp per visible pair and head in each pass,
