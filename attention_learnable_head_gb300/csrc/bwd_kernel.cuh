@@ -311,26 +311,44 @@ __device__ __forceinline__ void store_kv_grad_row(const BwdParams& p, int part, 
 // nl_row holds -lse * log2 e of the 64 queries.  Pairs of queries go through
 // the packed fp32 pair instructions; the exponentials stay per element.  With
 // kMask, entries whose (query, key) pair is not visible, or whose row or key
-// lies past the sequence, are exact zeros.
+// lies past the sequence, are exact zeros: per block of 16 queries, a block
+// that no key of the warp sees is written as zeros without its exponentials,
+// and only a block that some key sees in part is masked element by element.
+// The thread's visible queries are [lo, hi] (within the sequence; lo > hi for
+// none).
 template <bool kMask>
 __device__ __forceinline__ void bwd_p_chunk(const uint32_t* sr, const float* nl_row,
-                                            uint64_t sl2x2, int i_first, int imin, int imax,
-                                            int nq, bool key_ok, uint32_t* pk) {
+                                            uint64_t sl2x2, int i_first, int lo, int hi,
+                                            uint32_t* pk) {
   #pragma unroll
-  for (int e = 0; e < 64; e += 4) {
-    const float4 nl = *reinterpret_cast<const float4*>(nl_row + e);
+  for (int b = 0; b < 64; b += 16) {
+    const int b0 = i_first + b;               // first query of the block
+    bool none = false, part = false;
+    if (kMask) {
+      none = __all_sync(0xffffffffu, b0 + 15 < lo || b0 > hi);
+      part = __any_sync(0xffffffffu, b0 < lo || b0 + 15 > hi);
+    }
+    if (none) {
+      #pragma unroll
+      for (int e = b; e < b + 16; e += 2) pk[e >> 1] = 0u;
+      continue;
+    }
     #pragma unroll
-    for (int u = 0; u < 4; u += 2) {
-      const uint64_t x = ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])),
-                               sl2x2, u == 0 ? f2(nl.x, nl.y) : f2(nl.z, nl.w));
-      float p0 = ex2_approx(f2_lo(x));
-      float p1 = ex2_approx(f2_hi(x));
-      if (kMask) {
-        const int i = i_first + e + u;
-        if (!key_ok || i < imin || i > imax || i >= nq) p0 = 0.0f;
-        if (!key_ok || i + 1 < imin || i + 1 > imax || i + 1 >= nq) p1 = 0.0f;
+    for (int e = b; e < b + 16; e += 4) {
+      const float4 nl = *reinterpret_cast<const float4*>(nl_row + e);
+      #pragma unroll
+      for (int u = 0; u < 4; u += 2) {
+        const uint64_t x = ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])),
+                                 sl2x2, u == 0 ? f2(nl.x, nl.y) : f2(nl.z, nl.w));
+        float p0 = ex2_approx(f2_lo(x));
+        float p1 = ex2_approx(f2_hi(x));
+        if (part) {
+          const int i = i_first + e + u;
+          if (i < lo || i > hi) p0 = 0.0f;
+          if (i + 1 < lo || i + 1 > hi) p1 = 0.0f;
+        }
+        pk[(e + u) >> 1] = pack_f16x2(p0, p1);
       }
-      pk[(e + u) >> 1] = pack_f16x2(p0, p1);
     }
   }
 }
@@ -676,10 +694,13 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tmem_ld_x32(tST + 32, sr + 32);
         tmem_ld_wait();
         const float* nl_row = &s_nL[st][64 * hh];
+        // this key's visible queries within the sequence
+        const int vis_lo = key_ok ? imin : 1;
+        const int vis_hi = key_ok ? min(imax, sp.nq - 1) : 0;
         if (need_mask)
-          bwd_p_chunk<true>(sr, nl_row, sl2x2, i0, imin, imax, sp.nq, key_ok, pk);
+          bwd_p_chunk<true>(sr, nl_row, sl2x2, i0, vis_lo, vis_hi, pk);
         else
-          bwd_p_chunk<false>(sr, nl_row, sl2x2, i0, imin, imax, sp.nq, key_ok, pk);
+          bwd_p_chunk<false>(sr, nl_row, sl2x2, i0, vis_lo, vis_hi, pk);
       }
       tmem_st_x16(tST, pk);
       tmem_st_x16(tST + 16, pk + 16);
