@@ -18,6 +18,7 @@
 #include "fwd_band_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "merge_kernel.cuh"
+#include "schedule_kernel.cuh"
 
 // Device word a kernel sets when it gives up on a bounded wait.
 __device__ int g_attn_sink_device_error = 0;
@@ -248,9 +249,41 @@ int encode_rows(CUtensorMap* m, const void* ptr, long long tokens, int heads,
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Forward workspace: the fp16 copy of v.
-size_t fwd_workspace_bytes(const attn_sink_params* p, const Geometry& g) {
+// Entries of the tile-order table of a packed batch of several sequences
+// (schedule_kernel.cuh; query tiles, or key tiles with by_keys): at least the
+// number of 128-row tiles; 0 where the dense (tile, sequence) grid is used.
+int order_slots(const Geometry& g, bool by_keys) {
+  if (!g.varlen || g.num_seqs < 2) return 0;
+  const long long total = by_keys ? g.total_k : g.total_q;
+  const long long slots = (total + kBlockM - 1) / kBlockM + g.num_seqs;
+  return slots <= 65535 ? (int)slots : 0;
+}
+
+// Launches the sort of a packed batch's tiles into `table` (see order_slots).
+bool launch_order(const attn_sink_params* p, const Geometry& g, const int* cu_q,
+                  const int* cu_k, bool by_keys, bool chunk, int q_pos0, int slots,
+                  uint32_t* table, cudaStream_t stream) {
+  SchedParams sp;
+  sp.cu_q = cu_q;
+  sp.cu_k = cu_k;
+  sp.num_seqs = g.num_seqs;
+  sp.causal = p->causal;
+  sp.window = p->window > 0 ? p->window : 0;
+  sp.chunk = chunk ? 1 : 0;
+  sp.q_pos0 = chunk ? q_pos0 : 0;
+  sp.by_keys = by_keys ? 1 : 0;
+  sp.n_slots = slots;
+  sp.table = table;
+  attn_sink_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(sp);
+  return launched();
+}
+
+// Forward workspace: the fp16 copy of v, then the tile-order table.
+size_t fwd_v16_bytes(const attn_sink_params* p, const Geometry& g) {
   return align256((size_t)g.total_k * p->heads_kv * kHeadDim * 2);
+}
+size_t fwd_workspace_bytes(const attn_sink_params* p, const Geometry& g) {
+  return fwd_v16_bytes(p, g) + align256((size_t)order_slots(g, false) * sizeof(uint32_t));
 }
 
 // How many CTAs share one (kv head, key tile) in the backward pass.  Splitting
@@ -286,7 +319,9 @@ int choose_split(const attn_sink_params* p, const Geometry& g, int sm_count) {
 }
 
 struct BwdLayout {
-  size_t off_D, off_part, off_dq, off_dk, off_dv, off_q16, off_do16, off_k16, off_v16, total;
+  size_t off_D, off_part, off_dq, off_dk, off_dv, off_q16, off_do16, off_k16, off_v16, off_work,
+      total;
+  int slots;   // entries of the key-tile order table (0: dense grid)
   int n_blocks;
   int split;
 };
@@ -317,6 +352,9 @@ BwdLayout bwd_layout(const attn_sink_params* p, const Geometry& g, int sm_count)
   off += align256(k16);
   L.off_v16 = off;
   off += align256(k16);
+  L.slots = order_slots(g, true);
+  L.off_work = off;
+  off += align256((size_t)L.slots * sizeof(uint32_t));
   L.total = off;
   return L;
 }
@@ -432,9 +470,9 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   int st = validate(params, cu_seqlens_q, cu_seqlens_k, &g);
   if (st != ATTN_SINK_OK) return st;
   if (g.num_seqs == 0 || g.total_q == 0) return ATTN_SINK_OK;   // nothing to compute
-  const size_t v16_bytes = fwd_workspace_bytes(params, g);
-  if (v16_bytes > 0 && (workspace == nullptr || workspace_bytes < v16_bytes ||
-                        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+  const size_t ws_bytes = fwd_workspace_bytes(params, g);
+  if (ws_bytes > 0 && (workspace == nullptr || workspace_bytes < ws_bytes ||
+                       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return ATTN_SINK_ERR_WORKSPACE;
   if (q == nullptr || (!chunk && sink == nullptr) || out == nullptr || lse == nullptr)
     return ATTN_SINK_ERR_INVALID_ARG;
@@ -501,6 +539,16 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
 #endif
   if (fp.n_qtiles == 0) return ATTN_SINK_OK;
   dim3 grid(params->heads_q, fp.n_qtiles, g.num_seqs);
+  const int slots = order_slots(g, false);
+  if (slots > 0) {
+    uint32_t* table =
+        reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + fwd_v16_bytes(params, g));
+    if (!launch_order(params, g, cu_seqlens_q, cu_seqlens_k, false, chunk, q_pos0, slots, table,
+                      static_cast<cudaStream_t>(stream)))
+      return ATTN_SINK_ERR_CUDA;
+    fp.work = table;
+    grid = dim3(params->heads_q, slots, 1);
+  }
   const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_FWD, static_cast<cudaStream_t>(stream));
   attn_sink_fwd_kernel<<<grid, kFwdThreads, kFwdSmemBytes, static_cast<cudaStream_t>(stream)>>>(fp);
   const bool ok = launched();
@@ -856,6 +904,13 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
     bp.skip_q_step = g_test_skip_q_step.load();
 #endif
     dim3 grid(params->heads_kv * L.split, n_ktiles, g.num_seqs);
+    if (L.slots > 0) {
+      uint32_t* table = reinterpret_cast<uint32_t*>(ws + L.off_work);
+      if (!launch_order(params, g, cu_seqlens_q, cu_seqlens_k, true, false, 0, L.slots, table, s))
+        return ATTN_SINK_ERR_CUDA;
+      bp.work = table;
+      grid = dim3(params->heads_kv * L.split, L.slots, 1);
+    }
     const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_BWD_MAIN, s);
     attn_sink_bwd_main_kernel<<<grid, kBwdThreads, kBwdSmemBytes, s>>>(bp);
     const bool ok = launched();

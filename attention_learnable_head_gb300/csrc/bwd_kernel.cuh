@@ -80,6 +80,9 @@ struct BwdParams {
   float scale;         // softmax_scale
   float scale_log2;    // softmax_scale * log2(e)
   int n_ktiles;        // key tiles of the longest sequence
+  // Packed batches of several sequences: the key tile of CTA row blockIdx.y,
+  // as seq << 16 | key tile, heaviest first (null: blockIdx.y / z give them)
+  const uint32_t* work;
   int grad_fp32;
   int skip_dq;         // 1: no dQ here (the deterministic dQ kernel computes it)
 #ifdef ATTN_SINK_TEST_HOOKS
@@ -389,9 +392,19 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
   const int hpc = p.group / p.split;       // query heads handled by this CTA
   const int h_first = g * p.group + part * hpc;
   // Key tiles vary before sequences (low key tiles carry the most work: first),
-  // so the CTAs resident at one time work on one sequence.
-  const int ktile = blockIdx.y;
-  const int seq = blockIdx.z;
+  // so the CTAs resident at one time work on one sequence; a packed batch of
+  // several sequences takes its tiles from a table sorted by work across all
+  // sequences.
+  int ktile, seq;
+  if (p.work != nullptr) {
+    const uint32_t wk = p.work[blockIdx.y];
+    if (wk == kNoWork) return;                 // uniform per CTA
+    seq = (int)(wk >> 16);
+    ktile = (int)(wk & 0xFFFFu);
+  } else {
+    ktile = blockIdx.y;
+    seq = blockIdx.z;
+  }
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
   const int j0 = ktile * kBlockN;
   if (j0 >= sp.nk) return;                 // uniform per CTA

@@ -61,6 +61,9 @@ constexpr uint32_t kPTileBytes = kBlockM * kBlockN * 2;   // 32 KB bf16 tile (bw
 #define TEST_HOOK_FWD_ISSUE_K(n) true
 #endif
 
+// An unused entry of a tile-order table (schedule_kernel.cuh).
+constexpr uint32_t kNoWork = 0xFFFFFFFFu;
+
 constexpr int kFwdKStages = 3;      // K ring depth
 constexpr int kFwdVStages = 2;      // V ring depth
 constexpr int kFwdThreads = 320;    // 8 softmax warps, TMA warp, MMA warp
@@ -93,6 +96,9 @@ struct FwdParams {
   int causal, window;
   float scale_log2;   // softmax_scale * log2(e)
   int n_qtiles;       // 128-row query tiles of the longest sequence
+  // Packed batches of several sequences: the tile of CTA row blockIdx.y, as
+  // seq << 16 | query tile, heaviest first (null: blockIdx.y / z give them)
+  const uint32_t* work;
   // Key-chunk mode: no sink term, and query row i of every sequence sits at key
   // position i + q_pos0 (the default is bottom-right: q_pos0 = N_k - N_q).
   int chunk;
@@ -159,10 +165,19 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
 
   // Heads vary fastest (the query heads of a GQA group share K/V tiles in L2),
   // then query tiles, longest work first, then sequences, so the CTAs resident
-  // at one time read one sequence's keys.
+  // at one time read one sequence's keys; a packed batch of several sequences
+  // takes its tiles from a table sorted by work across all sequences.
   const int h = blockIdx.x;
-  const int qtile = p.n_qtiles - 1 - (int)blockIdx.y;
-  const int seq = blockIdx.z;
+  int qtile, seq;
+  if (p.work != nullptr) {
+    const uint32_t wk = p.work[blockIdx.y];
+    if (wk == kNoWork) return;                            // uniform per CTA
+    seq = (int)(wk >> 16);
+    qtile = (int)(wk & 0xFFFFu);
+  } else {
+    qtile = p.n_qtiles - 1 - (int)blockIdx.y;
+    seq = blockIdx.z;
+  }
   const SeqSpan sp = seq_span(p.cu_q, p.cu_k, seq, p.seqlen_q, p.seqlen_k);
   const int i0 = qtile * kBlockM;
   if (i0 >= sp.nq) return;                                // uniform per CTA

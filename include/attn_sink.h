@@ -248,9 +248,11 @@ int attn_sink_bwd_ex(const attn_sink_params* params, int flags, const void* q, c
 
 /*
  * Bytes of device workspace attn_sink_fwd needs (0 if the params are invalid):
- * an fp16 copy of v [T_k, H_kv, 64] for the tensor cores.  Same conventions as
- * attn_sink_bwd_workspace_size (packed fields when num_seqs > 0).  A workspace
- * that is missing, too small or not 256-byte aligned returns
+ * an fp16 copy of v [T_k, H_kv, 64] for the tensor cores and, for a packed
+ * batch of two or more sequences, a table of its query tiles in the order the
+ * forward runs them (heaviest first across sequences; 4 bytes a tile).  Same
+ * conventions as attn_sink_bwd_workspace_size (packed fields when num_seqs >
+ * 0).  A workspace that is missing, too small or not 256-byte aligned returns
  * ATTN_SINK_ERR_WORKSPACE.
  */
 size_t attn_sink_fwd_workspace_size(const attn_sink_params* params);
@@ -270,7 +272,8 @@ size_t attn_sink_fwd_workspace_size(const attn_sink_params* params);
  * this entry point; it is a deployment convenience.)
  *
  * Same arguments, layouts and results as attn_sink_fwd, minus the workspace.
- * The scratch it needs (the fp16 copy of v, attn_sink_fwd_workspace_size bytes)
+ * The scratch it needs (attn_sink_fwd_workspace_size bytes: the fp16 copy of v
+ * and the tile order)
  * lives in a file-scope device array of ATTN_SINK_NOALLOC_SCRATCH_BYTES; a
  * problem that needs more returns ATTN_SINK_ERR_WORKSPACE and launches nothing.
  * The call allocates nothing.
@@ -296,7 +299,8 @@ int attn_sink_fwd_noalloc(const attn_sink_params* params, const void* q, const v
  * per-block dsink partials, the fp32 dq accumulator [T_q, H_q, 64] (bf16 dq
  * only), fp16 copies of q, dout, k and v, and, when the backward splits a GQA
  * group over several CTAs (decided from the shapes and the current device's SM
- * count), fp32 dK/dV partials.
+ * count), fp32 dK/dV partials, and for a packed batch of two or more
+ * sequences a table of its key tiles in the order the backward runs them.
  * Query it on the device the backward will run on.
  */
 size_t attn_sink_bwd_workspace_size(const attn_sink_params* params);

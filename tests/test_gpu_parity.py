@@ -53,6 +53,17 @@ def test_small_cases(name, hq, hkv, lengths, causal, window, grad_dtype):
     check_against(run_gpu(c, grad_dtype=grad_dtype), _ref(c))
 
 
+def test_many_sequences_tile_order():
+    """A packed batch of 300 sequences of 1..400 tokens (and one of 1100): the
+    forward and backward run their tiles from a table sorted by work across
+    all sequences; every tile of every sequence must be computed once."""
+    g = torch.Generator().manual_seed(515)
+    lengths = [int(x) for x in torch.randint(1, 401, (300,), generator=g)] + [1100]
+    w = small_workload("many_seqs", 515, 4, 2, lengths, causal=True)
+    c = make_case(w)
+    check_against(run_gpu(c), _ref(c))
+
+
 def test_dense_batch_layout():
     w = small_workload("dense", 411, 8, 2, [200, 200, 200], causal=True)
     c = make_case(w)
