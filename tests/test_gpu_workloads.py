@@ -95,18 +95,22 @@ def test_varlen():
 
 
 def test_long_full():
+    """Sampled rows of every head and sequence (forward), and the whole
+    forward and backward of two kv groups: group 3 of sequence 1 and group 6
+    of sequence 3 (the last one, whose tiles run last)."""
     c = make_case(WORKLOADS["long_full"])
     res = run_gpu(c, dense=True)
     _check_rows(res, c, _sampled_rows(c, per_seq=12))
-    ref = _oracle(c, heads=_group_heads([3]), seqs=[1])
     n = c.lengths[0]
-    rows = slice(n, 2 * n)
-    for name in ("out", "dq"):
-        sel = (rows, slice(24, 32))
-        check_tensor(res, ref[name][sel], name, sel)
-    for name in ("dk", "dv"):
-        sel = (rows, slice(3, 4))
-        check_tensor(res, ref[name][sel], name, sel)
+    for kv, seq in ((3, 1), (6, 3)):
+        ref = _oracle(c, heads=_group_heads([kv]), seqs=[seq])
+        rows = slice(seq * n, (seq + 1) * n)
+        for name in ("out", "dq"):
+            sel = (rows, slice(8 * kv, 8 * kv + 8))
+            check_tensor(res, ref[name][sel], name, sel)
+        for name in ("dk", "dv"):
+            sel = (rows, slice(kv, kv + 1))
+            check_tensor(res, ref[name][sel], name, sel)
     ref = _oracle(c, heads=[5, 40])
     check_against({"dsink": res["dsink"]}, ref, heads=[5, 40])
 
