@@ -629,7 +629,7 @@ bool decode_group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 struct DecodeLayout {
   int splits;
-  size_t off_lo, off_lse, total;
+  size_t off_lo, off_lse, off_done, total;
 };
 
 // Key splits: enough (batch x kv head x split) CTAs for about eight waves of
@@ -655,7 +655,8 @@ bool decode_layout(const attn_sink_decode_params* p, int sm_count, DecodeLayout*
   const size_t o = (size_t)s * p->batch * p->heads_q * 64 * 2;   // bf16
   L->off_lo = align256(o);
   L->off_lse = L->off_lo + align256(o);
-  L->total = L->off_lse + align256((size_t)s * p->heads_q * p->batch * sizeof(float));
+  L->off_done = L->off_lse + align256((size_t)s * p->heads_q * p->batch * sizeof(float));
+  L->total = L->off_done + align256((size_t)p->batch * p->heads_kv * sizeof(int));
   return true;
 }
 
@@ -715,6 +716,11 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
   dp.o_part = reinterpret_cast<__nv_bfloat16*>(ws);
   dp.o_part_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.off_lo);
   dp.lse_part = reinterpret_cast<float*>(ws + L.off_lse);
+  dp.done = reinterpret_cast<int*>(ws + L.off_done);
+  dp.sink = sink;
+  dp.out = static_cast<__nv_bfloat16*>(out);
+  dp.out_lo = static_cast<__nv_bfloat16*>(out_residual);
+  dp.lse = lse;
   dp.err = err;
   dp.batch = params->batch;
   dp.heads_q = params->heads_q;
@@ -739,6 +745,10 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
                           CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, box)) != ATTN_SINK_OK)
       return st;
   }
+  // the per-(sequence, kv head) completion counters start at zero
+  if (cudaMemsetAsync(dp.done, 0, (size_t)params->batch * params->heads_kv * sizeof(int), s) !=
+      cudaSuccess)
+    return ATTN_SINK_ERR_CUDA;
   const dim3 grid(L.splits, params->heads_kv, params->batch);
   switch ((params->heads_q / params->heads_kv) * 2 + (tma ? 1 : 0)) {
     case 2: attn_sink_decode_kernel<1, false><<<grid, kDecThreads, 0, s>>>(dp); break;
@@ -750,9 +760,7 @@ int attn_sink_decode(const attn_sink_decode_params* params, const void* q, const
     case 16: attn_sink_decode_kernel<8, false><<<grid, kDecThreads, 0, s>>>(dp); break;
     default: attn_sink_decode_kernel<8, true><<<grid, kDecThreads, 0, s>>>(dp); break;
   }
-  if (!launched()) return ATTN_SINK_ERR_CUDA;
-  return attn_sink_merge(L.splits, params->batch, params->heads_q, kHeadDim, dp.o_part,
-                         dp.o_part_lo, dp.lse_part, sink, out, out_residual, lse, stream);
+  return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
 }
 
 size_t attn_sink_fwd_workspace_size(const attn_sink_params* params) {

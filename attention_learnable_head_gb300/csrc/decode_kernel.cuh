@@ -10,8 +10,10 @@
 //
 // Split-KV: CTA (split, kv head g, sequence b) attends the G = H_q / H_kv
 // query heads of g to one slice of b's keys, without the sink, and writes the
-// slice's normalised result and log-sum-exp; attn_sink_merge_kernel then adds
-// the sink once (the merge of the key-chunk forward).
+// slice's normalised result and log-sum-exp.  The last of the (b, g) CTAs to
+// finish (a counter per (b, g), zeroed before the launch) merges the slices
+// and adds the sink once, as attn_sink_merge_kernel does for key chunks, so a
+// decode step is one launch.
 //
 // The G query heads are the rows of a skinny product (G <= 8, padded to the 16
 // rows of a warp-level mma.sync m16n8k16; a tcgen05 MMA needs 64 or more rows).
@@ -49,6 +51,11 @@ struct DecodeParams {
   __nv_bfloat16* o_part;          // [splits][B][H_q][64] slice results
   __nv_bfloat16* o_part_lo;       // residuals of o_part
   float* lse_part;                // [splits][H_q][B] (natural log), -inf: no key
+  int* done;                      // [B][H_kv] CTAs of (b, g) finished (zero at launch)
+  const float* sink;              // [H_q]
+  __nv_bfloat16* out;             // [B][H_q][64]
+  __nv_bfloat16* out_lo;          // residual of out, or null
+  float* lse;                     // [H_q][B] (natural log)
   int* err;
   int batch, heads_q, heads_kv;
   int page_size, num_pages, max_pages;
@@ -76,6 +83,7 @@ attn_sink_decode_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ __align__(8) uint64_t kv_full[kDecStages];   // TMA path: the stage's copies landed
   __shared__ float s_m[kDecWarps][kDecMaxGroup];
   __shared__ float s_l[kDecWarps][kDecMaxGroup];
+  __shared__ int s_last;
   // the warps' O rows for the final merge reuse the K/V stages (free by then)
   float (*s_o)[kDecMaxGroup][64] = reinterpret_cast<float (*)[kDecMaxGroup][64]>(&s_kv[0][0][0]);
   static_assert(sizeof(float) * kDecWarps * kDecMaxGroup * 64 <= sizeof(s_kv),
@@ -408,6 +416,54 @@ attn_sink_decode_kernel(const __grid_constant__ DecodeParams p) {
     if (d0 == 0)
       p.lse_part[((size_t)split * p.heads_q + hq) * p.batch + b] =
           (ll > 0.0f) ? (mm + __log2f(ll)) * kLn2Dec : -INFINITY;
+  }
+
+  // ---- the last CTA of (b, g) merges the slices with the sink:
+  //   Z = sum_c exp(LSE_c) + exp(sink),  O = sum_c exp(LSE_c - log Z) O_c,
+  //   LSE = log Z (natural log; the merge of the key-chunk forward).
+  // Every CTA's slice results are visible before its count (fence, then the
+  // atomic); the last one fences again before it reads the others'.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0)
+    s_last = atomicAdd(p.done + (size_t)b * p.heads_kv + g, 1) == p.splits - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (h < G) {
+    const int hq = g * G + h;
+    const float sk = __ldg(p.sink + hq);
+    float m = sk;
+    for (int c = 0; c < p.splits; ++c)
+      m = fmaxf(m, __ldcg(p.lse_part + ((size_t)c * p.heads_q + hq) * p.batch + b));
+    const float m_use = (m == -INFINITY) ? 0.0f : m;
+    float z = (sk == -INFINITY) ? 0.0f : __expf(sk - m_use);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int c = 0; c < p.splits; ++c) {
+      const float lc = __ldcg(p.lse_part + ((size_t)c * p.heads_q + hq) * p.batch + b);
+      if (lc == -INFINITY) continue;                // the slice had no key
+      const float wc = __expf(lc - m_use);
+      z += wc;
+      const size_t ci = (((size_t)c * p.batch + b) * p.heads_q + hq) * 64 + d0;
+      const uint2 o = __ldcg(reinterpret_cast<const uint2*>(p.o_part + ci));
+      const uint2 r = __ldcg(reinterpret_cast<const uint2*>(p.o_part_lo + ci));
+      acc[0] = fmaf(wc, bf16_lo(o.x) + bf16_lo(r.x), acc[0]);
+      acc[1] = fmaf(wc, bf16_hi(o.x) + bf16_hi(r.x), acc[1]);
+      acc[2] = fmaf(wc, bf16_lo(o.y) + bf16_lo(r.y), acc[2]);
+      acc[3] = fmaf(wc, bf16_hi(o.y) + bf16_hi(r.y), acc[3]);
+    }
+    const float inv_z = (z > 0.0f) ? 1.0f / z : 0.0f;
+    uint32_t hi[2], lo2[2];
+    #pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float f0 = acc[2 * e] * inv_z, f1 = acc[2 * e + 1] * inv_z;
+      hi[e] = pack_bf16x2(f0, f1);
+      lo2[e] = pack_bf16x2(f0 - bf16_lo(hi[e]), f1 - bf16_hi(hi[e]));
+    }
+    const size_t oi = ((size_t)b * p.heads_q + hq) * 64 + d0;
+    *reinterpret_cast<uint2*>(p.out + oi) = make_uint2(hi[0], hi[1]);
+    if (p.out_lo) *reinterpret_cast<uint2*>(p.out_lo + oi) = make_uint2(lo2[0], lo2[1]);
+    if (d0 == 0) p.lse[(size_t)hq * p.batch + b] = (z > 0.0f) ? m_use + __logf(z) : -INFINITY;
   }
 }
 

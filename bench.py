@@ -388,9 +388,10 @@ def decode_case(batch: int, cached: int, heads_q: int, heads_kv: int, page: int,
 
 
 def run_decode(args):
-    """One step = attn_sink_decode (the split kernel and the sink merge) for a
-    batch of 128 sequences with 8192 cached keys each, H 64/8, page 16.  The
-    cache (2.1 GB) is larger than L2, so no flush is needed between steps."""
+    """One step = attn_sink_decode (one launch: the key-split kernel, whose last
+    CTA per (sequence, kv head) merges the splits with the sink) for a batch of
+    128 sequences with 8192 cached keys each, H 64/8, page 16.  The cache (2.1
+    GB) is larger than L2, so no flush is needed between steps."""
     from attention_learnable_head_gb300 import binding
     from attention_learnable_head_gb300.build import build
     B, L, HQ, HKV, PAGE, SCALE = 128, 8192, 64, 8, 16, 0.125

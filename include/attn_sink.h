@@ -184,7 +184,9 @@ typedef struct attn_sink_decode_params {
 
 /*
  * Bytes of device workspace attn_sink_decode needs (0 if the params are
- * invalid or batch = 0): the key-split partial results.
+ * invalid or batch = 0): the key-split partial results and a completion
+ * counter per (sequence, kv head), zeroed by the call before its one kernel
+ * launch (the last split of each pair merges the partials with the sink).
  */
 size_t attn_sink_decode_workspace_size(const attn_sink_decode_params* params);
 

@@ -18,21 +18,24 @@ from attention_learnable_head_gb300.inputs import make_case, small_workload
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(dev):
-    w = small_workload("noalloc", 991, 8, 2, [300, 129, 511], window=0)
+def _inputs(dev, window):
+    w = small_workload("noalloc", 991, 8, 2, [300, 129, 511], window=window)
     c = make_case(w)
     cu = torch.tensor(c.cu_seqlens, dtype=torch.int32, device=dev)
     t = [x.to(dev) for x in (c.q, c.k, c.v, c.sink)]
-    p = binding.make_params(c.q.shape, c.k.shape, causal=True, window=0,
+    p = binding.make_params(c.q.shape, c.k.shape, causal=True, window=window,
                             softmax_scale=w.scale, num_seqs=len(c.lengths),
                             max_seqlen_q=max(c.lengths), max_seqlen_k=max(c.lengths))
     return p, cu, t
 
 
-def test_noalloc_forward_matches_workspace_forward():
+@pytest.mark.parametrize("window", [0, 128])
+def test_noalloc_forward_matches_workspace_forward(window):
+    """Full causal (the tile kernel, with the packed batch's tile order in the
+    scratch) and W = 128 (the sliding-window kernel)."""
     build()
     dev = torch.device("cuda:0")
-    p, cu, (q, k, v, sink) = _inputs(dev)
+    p, cu, (q, k, v, sink) = _inputs(dev, window)
     ref_out, ref_res = torch.empty_like(q), torch.empty_like(q)
     ref_lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
     ws = torch.empty(binding.attn_sink_fwd_workspace_size(p), dtype=torch.uint8, device=dev)
