@@ -133,3 +133,16 @@ def test_decode_gptoss_serving_batch_sampled():
     ref_out, ref_lse = oracle_decode(q[idx], kc, vc, table[idx], lens_t[idx], sink, scale=0.125)
     assert_close("serving batch out", out[idx], ref_out)
     _check_lse(lse[:, idx], ref_lse)
+
+
+def test_decode_repeatable():
+    """The split results are merged by whichever CTA of a (sequence, kv head)
+    finishes last, in split order: ten runs of a batch with many splits per
+    sequence are bitwise equal (a stale or early read of another split's
+    partial would show up as a difference)."""
+    q, kc, vc, table, lens, sink = _paged_case(77, [4000, 3000, 17, 2500] * 8, 16, 16, 2)
+    first = _run(q, kc, vc, table, lens, sink, 0.125, 0)
+    for _ in range(9):
+        again = _run(q, kc, vc, table, lens, sink, 0.125, 0)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
