@@ -50,13 +50,16 @@ constexpr int kBandThreads = 320;
 constexpr int kBandTmaWarp = 8;
 constexpr int kBandMmaWarp = 9;
 constexpr uint32_t kBandTmemCols = 256;
-constexpr uint32_t kBandColO = 192;    // O: 64 fp32 columns
+constexpr uint32_t kBandColO = 176;    // O: 64 fp32 columns, then the row sum (16 columns)
+constexpr int kBandOCols = 80;         // N of the O product: 64 columns of V and one of ones
 constexpr int kBandMaxCols = 176;      // N: fits S below O and two CTAs' SMEM per SM
 constexpr int kBandCtasPerSm = 2;
 // Dynamic SMEM: Q (2 x 16 KB), K and V (N x 128 B each), the out and residual
-// staging tiles (2 x 16 KB), plus 1 KB of alignment slack.
+// staging tiles (2 x 16 KB), the ones block of the row sum (16 x 128 B), plus
+// 1 KB of alignment slack.
+constexpr int kBandOnesBytes = 16 * 128;
 __host__ __device__ constexpr int band_smem_bytes(int n_cols) {
-  return 1024 + 2 * (int)kTileBytes + 2 * n_cols * 128 + 2 * (int)kTileBytes;
+  return 1024 + 2 * (int)kTileBytes + 2 * n_cols * 128 + 2 * (int)kTileBytes + kBandOnesBytes;
 }
 constexpr int kBandSmemMax = band_smem_bytes(kBandMaxCols);
 
@@ -241,11 +244,11 @@ __device__ __forceinline__ float band_chunk_max(uint32_t taddr, int lo, int hi, 
 }
 
 // P = exp2(S * scale log2 e - m) of one chunk (masked columns hold -inf and
-// give 0), summed into rs and written as fp16 pairs to TMEM at tp (NC / 2
-// columns).
+// give 0), written as fp16 pairs to TMEM at tp (NC / 2 columns).  The row sum
+// of P is not formed here: the O product sums the fp16 P it multiplies.
 template <int NC>
 __device__ __forceinline__ void band_chunk_exp(uint32_t ts, uint32_t tp, uint64_t sl2x2,
-                                               uint64_t negm2, uint64_t& rs) {
+                                               uint64_t negm2) {
   uint32_t a[NC];
   band_ld<NC>(ts, a);
   tmem_ld_wait();
@@ -254,10 +257,7 @@ __device__ __forceinline__ void band_chunk_exp(uint32_t ts, uint32_t tp, uint64_
   for (int e = 0; e < NC; e += 2) {
     const uint64_t x =
         ffma2(f2(__uint_as_float(a[e]), __uint_as_float(a[e + 1])), sl2x2, negm2);
-    const float e0 = ex2_approx(f2_lo(x));
-    const float e1 = ex2_approx(f2_hi(x));
-    rs = fadd2(rs, f2(e0, e1));
-    pk[e >> 1] = pack_f16x2(e0, e1);
+    pk[e >> 1] = pack_f16x2(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
   }
   if constexpr (NC == 32) tmem_st_x16(tp, pk);
   else tmem_st_x8(tp, pk);
@@ -273,14 +273,10 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
   __shared__ __align__(8) uint64_t s_full, p_full, pv_done, o_free, mma_drained;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  // The halves' row maxima ([half][row]) and row sums.  One buffer of maxima
-  // is enough: S of the next item, before whose pass 1 a half rewrites its
-  // entry, needs P of this item from every thread, i.e. after its partner read
-  // it.  The sums are read one item later (in the deferred epilogue), so they
-  // alternate between two buffers; PV of the next item, behind which S of the
-  // item after that is issued, waits for every thread's epilogue read.
+  // The halves' row maxima ([half][row]).  One buffer is enough: S of the
+  // next item, before whose pass 1 a half rewrites its entry, needs P of this
+  // item from every thread, i.e. after its partner read it.
   __shared__ float s_mx[2][kBlockM];
-  __shared__ float s_red_l[2][2][kBlockM];   // [item parity][half][row]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -294,7 +290,18 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
   uint8_t* sV = sK + kv_bytes;               // N x 128 B
   uint8_t* sOut = sV + kv_bytes;             // 16 KB out tile, then 16 KB residual tile
   uint8_t* sOutLo = sOut + kTileBytes;
+  uint8_t* sOnes = sOutLo + kTileBytes;      // 16 rows x 128 B, see below
 
+  // The ones block: the second 64-wide block of the O product's B operand (V
+  // is MN-major, 128-byte rows of 64 values), read for every 16-key step: 16
+  // rows whose first value (output column 64, the row sum) is 1 and the rest 0,
+  // 128B-swizzled like the V rows (16-byte chunk j of row r at chunk j ^ (r % 8)).
+  for (int i = tid; i < kBandOnesBytes / 4; i += kBandThreads) {
+    const int row = i >> 5, word = i & 31;             // 32 words a row
+    const int first = ((0 ^ (row & 7)) << 2);          // word 0 of chunk 0, swizzled
+    reinterpret_cast<uint32_t*>(sOnes)[i] = (word == first) ? 0x3C00u : 0u;   // fp16 1.0
+  }
+  fence_proxy_async_smem();                            // the MMA (async proxy) reads it
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
@@ -403,10 +410,13 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
     // item's O has been read out.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(kBlockM, N, false, false);
-      const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
+      const uint32_t idesc_o = make_idesc(kFmtF16, kBlockM, kBandOCols, false, true);
       const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dK = make_sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV = make_sdesc_sw128(smem_u32(sV), 16384, 1024);   // MN-major
+      // V, MN-major; its second 64-wide block (output columns 64..127, of which
+      // the product reads 64..79) is the ones block, at the distance LBO from
+      // each 16-key step's start
+      const uint64_t dV = make_sdesc_sw128(smem_u32(sV), smem_u32(sOnes) - smem_u32(sV), 1024);
       constexpr uint32_t kQU = kTileBytes >> 4;
       const int ks0 = p.half0_cols >> 4;   // 16-key steps of half 0
       const int nks = N >> 4;
@@ -444,7 +454,9 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
         mma_ts(tmem + kBandColO, a_col, b_desc, idesc_o, 0);
         for (int kk = 1; kk < nks; ++kk) {
           a_col += (kk == ks0) ? 8u + 8u * ks0 : 8u;
+          // start 2048 bytes (16 rows) on, LBO 2048 bytes less: still the ones block
           b_desc += 128u;
+          b_desc -= (uint64_t)128u << 16;
           mma_ts(tmem + kBandColO, a_col, b_desc, idesc_o, 1);
         }
         mma_commit(&pv_done);
@@ -488,12 +500,13 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
     // left in its sequence from there, this row's max (log2 units)
     int pg = 0, ptok = 0, prem = 0;
     float pm = -INFINITY;
+    float psink = 0.0f;   // the previous item's sink term of the row sum, 2^(sink - m)
     BandWalk w;
     w.start(p);
     while (true) {
       const bool have = w.more(p);
       int ng = 0, ntok = 0, nrem = 0;
-      float m = -INFINITY;
+      float m = -INFINITY, nsink = 0.0f;
       if (have) {
         const BandItem& it = w.it;
         const int h = it.g * p.group + hh;
@@ -527,20 +540,18 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
           m = fmaxf(fmaxf(mx, s_mx[c ^ 1][r]) * sl2, sink_l2);
           const float m_use = (m == -INFINITY) ? 0.0f : m;
           const uint64_t negm2 = f2(-m_use, -m_use);
-          uint64_t rs = f2(0.0f, 0.0f);
+
           // P of keys [cc, cc + 32) goes to columns [cc / 2, cc / 2 + 16) of the
           // half: S columns this thread has already read.
           int cc = 0;
           #pragma unroll 1
           for (; cc + 32 <= nc; cc += 32)
-            band_chunk_exp<32>(tS + cc, tS + (cc >> 1), sl2x2, negm2, rs);
-          if (cc < nc) band_chunk_exp<16>(tS + cc, tS + (cc >> 1), sl2x2, negm2, rs);
+            band_chunk_exp<32>(tS + cc, tS + (cc >> 1), sl2x2, negm2);
+          if (cc < nc) band_chunk_exp<16>(tS + cc, tS + (cc >> 1), sl2x2, negm2);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&p_full);
-          float l = f2_lo(rs) + f2_hi(rs);
-          if (c == 0 && sink_h > -INFINITY) l += ex2_approx(sink_l2 - m_use);
-          s_red_l[li & 1][c][r] = l;
+          if (sink_h > -INFINITY) nsink = ex2_approx(sink_l2 - m_use);
         } else {
           abort_flag = 1;
         }
@@ -556,10 +567,13 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
           break;
         }
         tc_fence_after();
-        const float lt = s_red_l[(li - 1) & 1][0][r] + s_red_l[(li - 1) & 1][1][r];
+        // the row sum: the O product's column 64 (the fp16 P it multiplied,
+        // summed in fp32) plus the sink's term
         uint32_t o[32];
         tmem_ld_x32(tO, o);
+        const uint32_t lsum = tmem_ld_x1(tO - 32u * c + 64u);
         tmem_ld_wait();
+        const float lt = __uint_as_float(lsum) + psink;
         tc_fence_before();
         mbar_arrive(&o_free);
         const float inv_l = (lt > 0.0f) ? 1.0f / lt : 0.0f;
@@ -608,6 +622,7 @@ attn_sink_fwd_band_kernel(const __grid_constant__ FwdBandParams p) {
       ptok = ntok;
       prem = nrem;
       pm = m;
+      psink = nsink;
       ++li;
       w.advance(p);
     }
