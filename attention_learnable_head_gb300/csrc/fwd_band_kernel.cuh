@@ -16,8 +16,9 @@
 // which each row uses 128, against 256 of which 128 are used for a 128-token
 // tile of one head.  Because the whole window fits one S, the softmax is a
 // single pass: row max (with the sink logit), P = exp2(S * scale log2 e - m)
-// in fp16, O = P V in one product (K = N), out = O / l, lse = ln 2 (m +
-// log2 l); no running max, no rescaling of O.
+// in fp16, O = P V and l = sum P in one product (K = N), plus the sink's term
+// 2^(sink log2 e - m); out = O / l, lse = ln 2 (m + log2 l); no running max,
+// no rescaling of O.
 //
 // Persistent: gridDim.x CTAs (two per SM) walk the items item = blockIdx.x +
 // k gridDim.x, ordered kv group fastest, then token blocks, then sequences;
@@ -34,7 +35,9 @@
 // TMEM (256 columns): S in [0, N) as fp32; the softmax writes P (fp16 pairs)
 // over the S columns it has read, half 0 (keys [0, N0)) into columns
 // [0, N0/2), half 1 (keys [N0, N)) into [N0, N0 + (N - N0)/2), so every
-// 16-key step of PV reads 8 consecutive columns; O in [192, 256).  S of the
+// 16-key step of PV reads 8 consecutive columns; O in [176, 256): the product
+// has N = 80, its columns 64..79 multiplying a constant block of ones, so
+// column 64 is the row sum of the fp16 P (no sum in the softmax).  S of the
 // next item is issued after PV of this one, which reads P first (tcgen05 MMAs
 // of a CTA run in issue order).
 //
