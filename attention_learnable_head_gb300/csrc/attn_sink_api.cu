@@ -497,6 +497,10 @@ int fwd_impl(const attn_sink_params* params, const void* q, const void* k, const
   if ((st = encode_rows(&fp.tm_k, kp, tk, hk)) != ATTN_SINK_OK) return st;
   if ((st = encode_rows(&fp.tm_v, vp, tk, hk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != ATTN_SINK_OK)
     return st;
+  if ((st = encode_rows(&fp.tm_out, out, g.total_q, params->heads_q)) != ATTN_SINK_OK ||
+      (st = encode_rows(&fp.tm_out_lo, out_residual ? out_residual : out, g.total_q,
+                        params->heads_q)) != ATTN_SINK_OK)
+    return st;
   if (g.total_k > 0) {
     // fp16 copy of v for the P V products
     const size_t n8 = (size_t)g.total_k * params->heads_kv * kHeadDim / 8;

@@ -82,6 +82,8 @@ struct FwdParams {
   CUtensorMap tm_q;   // [T_q][H_q][64] bf16, box 64 x 1 x 128, 128B swizzle
   CUtensorMap tm_k;   // [T_k][H_kv][64]
   CUtensorMap tm_v;
+  CUtensorMap tm_out;     // out, box 64 x 1 x 128 (stores of whole tiles)
+  CUtensorMap tm_out_lo;  // its residual (unused without one)
   const int* cu_q;    // null for a dense batch
   const int* cu_k;
   const float* sink;  // [H_q] fp32, or
@@ -504,10 +506,13 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
       uint32_t o[32];
       tmem_ld_x32(tO, o);
       tmem_ld_wait();
-      if (valid) {
+      // A whole tile goes out through two 128B-swizzled SMEM tiles (the K ring,
+      // idle now: every copy into it has been consumed) and TMA stores, which
+      // run on while the CTA ends; a tile past its sequence's end stores its
+      // valid rows directly.
+      const bool whole = i0 + kBlockM <= sp.nq;             // same for every row
+      if (whole || valid) {
         const size_t base = (row * p.heads_q + h) * kHeadDim + 32 * c;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + base);
-        uint4* dlo = p.out_lo ? reinterpret_cast<uint4*>(p.out_lo + base) : nullptr;
         #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float f[8];
@@ -519,11 +524,31 @@ attn_sink_fwd_kernel(const __grid_constant__ FwdParams p) {
             hi[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
             lo2[e] = pack_bf16x2(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
           }
-          dst[u] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          if (dlo) dlo[u] = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+          if (whole) {
+            const uint32_t off = sw128_offset((uint32_t)r, (uint32_t)(4 * c + u));
+            st_shared_v4(smem_u32(sK) + off, hi[0], hi[1], hi[2], hi[3]);
+            if (p.out_lo)
+              st_shared_v4(smem_u32(sK) + kTileBytes + off, lo2[0], lo2[1], lo2[2], lo2[3]);
+          } else {
+            reinterpret_cast<uint4*>(p.out + base)[u] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            if (p.out_lo)
+              reinterpret_cast<uint4*>(p.out_lo + base)[u] =
+                  make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+          }
         }
-        if (c == 0)
+        if (c == 0 && valid)
           p.lse[(size_t)h * p.total_q + row] = (lt > 0.0f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+      }
+      if (whole) {
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 2 * kBlockM);
+        if (warp == 0 && lane == 0) {
+          const uint64_t once = l2_policy_evict_first();
+          tma_store_3d_hint(&p.tm_out, sK, 0, h, sp.q0 + i0, once);
+          if (p.out_lo) tma_store_3d_hint(&p.tm_out_lo, sK + kTileBytes, 0, h, sp.q0 + i0, once);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // the tiles are read before the CTA releases SMEM
+        }
       }
     }
   }
