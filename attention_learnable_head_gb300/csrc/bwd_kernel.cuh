@@ -548,7 +548,8 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
     //                the next dP^T, so that the compute warps' next operand is
     //                ahead of them in the tensor pipe
     // A stage of Q/dO is refilled once both issuers' commits on q_empty have
-    // landed; B's commit on ds_free[b] releases dS^T buffer b two steps later.
+    // landed (A's after dV, B's after dK); B's commit on ds_free[b] releases
+    // dS^T buffer b two steps later.
     if (lane == 0) {
       const bool issuer_a = warp == kBwdMmaWarp;
       const uint32_t id_s = make_idesc(kFmtF16, kBlockN, kBlockM, false, false);
@@ -628,6 +629,10 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
           for (int k = 0; k < kBlockM / 16; ++k)
             mma_ss(tmem + kColDK, dS_k + so + (k >> 2) * kTileU + 2 * (k & 3),
                    dQ_mn + st * kTileU + 128 * k, id_dvdk, (m > 0 || k > 0));
+          // dK is this step's last reader of its Q/dO stage (dQ reads dS^T and
+          // K): release the stage now, not after dQ, so that its refill starts
+          // earlier
+          mma_commit(&q_empty[st]);
           if (!p.skip_dq) {
             // the dQ warps have read the previous dQ out of TMEM
             if (!mbar_wait(&dq_free, m & 1, &abort_flag)) { ok = false; break; }
@@ -639,7 +644,6 @@ attn_sink_bwd_main_kernel(const __grid_constant__ BwdParams p) {
             mma_commit(&mma2_done);
           }
           mma_commit(&ds_free[m & 1]);
-          mma_commit(&q_empty[st]);
         }
       }
       if (!ok) {
