@@ -319,6 +319,8 @@ def attn_sink_launch_count() -> int:
 
 ATTN_SINK_KERNEL_FWD = 0
 ATTN_SINK_KERNEL_BWD_MAIN = 1
+ATTN_SINK_KERNEL_BWD_DQ = 2
+ATTN_SINK_KERNEL_MERGE = 3
 
 
 def attn_sink_kernel_timing(on: bool) -> int:

@@ -50,7 +50,7 @@ inline bool launched() {
   return true;
 }
 
-// Optional per-launch timing of the two main kernels (attn_sink_kernel_timing):
+// Optional per-launch timing of the library's main kernels (attn_sink_kernel_timing):
 // an event pair recorded on the launching stream around each launch, read back
 // and summed by attn_sink_kernel_time.  Events are reused through a pool.
 struct TimedLaunch {
@@ -620,8 +620,11 @@ int attn_sink_merge(int num_chunks, int total_q, int heads_q, int head_dim, cons
   mp.heads_q = heads_q;
   const size_t pairs = (size_t)total_q * heads_q;
   const int blocks = (int)std::min<size_t>((pairs + 31) / 32, (size_t)sms * 8);
+  const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_MERGE, static_cast<cudaStream_t>(stream));
   attn_sink_merge_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(mp);
-  return launched() ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
+  const bool ok = launched();
+  timing_end(t, static_cast<cudaStream_t>(stream), ok);
+  return ok ? ATTN_SINK_OK : ATTN_SINK_ERR_CUDA;
 }
 
 }  // extern "C"
@@ -970,9 +973,12 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
     dp.scale_log2 = scale * kLog2e;
     dp.n_qtiles = n_qtiles;
     dp.grad_fp32 = params->grad_dtype;
+    const TimedLaunch t = timing_begin(ATTN_SINK_KERNEL_BWD_DQ, s);
     attn_sink_bwd_dq_kernel<<<dim3(params->heads_q, g.num_seqs, n_qtiles), kDqThreads,
                               kDqSmemBytes, s>>>(dp);
-    if (!launched()) return ATTN_SINK_ERR_CUDA;
+    const bool ok = launched();
+    timing_end(t, s, ok);
+    if (!ok) return ATTN_SINK_ERR_CUDA;
   }
   // 3'. dq (bf16) from the fp32 accumulator
   if (!deterministic && g.total_q > 0 && params->grad_dtype == 0) {

@@ -387,12 +387,16 @@ int attn_sink_last_cuda_error(void);
  * Measurement hooks (no counterpart in the papers: they time this library's
  * own kernels).  Kernel ids for attn_sink_kernel_time:
  */
-#define ATTN_SINK_KERNEL_FWD 0      /* attn_sink_fwd_kernel (the whole forward product) */
-#define ATTN_SINK_KERNEL_BWD_MAIN 1 /* attn_sink_bwd_main_kernel (all five backward products) */
-#define ATTN_SINK_KERNEL_COUNT 2
+#define ATTN_SINK_KERNEL_FWD 0      /* the forward kernel: attn_sink_fwd_kernel or, for a
+                                       sliding window, attn_sink_fwd_band_kernel */
+#define ATTN_SINK_KERNEL_BWD_MAIN 1 /* attn_sink_bwd_main_kernel (all five backward products;
+                                       without dQ under attn_sink_bwd_deterministic) */
+#define ATTN_SINK_KERNEL_BWD_DQ 2   /* attn_sink_bwd_dq_kernel (attn_sink_bwd_deterministic) */
+#define ATTN_SINK_KERNEL_MERGE 3    /* attn_sink_merge_kernel (attn_sink_merge) */
+#define ATTN_SINK_KERNEL_COUNT 4
 
 /*
- * on != 0: from now on every launch of the two kernels above is bracketed by a
+ * on != 0: from now on every launch of the kernels above is bracketed by a
  * pair of CUDA events recorded on the launching stream (the events belong to
  * the library and are reused); on == 0 stops that.  Off at load.  Always
  * returns ATTN_SINK_OK.

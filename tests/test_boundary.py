@@ -183,9 +183,10 @@ def test_kernel_time_without_launches():
     # No timed launch has happened in this process: zero sums, OK status; a bad
     # id or a null pointer is an argument error.
     assert binding.attn_sink_kernel_timing(False) == OK
-    for k in (binding.ATTN_SINK_KERNEL_FWD, binding.ATTN_SINK_KERNEL_BWD_MAIN):
+    for k in (binding.ATTN_SINK_KERNEL_FWD, binding.ATTN_SINK_KERNEL_BWD_MAIN,
+              binding.ATTN_SINK_KERNEL_BWD_DQ, binding.ATTN_SINK_KERNEL_MERGE):
         assert binding.attn_sink_kernel_time(k) == (OK, 0.0, 0)
-    assert binding.attn_sink_kernel_time(2)[0] == INVALID
+    assert binding.attn_sink_kernel_time(4)[0] == INVALID
     assert binding.attn_sink_kernel_time(-1)[0] == INVALID
     assert binding.lib().attn_sink_kernel_time(0, None, None) == INVALID
 
