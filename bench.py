@@ -656,6 +656,10 @@ def main():
     ap.add_argument("--deterministic", action="store_true",
                     help="the same fwd+bwd step with the bitwise-reproducible backward "
                          "(attn_sink_bwd_deterministic); its own metric and config")
+    ap.add_argument("--sink-bf16", action="store_true",
+                    help="the same fwd+bwd step with the sink as a bf16 parameter whose "
+                         "gradient accumulates (attn_sink_fwd_ex / attn_sink_bwd_ex flags); its "
+                         "own metric and config")
     ap.add_argument("--chunks", type=int, default=0, metavar="C",
                     help="time the forward over C key chunks of every sequence plus the "
                          "sink-aware merge instead (one JSON line of its own)")
@@ -720,7 +724,12 @@ def main():
     out_res = torch.empty_like(q)
     lse = torch.empty((w.heads_q, sum(lengths)), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dsink = torch.empty_like(sink)
+    if args.sink_bf16:
+        # the sink as a bf16 training parameter; its gradient accumulates into dsink
+        sink = sink.to(torch.bfloat16)
+        dsink = torch.zeros_like(sink)
+    else:
+        dsink = torch.empty_like(sink)
     nws = binding.attn_sink_bwd_workspace_size(p)
     workspace = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
     fws = torch.empty(max(binding.attn_sink_fwd_workspace_size(p), 1), dtype=torch.uint8,
@@ -728,20 +737,31 @@ def main():
     cu_arg = cu if packed else None
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
+    if args.sink_bf16:
+        def fwd_fn(*a):
+            return binding.attn_sink_fwd_ex(a[0], binding.ATTN_SINK_FLAG_SINK_BF16, *a[1:])
+    else:
+        fwd_fn = binding.attn_sink_fwd
+
     def fwd():
-        st = binding.attn_sink_fwd(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse, fws,
-                                   fws.numel())
+        st = fwd_fn(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse, fws, fws.numel())
         if st:
             raise binding.AttnSinkError(st, "attn_sink_fwd")
 
     det = args.deterministic
     bwd_fn = binding.attn_sink_bwd_deterministic if det else binding.attn_sink_bwd
+    if args.sink_bf16:
+        bwd_flags = (binding.ATTN_SINK_FLAG_SINK_BF16 | binding.ATTN_SINK_FLAG_ACCUMULATE_DSINK
+                     | (binding.ATTN_SINK_FLAG_DETERMINISTIC if det else 0))
+
+        def bwd_fn(*a):
+            return binding.attn_sink_bwd_ex(a[0], bwd_flags, *a[1:])
 
     def bwd():
         st = bwd_fn(p, q, k, v, sink, cu_arg, cu_arg, out, out_res, lse, dout, dq, dk, dv, dsink,
                     workspace, workspace.numel())
         if st:
-            raise binding.AttnSinkError(st, bwd_fn.__name__)
+            raise binding.AttnSinkError(st, "attn_sink_bwd")
     timed_kernels = [binding.ATTN_SINK_KERNEL_FWD, binding.ATTN_SINK_KERNEL_BWD_MAIN]
     if det:
         timed_kernels.append(binding.ATTN_SINK_KERNEL_BWD_DQ)
@@ -837,8 +857,7 @@ def main():
         s_cmp.wait_event(in_ready[bsel])
         if i >= 2:
             s_cmp.wait_event(out_done[bsel])         # step i-2's results are on the host
-        st = binding.attn_sink_fwd(p, qb, kb, vb, sb, cu_arg, cu_arg, ob, orb, lb, fws,
-                                   fws.numel(), s_cmp)
+        st = fwd_fn(p, qb, kb, vb, sb, cu_arg, cu_arg, ob, orb, lb, fws, fws.numel(), s_cmp)
         if st == 0:
             st = bwd_fn(p, qb, kb, vb, sb, cu_arg, cu_arg, ob, orb, lb, dob, dqb, dkb, dvb, dsb,
                         workspace, workspace.numel(), s_cmp)
@@ -920,10 +939,15 @@ def main():
            "bwd_ceiling_tflops": ex2_per_s * 10 * w.head_dim / 1e12,
            "note": "fwd 4 d and bwd 10 d algorithmic flops per exponential"}
     config = config_dict(w, lengths, ws)
+    metric = METRIC
     if det:
         config["backward"] = "deterministic"
+        metric = DET_METRIC
+    if args.sink_bf16:
+        config["sink"] = "bf16 parameter, dsink accumulated"
+        metric = metric.replace("TFLOP/s", "TFLOP/s (bf16 sink, accumulated dsink)", 1)
     line = {
-        "metric": DET_METRIC if det else METRIC, "value": value, "unit": "TFLOP/s",
+        "metric": metric, "value": value, "unit": "TFLOP/s",
         "n_gpus": ws, "steps": n, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config,
