@@ -14,11 +14,14 @@
 //
 // One CTA per (query head h, sequence, 128-row query tile), longest first.
 // Warps 0-7 (thread = query row = TMEM lane; warps 4c..4c+3 take the key half
-// c, columns [64c, 64c+64) of a key tile) form dS from S and dP and write it
-// (fp16) over the S columns they have read; warp 8 issues TMA (Q, dO once; K/V
-// through a ring); warp 9 issues the MMAs: S and dP (M=N=128, fp16 from SMEM),
-// then dQ += dS K (M=128, N=64, K=128: dS from TMEM, K read MN-major).
-// TMEM: S 0-127, dP 128-255, dQ 256-319.
+// c, columns [64c, 64c+64) of a key tile) read S, signal that it has been read
+// (s_read), form P, then read dP and write dS (fp16) over the dP columns they
+// have read; warp 8 issues TMA (Q, dO once; K/V through a ring); warp 9 issues
+// the MMAs: S (M=N=128, fp16 from SMEM) as soon as the previous S has been
+// read, dQ += dS K (M=128, N=64, K=128: dS from TMEM, K read MN-major) once
+// dS is written, then dP (M=N=128) into the columns dQ has read.  So the next
+// tile's S is computed while this tile's dS is formed, and its dP while P of
+// the next tile is.  TMEM: S 0-127, dP 128-255, dQ 256-319.
 #pragma once
 #include <cuda_bf16.h>
 #include "fwd_kernel.cuh"
@@ -53,13 +56,14 @@ struct DqParams {
   int grad_fp32;
 };
 
-// dS of 32 keys of one query row (thread = row), fp16-packed.
+// P of 64 keys of one query row (thread = row), in place over S (fp32):
+//   P = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
+// with kMask, keys outside [jmin, jmax] exactly 0.
 template <bool kMask>
-__device__ __forceinline__ void dq_ds_chunk(const uint32_t* sr, const uint32_t* dr,
-                                            uint64_t sl2x2, uint64_t nlse2x2, uint64_t d2,
-                                            int j_first, int jmin, int jmax, uint32_t* dk) {
+__device__ __forceinline__ void dq_p_chunk(uint32_t* sr, uint64_t sl2x2, uint64_t nlse2x2,
+                                           int j_first, int jmin, int jmax) {
   #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
+  for (int e = 0; e < 64; e += 2) {
     const uint64_t x =
         ffma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, nlse2x2);
     float p0 = ex2_approx(f2_lo(x));
@@ -69,8 +73,19 @@ __device__ __forceinline__ void dq_ds_chunk(const uint32_t* sr, const uint32_t* 
       if (j < jmin || j > jmax) p0 = 0.0f;
       if (j + 1 < jmin || j + 1 > jmax) p1 = 0.0f;
     }
+    sr[e] = __float_as_uint(p0);
+    sr[e + 1] = __float_as_uint(p1);
+  }
+}
+
+// dS = P o (dP - D) of 32 keys of one query row, fp16-packed.
+__device__ __forceinline__ void dq_ds_chunk(const uint32_t* pr, const uint32_t* dr, uint64_t d2,
+                                            uint32_t* dk) {
+  #pragma unroll
+  for (int e = 0; e < 32; e += 2) {
     const uint64_t ds =
-        fmul2(f2(p0, p1), fsub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), d2));
+        fmul2(f2(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])),
+              fsub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), d2));
     dk[e >> 1] = pack_f16x2(f2_lo(ds), f2_hi(ds));
   }
 }
@@ -78,7 +93,7 @@ __device__ __forceinline__ void dq_ds_chunk(const uint32_t* sr, const uint32_t* 
 __global__ void __launch_bounds__(kDqThreads, 1)
 attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, s_full, p_full, dq_done;
+  __shared__ __align__(8) uint64_t q_full, s_full, s_read, dp_full, p_full, dq_done;
   __shared__ __align__(8) uint64_t kv_full[kDqStages], kv_empty[kDqStages];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -126,6 +141,8 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     abort_flag = 0;
     mbar_init(&q_full, 1);
     mbar_init(&s_full, 1);
+    mbar_init(&s_read, 2 * kBlockM);
+    mbar_init(&dp_full, 1);
     mbar_init(&p_full, 2 * kBlockM);
     mbar_init(&dq_done, 1);
     for (int s = 0; s < kDqStages; ++s) {
@@ -177,10 +194,10 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     }
   } else if (warp == kDqMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    // S(n+1) and dP(n+1) are issued right after dQ(n): the same thread issues
-    // them and tcgen05 MMAs execute in issue order, so dQ(n) has read dS(n)
-    // (over the S columns) before S(n+1) overwrites it; dP(n) was read by the
-    // compute warps before they arrived on p_full(n).
+    // Per key tile n, in issue order (tcgen05 MMAs of one thread run in that
+    // order): S(n+1) once S(n) has been read (s_read), dQ(n) once dS(n) is in
+    // the dP columns (p_full), then dP(n+1), which overwrites those columns
+    // after dQ(n) has read them.
     if (lane == 0) {
       const uint32_t id_s = make_idesc(kFmtF16, kBlockM, kBlockN, false, false);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
@@ -197,25 +214,34 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
           mma_ss(tmem + kDqColS, dQ0 + 2 * k, dK0 + st * kTileU + 2 * k, id_s, k > 0);
-        #pragma unroll
-        for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kDqColDP, dO0 + 2 * k, dV0 + st * kTileU + 2 * k, id_s, k > 0);
         mma_commit(&s_full);
         return true;
       };
+      auto issue_dp = [&](int n) {
+        const int st = n % kDqStages;
+        #pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_ss(tmem + kDqColDP, dO0 + 2 * k, dV0 + st * kTileU + 2 * k, id_s, k > 0);
+        mma_commit(&dp_full);
+      };
       bool ok = mbar_wait(&q_full, 0, &abort_flag) && issue_s(0);
+      if (ok) issue_dp(0);
       for (int n = 0; ok && n < num; ++n) {
         const int st = n % kDqStages;
+        // S(n+1) into the S columns the compute warps have read
+        if (n + 1 < num) {
+          if (!mbar_wait(&s_read, n & 1, &abort_flag) || !issue_s(n + 1)) { ok = false; break; }
+        }
         if (!mbar_wait(&p_full, n & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         // dQ += dS K: k-step kk covers keys [16 kk, 16 kk + 16) of the tile; the
-        // key half c = kk / 4 wrote its dS over S columns [64 c, 64 c + 32).
+        // key half c = kk / 4 wrote its dS over dP columns [64 c, 64 c + 32).
         #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + kDqColDQ, tmem + kDqColS + 64 * (kk >> 2) + 8 * (kk & 3),
+          mma_ts(tmem + kDqColDQ, tmem + kDqColDP + 64 * (kk >> 2) + 8 * (kk & 3),
                  dKmn + st * kTileU + 128 * kk, id_dq, (n > 0 || kk > 0));
-        mma_commit(&kv_empty[st]);
-        if (n + 1 < num) ok = issue_s(n + 1);
+        mma_commit(&kv_empty[st]);          // K(n) and V(n) have been read
+        if (n + 1 < num) issue_dp(n + 1);   // its stage landed before S(n+1) was issued
       }
       if (!ok) {
         abort_flag = 1;
@@ -246,19 +272,28 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
       const bool need_mask = (j0 + 64 > sp.nk) ||
                              (p.causal && (j0 + 63 > i0 + off ||
                                            (p.window > 0 && j0 <= tile_r1 + off - p.window)));
+      // S -> registers; its columns are then free for the next tile's S
+      uint32_t pr[64];
+      tmem_ld_x32(tmem + lane_base + kDqColS + 64 * c, pr);
+      tmem_ld_x32(tmem + lane_base + kDqColS + 64 * c + 32, pr + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&s_read);
+      // P in place (fp32), masked entries exactly 0
+      if (need_mask)
+        dq_p_chunk<true>(pr, sl2x2, nlse2x2, j0, jmin, jmax);
+      else
+        dq_p_chunk<false>(pr, sl2x2, nlse2x2, j0, jmin, jmax);
+      if (!mbar_wait_warp(&dp_full, it & 1, &abort_flag)) { ok = false; break; }
+      tc_fence_after();
       #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tmem + lane_base + kDqColS + 64 * c + cc, sr);
+        uint32_t dr[32], dk[16];
         tmem_ld_x32(tmem + lane_base + kDqColDP + 64 * c + cc, dr);
         tmem_ld_wait();
-        uint32_t dk[16];
-        if (need_mask)
-          dq_ds_chunk<true>(sr, dr, sl2x2, nlse2x2, d2, j0 + cc, jmin, jmax, dk);
-        else
-          dq_ds_chunk<false>(sr, dr, sl2x2, nlse2x2, d2, j0 + cc, jmin, jmax, dk);
-        // dS over S columns this thread has already read (chunk cc -> cc / 2)
-        tmem_st_x16(tmem + lane_base + kDqColS + 64 * c + (cc >> 1), dk);
+        dq_ds_chunk(pr + cc, dr, d2, dk);
+        // dS over dP columns this thread has already read (chunk cc -> cc / 2)
+        tmem_st_x16(tmem + lane_base + kDqColDP + 64 * c + (cc >> 1), dk);
       }
       tmem_st_wait();
       tc_fence_before();
