@@ -17,11 +17,12 @@
 // c, columns [64c, 64c+64) of a key tile) read S, signal that it has been read
 // (s_read), form P, then read dP and write dS (fp16) over the dP columns they
 // have read; warp 8 issues TMA (Q, dO once; K/V through a ring); warp 9 issues
-// the MMAs: S (M=N=128, fp16 from SMEM) as soon as the previous S has been
-// read, dQ += dS K (M=128, N=64, K=128: dS from TMEM, K read MN-major) once
-// dS is written, then dP (M=N=128) into the columns dQ has read.  So the next
-// tile's S is computed while this tile's dS is formed, and its dP while P of
-// the next tile is.  TMEM: S 0-127, dP 128-255, dQ 256-319.
+// the MMAs: S and dP of the next tile (M=N=128, fp16 from SMEM; dP into the
+// other of two buffers) as soon as this tile's S has been read, and
+// dQ += dS K (M=128, N=64, K=128: dS from TMEM, K read MN-major) once dS is
+// written.  So the next tile's S and dP are computed while this tile's P and
+// dS are formed.  TMEM: S 0-127, dP of even tiles 128-255, dQ 256-319, dP of
+// odd tiles 320-447.
 #pragma once
 #include <cuda_bf16.h>
 #include "fwd_kernel.cuh"
@@ -34,7 +35,9 @@ constexpr int kDqMmaWarp = 9;
 constexpr int kDqStages = 3;
 // Q, dO, kDqStages x (K, V)
 constexpr int kDqSmemBytes = 1024 + (int)kTileBytes * (2 + 2 * kDqStages);
-constexpr uint32_t kDqColS = 0, kDqColDP = 128, kDqColDQ = 256;
+constexpr uint32_t kDqColS = 0, kDqColDP = 128, kDqColDQ = 256, kDqColDP1 = 320;
+// dP (and, once formed, dS) of key tile n
+__host__ __device__ constexpr uint32_t dq_col_dp(int n) { return (n & 1) ? kDqColDP1 : kDqColDP; }
 
 struct DqParams {
   CUtensorMap tm_q;    // [T_q][H_q][64] fp16 copy of q
@@ -93,7 +96,12 @@ __device__ __forceinline__ void dq_ds_chunk(const uint32_t* pr, const uint32_t* 
 __global__ void __launch_bounds__(kDqThreads, 1)
 attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, s_full, s_read, dp_full, p_full, dq_done;
+  __shared__ __align__(8) uint64_t q_full, s_full, s_read, dq_done;
+  // Tile n completes dp_full[n & 1] (its dP) and p_full[n & 1] (its dS): dP(n+1)
+  // is issued before the compute warps wait for dP(n), and they may finish
+  // tile n+1 before the MMA thread waits for dS(n), so a single barrier could
+  // run two phases ahead of its waiter
+  __shared__ __align__(8) uint64_t dp_full[2], p_full[2];
   __shared__ __align__(8) uint64_t kv_full[kDqStages], kv_empty[kDqStages];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -142,8 +150,10 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     mbar_init(&q_full, 1);
     mbar_init(&s_full, 1);
     mbar_init(&s_read, 2 * kBlockM);
-    mbar_init(&dp_full, 1);
-    mbar_init(&p_full, 2 * kBlockM);
+    mbar_init(&dp_full[0], 1);
+    mbar_init(&dp_full[1], 1);
+    mbar_init(&p_full[0], 2 * kBlockM);
+    mbar_init(&p_full[1], 2 * kBlockM);
     mbar_init(&dq_done, 1);
     for (int s = 0; s < kDqStages; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -195,9 +205,9 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   } else if (warp == kDqMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     // Per key tile n, in issue order (tcgen05 MMAs of one thread run in that
-    // order): S(n+1) once S(n) has been read (s_read), dQ(n) once dS(n) is in
-    // the dP columns (p_full), then dP(n+1), which overwrites those columns
-    // after dQ(n) has read them.
+    // order): S(n+1) and dP(n+1) once S(n) has been read (s_read; dP(n+1)'s
+    // buffer last held dS(n-1), which dQ(n-1), issued before, has read), then
+    // dQ(n) once dS(n) is in its dP buffer (p_full).
     if (lane == 0) {
       const uint32_t id_s = make_idesc(kFmtF16, kBlockM, kBlockN, false, false);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
@@ -221,27 +231,29 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         const int st = n % kDqStages;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kDqColDP, dO0 + 2 * k, dV0 + st * kTileU + 2 * k, id_s, k > 0);
-        mma_commit(&dp_full);
+          mma_ss(tmem + dq_col_dp(n), dO0 + 2 * k, dV0 + st * kTileU + 2 * k, id_s, k > 0);
+        mma_commit(&dp_full[n & 1]);
       };
       bool ok = mbar_wait(&q_full, 0, &abort_flag) && issue_s(0);
       if (ok) issue_dp(0);
       for (int n = 0; ok && n < num; ++n) {
         const int st = n % kDqStages;
-        // S(n+1) into the S columns the compute warps have read
+        // S(n+1) into the S columns the compute warps have read, dP(n+1) into
+        // the other dP buffer (its stage landed before S(n+1) was issued)
         if (n + 1 < num) {
           if (!mbar_wait(&s_read, n & 1, &abort_flag) || !issue_s(n + 1)) { ok = false; break; }
+          issue_dp(n + 1);
         }
-        if (!mbar_wait(&p_full, n & 1, &abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         // dQ += dS K: k-step kk covers keys [16 kk, 16 kk + 16) of the tile; the
-        // key half c = kk / 4 wrote its dS over dP columns [64 c, 64 c + 32).
+        // key half c = kk / 4 wrote its dS over columns [64 c, 64 c + 32) of
+        // the tile's dP buffer.
         #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + kDqColDQ, tmem + kDqColDP + 64 * (kk >> 2) + 8 * (kk & 3),
+          mma_ts(tmem + kDqColDQ, tmem + dq_col_dp(n) + 64 * (kk >> 2) + 8 * (kk & 3),
                  dKmn + st * kTileU + 128 * kk, id_dq, (n > 0 || kk > 0));
         mma_commit(&kv_empty[st]);          // K(n) and V(n) have been read
-        if (n + 1 < num) issue_dp(n + 1);   // its stage landed before S(n+1) was issued
       }
       if (!ok) {
         abort_flag = 1;
@@ -284,20 +296,20 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         dq_p_chunk<true>(pr, sl2x2, nlse2x2, j0, jmin, jmax);
       else
         dq_p_chunk<false>(pr, sl2x2, nlse2x2, j0, jmin, jmax);
-      if (!mbar_wait_warp(&dp_full, it & 1, &abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&dp_full[it & 1], (it >> 1) & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
       #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t dr[32], dk[16];
-        tmem_ld_x32(tmem + lane_base + kDqColDP + 64 * c + cc, dr);
+        tmem_ld_x32(tmem + lane_base + dq_col_dp(it) + 64 * c + cc, dr);
         tmem_ld_wait();
         dq_ds_chunk(pr + cc, dr, d2, dk);
         // dS over dP columns this thread has already read (chunk cc -> cc / 2)
-        tmem_st_x16(tmem + lane_base + kDqColDP + 64 * c + (cc >> 1), dk);
+        tmem_st_x16(tmem + lane_base + dq_col_dp(it) + 64 * c + (cc >> 1), dk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive(&p_full[it & 1]);
     }
     // fin is warp-uniform (every wait above is), so the whole warp reaches the
     // .sync.aligned TMEM load; only the stores depend on the row.
