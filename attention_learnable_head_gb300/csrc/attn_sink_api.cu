@@ -955,8 +955,9 @@ int bwd_impl(const attn_sink_params* params, const void* q, const void* k, const
       return st;
     if ((st = encode_rows(&dp.tm_do, do16, g.total_q, params->heads_q, f16)) != ATTN_SINK_OK)
       return st;
-    if ((st = encode_rows(&dp.tm_k, kp, tk, hk, f16)) != ATTN_SINK_OK) return st;
-    if ((st = encode_rows(&dp.tm_v, vp, tk, hk, f16)) != ATTN_SINK_OK) return st;
+    // K and V come in steps of kDqKeys keys
+    if ((st = encode_rows(&dp.tm_k, kp, tk, hk, f16, kDqKeys)) != ATTN_SINK_OK) return st;
+    if ((st = encode_rows(&dp.tm_v, vp, tk, hk, f16, kDqKeys)) != ATTN_SINK_OK) return st;
     dp.cu_q = cu_seqlens_q;
     dp.cu_k = cu_seqlens_k;
     dp.LD = LD;

@@ -3,26 +3,28 @@
 // The main backward adds each key tile's dQ contribution into one fp32
 // accumulator in whatever order the hardware completes the reduce-adds, so dQ
 // is not bitwise reproducible.  This kernel computes dQ query-stationary
-// instead, with a fixed summation order over the key tiles:
+// instead, with a fixed summation order over the keys:
 //   S  = Q K^T,  P = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
 //   dP = dO V^T, dS = P o (dP - D)
-//   dQ = scale * sum_j dS_j K_j          (key tiles in increasing order)
+//   dQ = scale * sum_j dS_j K_j          (key steps in increasing order)
 // (the explicit backward of the concat-sink softmax; the sink adds no key row,
 // so it enters dQ only through lse and D).  It costs two more products than
 // the fused backward (S and dP are computed again): the price of
 // reproducibility.
 //
-// One CTA per (query head h, sequence, 128-row query tile), longest first.
-// Warps 0-7 (thread = query row = TMEM lane; warps 4c..4c+3 take the key half
-// c, columns [64c, 64c+64) of a key tile) read S, signal that it has been read
+// One CTA per (query head h, sequence, 128-row query tile), longest first,
+// two CTAs per SM, stepping over the visible keys 64 at a time.  Warps 0-7
+// (thread = query row = TMEM lane; warps 4c..4c+3 take the key half c, columns
+// [32c, 32c+32) of a step) read S, signal that it has been read
 // (s_read), form P, then read dP and write dS (fp16) over the dP columns they
 // have read; warp 8 issues TMA (Q, dO once; K/V through a ring); warp 9 issues
-// the MMAs: S and dP of the next tile (M=N=128, fp16 from SMEM; dP into the
-// other of two buffers) as soon as this tile's S has been read, and
-// dQ += dS K (M=128, N=64, K=128: dS from TMEM, K read MN-major) once dS is
-// written.  So the next tile's S and dP are computed while this tile's P and
-// dS are formed.  TMEM: S 0-127, dP of even tiles 128-255, dQ 256-319, dP of
-// odd tiles 320-447.
+// the MMAs: S and dP of the next step (M=128, N=64, fp16 from SMEM; dP into
+// the other of two buffers) as soon as this step's S has been read, and
+// dQ += dS K (M=128, N=64, K=64: dS from TMEM, K read MN-major) once dS is
+// written.  So the next step's S and dP are computed while this step's P and
+// dS are formed, and the second CTA of the SM fills the remaining gaps.
+// TMEM (256 columns): S 0-63, dP of even steps 64-127, dQ 128-191, dP of odd
+// steps 192-255.
 #pragma once
 #include <cuda_bf16.h>
 #include "fwd_kernel.cuh"
@@ -32,11 +34,14 @@ namespace attn_sink {
 constexpr int kDqThreads = 320;
 constexpr int kDqTmaWarp = 8;
 constexpr int kDqMmaWarp = 9;
-constexpr int kDqStages = 3;
-// Q, dO, kDqStages x (K, V)
-constexpr int kDqSmemBytes = 1024 + (int)kTileBytes * (2 + 2 * kDqStages);
-constexpr uint32_t kDqColS = 0, kDqColDP = 128, kDqColDQ = 256, kDqColDP1 = 320;
-// dP (and, once formed, dS) of key tile n
+constexpr int kDqKeys = 64;                                   // keys per step
+constexpr uint32_t kDqKvBytes = kDqKeys * kHeadDim * 2;       // 8 KB K or V tile
+constexpr int kDqStages = 4;
+// Q, dO, kDqStages x (K, V): ~99 KB, two CTAs per SM
+constexpr int kDqSmemBytes = 1024 + 2 * (int)kTileBytes + kDqStages * 2 * (int)kDqKvBytes;
+constexpr uint32_t kDqTmemCols = 256;
+constexpr uint32_t kDqColS = 0, kDqColDP = 64, kDqColDQ = 128, kDqColDP1 = 192;
+// dP (and, once formed, dS) of key step n
 __host__ __device__ constexpr uint32_t dq_col_dp(int n) { return (n & 1) ? kDqColDP1 : kDqColDP; }
 
 struct DqParams {
@@ -59,14 +64,14 @@ struct DqParams {
   int grad_fp32;
 };
 
-// P of 64 keys of one query row (thread = row), in place over S (fp32):
+// P of 32 keys of one query row (thread = row), in place over S (fp32):
 //   P = exp2(S * scale * log2 e - lse * log2 e)   (lse includes the sink)
 // with kMask, keys outside [jmin, jmax] exactly 0.
 template <bool kMask>
 __device__ __forceinline__ void dq_p_chunk(uint32_t* sr, uint64_t sl2x2, uint64_t nlse2x2,
                                            int j_first, int jmin, int jmax) {
   #pragma unroll
-  for (int e = 0; e < 64; e += 2) {
+  for (int e = 0; e < 32; e += 2) {
     const uint64_t x =
         ffma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, nlse2x2);
     float p0 = ex2_approx(f2_lo(x));
@@ -93,13 +98,13 @@ __device__ __forceinline__ void dq_ds_chunk(const uint32_t* pr, const uint32_t* 
   }
 }
 
-__global__ void __launch_bounds__(kDqThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 2)
 attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, s_full, s_read, dq_done;
-  // Tile n completes dp_full[n & 1] (its dP) and p_full[n & 1] (its dS): dP(n+1)
+  // Step n completes dp_full[n & 1] (its dP) and p_full[n & 1] (its dS): dP(n+1)
   // is issued before the compute warps wait for dP(n), and they may finish
-  // tile n+1 before the MMA thread waits for dS(n), so a single barrier could
+  // step n+1 before the MMA thread waits for dS(n), so a single barrier could
   // run two phases ahead of its waiter
   __shared__ __align__(8) uint64_t dp_full[2], p_full[2];
   __shared__ __align__(8) uint64_t kv_full[kDqStages], kv_empty[kDqStages];
@@ -116,8 +121,15 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int off = sp.nk - sp.nq;                          // bottom-right alignment
-  const KeyRange kr = key_tiles(i0, min(i0 + kBlockM, sp.nq) - 1, sp, off, p.causal, p.window);
-  const int num = kr.num;
+  // the keys the tile's rows can see, in steps of 64
+  const int tile_r1 = min(i0 + kBlockM, sp.nq) - 1;
+  int kv_lo = 0, kv_hi = sp.nk;
+  if (p.causal) {
+    kv_hi = min(sp.nk, tile_r1 + off + 1);
+    if (p.window > 0) kv_lo = max(0, i0 + off - p.window + 1);
+  }
+  const int lo64 = kv_lo / kDqKeys;
+  const int num = kv_hi > kv_lo ? (kv_hi + kDqKeys - 1) / kDqKeys - lo64 : 0;
 
   if (num == 0) {
     // No row of this tile sees a key: dQ = 0.
@@ -142,8 +154,8 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sdO = sQ + kTileBytes;
-  uint8_t* sK = sdO + kTileBytes;                         // kDqStages tiles
-  uint8_t* sV = sK + kDqStages * kTileBytes;              // kDqStages tiles
+  uint8_t* sK = sdO + kTileBytes;                         // kDqStages 64-key tiles
+  uint8_t* sV = sK + kDqStages * kDqKvBytes;              // kDqStages 64-key tiles
 
   if (tid == 0) {
     abort_flag = 0;
@@ -162,7 +174,7 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     fence_mbarrier_init();
   }
   if (warp == kDqMmaWarp) {
-    tmem_alloc(&tmem_base_sh, 512);
+    tmem_alloc(&tmem_base_sh, kDqTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -189,10 +201,10 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
           atomicCAS(p.err, 0, DEVERR_TIMEOUT_BWD + 5);
           break;
         }
-        const int row = sp.k0 + (kr.lo + it) * kBlockN;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTileBytes);
-        tma_load_3d(&p.tm_k, &kv_full[st], sK + st * kTileBytes, 0, g, row);
-        tma_load_3d(&p.tm_v, &kv_full[st], sV + st * kTileBytes, 0, g, row);
+        const int row = sp.k0 + (lo64 + it) * kDqKeys;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kDqKvBytes);
+        tma_load_3d(&p.tm_k, &kv_full[st], sK + st * kDqKvBytes, 0, g, row);
+        tma_load_3d(&p.tm_v, &kv_full[st], sV + st * kDqKvBytes, 0, g, row);
         issued = it + 1;
       }
       if (abort_flag) {
@@ -204,26 +216,26 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     }
   } else if (warp == kDqMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    // Per key tile n, in issue order (tcgen05 MMAs of one thread run in that
+    // Per key step n, in issue order (tcgen05 MMAs of one thread run in that
     // order): S(n+1) and dP(n+1) once S(n) has been read (s_read; dP(n+1)'s
     // buffer last held dS(n-1), which dQ(n-1), issued before, has read), then
     // dQ(n) once dS(n) is in its dP buffer (p_full).
     if (lane == 0) {
-      const uint32_t id_s = make_idesc(kFmtF16, kBlockM, kBlockN, false, false);
+      const uint32_t id_s = make_idesc(kFmtF16, kBlockM, kDqKeys, false, false);
       const uint32_t id_dq = make_idesc(kFmtF16, kBlockM, kHeadDim, false, true);
       const uint64_t dQ0 = make_sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dO0 = make_sdesc_sw128(smem_u32(sdO), 16, 1024);
       const uint64_t dK0 = make_sdesc_sw128(smem_u32(sK), 16, 1024);       // K-major
       const uint64_t dKmn = make_sdesc_sw128(smem_u32(sK), 16384, 1024);   // MN-major
       const uint64_t dV0 = make_sdesc_sw128(smem_u32(sV), 16, 1024);
-      constexpr uint32_t kTileU = kTileBytes >> 4;
+      constexpr uint32_t kKvU = kDqKvBytes >> 4;
       auto issue_s = [&](int n) -> bool {
         const int st = n % kDqStages;
         if (!mbar_wait(&kv_full[st], (n / kDqStages) & 1, &abort_flag)) return false;
         tc_fence_after();
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + kDqColS, dQ0 + 2 * k, dK0 + st * kTileU + 2 * k, id_s, k > 0);
+          mma_ss(tmem + kDqColS, dQ0 + 2 * k, dK0 + st * kKvU + 2 * k, id_s, k > 0);
         mma_commit(&s_full);
         return true;
       };
@@ -231,7 +243,7 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         const int st = n % kDqStages;
         #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
-          mma_ss(tmem + dq_col_dp(n), dO0 + 2 * k, dV0 + st * kTileU + 2 * k, id_s, k > 0);
+          mma_ss(tmem + dq_col_dp(n), dO0 + 2 * k, dV0 + st * kKvU + 2 * k, id_s, k > 0);
         mma_commit(&dp_full[n & 1]);
       };
       bool ok = mbar_wait(&q_full, 0, &abort_flag) && issue_s(0);
@@ -246,13 +258,13 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         }
         if (!mbar_wait(&p_full[n & 1], (n >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // dQ += dS K: k-step kk covers keys [16 kk, 16 kk + 16) of the tile; the
-        // key half c = kk / 4 wrote its dS over columns [64 c, 64 c + 32) of
-        // the tile's dP buffer.
+        // dQ += dS K: k-step kk covers keys [16 kk, 16 kk + 16) of the step; the
+        // key half c = kk / 2 wrote its dS over columns [32 c, 32 c + 16) of
+        // the step's dP buffer.
         #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + kDqColDQ, tmem + dq_col_dp(n) + 64 * (kk >> 2) + 8 * (kk & 3),
-                 dKmn + st * kTileU + 128 * kk, id_dq, (n > 0 || kk > 0));
+        for (int kk = 0; kk < kDqKeys / 16; ++kk)
+          mma_ts(tmem + kDqColDQ, tmem + dq_col_dp(n) + 32 * (kk >> 1) + 8 * (kk & 1),
+                 dKmn + st * kKvU + 128 * kk, id_dq, (n > 0 || kk > 0));
         mma_commit(&kv_empty[st]);          // K(n) and V(n) have been read
       }
       if (!ok) {
@@ -275,19 +287,17 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
     const uint64_t sl2x2 = f2(sl2, sl2), nlse2x2 = f2(ld.x, ld.x), d2 = f2(ld.y, ld.y);
     const int jmax = p.causal ? min(sp.nk - 1, i + off) : sp.nk - 1;   // inclusive
     const int jmin = (p.causal && p.window > 0) ? i + off - p.window + 1 : 0;
-    const int tile_r1 = min(i0 + kBlockM, sp.nq) - 1;
     bool ok = true;
     for (int it = 0; it < num; ++it) {
       if (!mbar_wait_warp(&s_full, it & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const int j0 = (kr.lo + it) * kBlockN + 64 * c;          // first key of this half
-      const bool need_mask = (j0 + 64 > sp.nk) ||
-                             (p.causal && (j0 + 63 > i0 + off ||
+      const int j0 = (lo64 + it) * kDqKeys + 32 * c;           // first key of this half
+      const bool need_mask = (j0 + 32 > sp.nk) ||
+                             (p.causal && (j0 + 31 > i0 + off ||
                                            (p.window > 0 && j0 <= tile_r1 + off - p.window)));
-      // S -> registers; its columns are then free for the next tile's S
-      uint32_t pr[64];
-      tmem_ld_x32(tmem + lane_base + kDqColS + 64 * c, pr);
-      tmem_ld_x32(tmem + lane_base + kDqColS + 64 * c + 32, pr + 32);
+      // S -> registers; its columns are then free for the next step's S
+      uint32_t pr[32];
+      tmem_ld_x32(tmem + lane_base + kDqColS + 32 * c, pr);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&s_read);
@@ -298,14 +308,13 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
         dq_p_chunk<false>(pr, sl2x2, nlse2x2, j0, jmin, jmax);
       if (!mbar_wait_warp(&dp_full[it & 1], (it >> 1) & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      #pragma unroll
-      for (int cc = 0; cc < 64; cc += 32) {
+      {
         uint32_t dr[32], dk[16];
-        tmem_ld_x32(tmem + lane_base + dq_col_dp(it) + 64 * c + cc, dr);
+        tmem_ld_x32(tmem + lane_base + dq_col_dp(it) + 32 * c, dr);
         tmem_ld_wait();
-        dq_ds_chunk(pr + cc, dr, d2, dk);
-        // dS over dP columns this thread has already read (chunk cc -> cc / 2)
-        tmem_st_x16(tmem + lane_base + dq_col_dp(it) + 64 * c + (cc >> 1), dk);
+        dq_ds_chunk(pr, dr, d2, dk);
+        // dS (16 packed columns) over the dP columns this thread has read
+        tmem_st_x16(tmem + lane_base + dq_col_dp(it) + 32 * c, dk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -353,7 +362,7 @@ attn_sink_bwd_dq_kernel(const __grid_constant__ DqParams p) {
   __syncthreads();
   if (warp == kDqMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kDqTmemCols);
   }
 }
 
